@@ -1,0 +1,108 @@
+"""ctypes front end of the C oracle (``pa_oracle.c``).
+
+TEST INFRASTRUCTURE: only the tests, the smoke check and the benchmark's
+CPU-baseline leg may call it.  Inputs are numpy arrays; nothing here touches
+a GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import numpy as np
+
+from .build import LIB, build_oracle
+
+_lib: Optional[ctypes.CDLL] = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            build_oracle()
+        L = ctypes.CDLL(LIB)
+        L.pa_oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        L.pa_oracle_half_to_double.restype = ctypes.c_double
+        L.pa_oracle_locate_kv.argtypes = [_I64, _P, _I, ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.POINTER(ctypes.c_int32)]
+        L.pa_oracle_locate_kv.restype = _I
+        L.pa_oracle_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I]
+        L.pa_oracle_reshape_and_cache.restype = _I
+        L.pa_oracle_decode.argtypes = [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I64,
+                                       ctypes.c_double, _I]
+        L.pa_oracle_decode.restype = _I
+        L.pa_oracle_max_threads.argtypes = []
+        L.pa_oracle_max_threads.restype = _I
+        _lib = L
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+def half_to_double(bits: int) -> float:
+    return lib().pa_oracle_half_to_double(int(bits) & 0xFFFF)
+
+
+def locate_kv(logical_token_idx: int, block_table, block_size: int) -> Tuple[int, int]:
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    phys = ctypes.c_int32()
+    off = ctypes.c_int32()
+    rc = lib().pa_oracle_locate_kv(int(logical_token_idx), _ptr(bt), int(block_size),
+                                   ctypes.byref(phys), ctypes.byref(off))
+    if rc:
+        raise OracleError(f"locate_kv failed ({rc})")
+    return int(phys.value), int(off.value)
+
+
+def reshape_and_cache(key: np.ndarray, value: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                      slot_mapping: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Return updated copies of the pools (inputs are left untouched)."""
+    assert key.dtype == np.float16 and value.dtype == np.float16
+    kc = np.ascontiguousarray(k_cache).copy()
+    vc = np.ascontiguousarray(v_cache).copy()
+    N, B, Hk, d = kc.shape
+    key = np.ascontiguousarray(key)
+    value = np.ascontiguousarray(value)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    rc = lib().pa_oracle_reshape_and_cache(_ptr(key), _ptr(value), _ptr(kc), _ptr(vc), _ptr(sm),
+                                           int(sm.size), N, B, Hk, d)
+    if rc:
+        raise OracleError(f"reshape_and_cache precondition failed ({rc})")
+    return kc, vc
+
+
+def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables: np.ndarray,
+           context_lens: np.ndarray, scale: float, num_threads: int = 0) -> np.ndarray:
+    """float64 attention output [S, H, d]."""
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    k_cache = np.ascontiguousarray(k_cache)
+    v_cache = np.ascontiguousarray(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    S, H, d = q.shape
+    N, B, Hk, d2 = k_cache.shape
+    assert d == d2 and bt.shape[0] == S and cl.shape == (S,)
+    out = np.zeros((S, H, d), dtype=np.float64)
+    rc = lib().pa_oracle_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt),
+                                int(bt.shape[1]), _ptr(cl), S, H, Hk, d, B, N, float(scale),
+                                int(num_threads))
+    if rc:
+        raise OracleError(f"decode precondition failed ({rc})")
+    return out
+
+
+def max_threads() -> int:
+    return int(lib().pa_oracle_max_threads())

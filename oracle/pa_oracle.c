@@ -1,0 +1,227 @@
+/*
+ * pa_oracle.c -- plain float64 CPU oracle for paged KV-cache decode attention.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg load this library.  It shares no code, header or constant
+ * with the CUDA library: it has its own float16 decoding, its own address
+ * translation and its own attention, all written for clarity, not speed.
+ *
+ * What it computes (sources, by page title and section):
+ *
+ *  - Address translation, "locate_kv": a logical token position t maps to
+ *    logical block t / block_size and slot t % block_size, and the block
+ *    table turns the logical block into a physical block id.  ("Unveiling the
+ *    NVIDIA driver stack: GPU page tables and vLLM PagedAttention",
+ *    section 6, "code view"; worked example: position 37 with table
+ *    [7, 42, 9, 103] lands in physical block 9, slot 5.)
+ *
+ *  - The cache write: a new token's K and V go into the next free slot of the
+ *    sequence's last block.  The slot is given here as one flat number
+ *    slot = physical_block * block_size + offset; negative slots are padding
+ *    and are skipped.  ("vLLM PagedAttention source walk-through", section
+ *    3.2, append_token and _write_kv_to_block; "Efficient Memory Management
+ *    for LLM Serving with PagedAttention -- in-depth reading", sections 3.2
+ *    and 3.4, step 1.)
+ *
+ *  - Decode attention: paged attention is mathematically the same as ordinary
+ *    attention over the sequence's keys and values ("in-depth reading",
+ *    section 4.4; "walk-through", section 3.4).  So the oracle gathers the
+ *    ctx valid keys and values of a sequence through the block table into
+ *    contiguous arrays and applies the textbook softmax: scores
+ *    x_i = scale * q . k_i, m = max_i x_i, p_i = exp(x_i - m) / sum_j
+ *    exp(x_j - m), out = sum_i p_i v_i (the two-pass form the walk-through's
+ *    section 3.4 calls "traditional").  Query head h reads KV head
+ *    h / (num_heads / num_kv_heads) (grouped-query attention with consecutive
+ *    groups; the pages do not fix the mapping).
+ *
+ *  The K and V pools have the layout [num_blocks, block_size, num_kv_heads,
+ *  head_dim]; values are IEEE binary16 bit patterns.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG 1
+#define ORACLE_BAD_BLOCK 2
+#define ORACLE_BAD_CONTEXT 3
+#define ORACLE_DUPLICATE_SLOT 4
+#define ORACLE_BAD_SLOT 5
+#define ORACLE_NO_MEMORY 6
+
+/* IEEE 754 binary16 -> double, from the format's definition: 1 sign bit,
+ * 5 exponent bits (bias 15), 10 fraction bits.  Exponent 0 encodes zero and
+ * subnormals (fraction * 2^-24), exponent 31 encodes infinities and NaNs. */
+double pa_oracle_half_to_double(uint16_t bits) {
+    const int sign = (bits >> 15) & 1;
+    const int expo = (bits >> 10) & 0x1f;
+    const int frac = bits & 0x3ff;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -24);
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + frac), expo - 25);
+    }
+    return sign ? -v : v;
+}
+
+/* Logical token position -> (physical block, slot in block). */
+int pa_oracle_locate_kv(int64_t logical_token_idx, const int32_t* block_table, int block_size,
+                        int32_t* physical_block, int32_t* offset_in_block) {
+    if (logical_token_idx < 0 || block_size <= 0 || !block_table) return ORACLE_BAD_ARG;
+    const int64_t logical_block = logical_token_idx / block_size;
+    *offset_in_block = (int32_t)(logical_token_idx % block_size);
+    *physical_block = block_table[logical_block];
+    return ORACLE_OK;
+}
+
+static int cmp_i64(const void* a, const void* b) {
+    const int64_t x = *(const int64_t*)a, y = *(const int64_t*)b;
+    return (x > y) - (x < y);
+}
+
+/* Write each new token's K and V rows (all KV heads) into its slot.  The
+ * pools are updated in place; slots < 0 are skipped; slots must be distinct. */
+int pa_oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint16_t* k_cache,
+                                uint16_t* v_cache, const int64_t* slot_mapping, int64_t num_tokens,
+                                int64_t num_blocks, int block_size, int num_kv_heads, int head_dim) {
+    if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return ORACLE_BAD_ARG;
+    if (num_tokens == 0) return ORACLE_OK;
+    /* precondition: distinct non-negative slots */
+    int64_t* sorted = (int64_t*)malloc(sizeof(int64_t) * (size_t)num_tokens);
+    if (!sorted) return ORACLE_NO_MEMORY;
+    memcpy(sorted, slot_mapping, sizeof(int64_t) * (size_t)num_tokens);
+    qsort(sorted, (size_t)num_tokens, sizeof(int64_t), cmp_i64);
+    for (int64_t i = 1; i < num_tokens; ++i) {
+        if (sorted[i] >= 0 && sorted[i] == sorted[i - 1]) {
+            free(sorted);
+            return ORACLE_DUPLICATE_SLOT;
+        }
+    }
+    free(sorted);
+    const int64_t row = (int64_t)num_kv_heads * head_dim; /* elements of one token, all heads */
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * block_size) return ORACLE_BAD_SLOT;
+        const int64_t block = slot / block_size;
+        const int64_t off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            for (int j = 0; j < head_dim; ++j) {
+                const int64_t src = t * row + (int64_t)h * head_dim + j;
+                const int64_t dst = ((block * block_size + off) * num_kv_heads + h) * head_dim + j;
+                k_cache[dst] = key[src];
+                v_cache[dst] = value[src];
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* One (sequence, query head): gather, score, softmax, weighted sum. */
+static int decode_one(double* out, const uint16_t* q_row, const uint16_t* k_cache,
+                      const uint16_t* v_cache, const int32_t* table, int max_blocks_per_seq,
+                      int ctx, int num_kv_heads, int kv_head, int head_dim, int block_size,
+                      int64_t num_blocks, double scale) {
+    if (ctx < 0 || (int64_t)ctx > (int64_t)max_blocks_per_seq * block_size) return ORACLE_BAD_CONTEXT;
+    for (int j = 0; j < head_dim; ++j) out[j] = 0.0;
+    if (ctx == 0) return ORACLE_OK; /* an empty sequence yields zeros */
+
+    double* K = (double*)malloc(sizeof(double) * (size_t)ctx * head_dim);
+    double* V = (double*)malloc(sizeof(double) * (size_t)ctx * head_dim);
+    double* x = (double*)malloc(sizeof(double) * (size_t)ctx);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    if (!K || !V || !x || !qd) {
+        free(K); free(V); free(x); free(qd);
+        return ORACLE_NO_MEMORY;
+    }
+    int rc = ORACLE_OK;
+    /* gather the valid keys and values into contiguous [ctx, head_dim] arrays */
+    for (int i = 0; i < ctx && rc == ORACLE_OK; ++i) {
+        int32_t phys, off;
+        pa_oracle_locate_kv(i, table, block_size, &phys, &off);
+        if (phys < 0 || (int64_t)phys >= num_blocks) {
+            rc = ORACLE_BAD_BLOCK;
+            break;
+        }
+        const int64_t base = (((int64_t)phys * block_size + off) * num_kv_heads + kv_head) * head_dim;
+        for (int j = 0; j < head_dim; ++j) {
+            K[(size_t)i * head_dim + j] = pa_oracle_half_to_double(k_cache[base + j]);
+            V[(size_t)i * head_dim + j] = pa_oracle_half_to_double(v_cache[base + j]);
+        }
+    }
+    if (rc == ORACLE_OK) {
+        for (int j = 0; j < head_dim; ++j) qd[j] = pa_oracle_half_to_double(q_row[j]);
+        /* pass 1: scores and their maximum */
+        double m = -INFINITY;
+        for (int i = 0; i < ctx; ++i) {
+            double dot = 0.0;
+            for (int j = 0; j < head_dim; ++j) dot += qd[j] * K[(size_t)i * head_dim + j];
+            x[i] = scale * dot;
+            if (x[i] > m) m = x[i];
+        }
+        /* pass 2: normalised weights and the weighted sum of values */
+        double denom = 0.0;
+        for (int i = 0; i < ctx; ++i) {
+            x[i] = exp(x[i] - m);
+            denom += x[i];
+        }
+        for (int i = 0; i < ctx; ++i) {
+            const double p = x[i] / denom;
+            for (int j = 0; j < head_dim; ++j) out[j] += p * V[(size_t)i * head_dim + j];
+        }
+    }
+    free(K); free(V); free(x); free(qd);
+    return rc;
+}
+
+/* Decode attention for every (sequence, query head).
+ * out: [num_seqs, num_heads, head_dim] float64; q: [num_seqs, num_heads,
+ * head_dim] binary16; block_tables: [num_seqs, max_blocks_per_seq].
+ * num_threads <= 0 uses every available thread. */
+int pa_oracle_decode(double* out, const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                     int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                     int64_t num_blocks, double scale, int num_threads) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || num_heads % num_kv_heads != 0)
+        return ORACLE_BAD_ARG;
+    const int group = num_heads / num_kv_heads;
+    const int64_t work = (int64_t)num_seqs * num_heads;
+    int rc = ORACLE_OK;
+#ifdef _OPENMP
+    const int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+#endif
+    for (int64_t w = 0; w < work; ++w) {
+        const int s = (int)(w / num_heads);
+        const int h = (int)(w % num_heads);
+        const int r = decode_one(out + w * head_dim, q + w * head_dim, k_cache, v_cache,
+                                 block_tables + (int64_t)s * max_blocks_per_seq, max_blocks_per_seq,
+                                 context_lens[s], num_kv_heads, h / group, head_dim, block_size,
+                                 num_blocks, scale);
+        if (r != ORACLE_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            rc = r;
+        }
+    }
+    return rc;
+}
+
+/* Threads an OpenMP region of this library would use by default. */
+int pa_oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,436 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Every check here runs on the CPU.  Sources are the pages' worked example and
+byte sizes (stored under tests/golden/ with their citations), closed forms,
+invariants that paged attention must keep, and an independent library
+attention (torch's scaled_dot_product_attention in float64).  The last test
+plants mistakes in a copy of the oracle and shows that the pins catch them.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import c_oracle, numpy_oracle
+from paged_kv_cache_173_gb300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _written(batch):
+    """Pools after the new tokens are written (oracle write path)."""
+    return c_oracle.reshape_and_cache(batch.key, batch.value, batch.k_cache, batch.v_cache,
+                                      batch.slot_mapping)
+
+
+def _sdpa_contiguous(q, K, V, scale, group):
+    """Library attention of one sequence: q [H, d], K/V [n, Hk, d] (float64)."""
+    qt = torch.from_numpy(np.asarray(q, dtype=np.float64))[None, :, None, :]
+    kt = torch.from_numpy(np.asarray(K, dtype=np.float64)).permute(1, 0, 2)
+    vt = torch.from_numpy(np.asarray(V, dtype=np.float64)).permute(1, 0, 2)
+    kt = kt.repeat_interleave(group, dim=0)[None]
+    vt = vt.repeat_interleave(group, dim=0)[None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=float(scale))
+    return o[0, :, 0, :].numpy()
+
+
+# --------------------------------------------------------------------------
+# float16 decoding
+# --------------------------------------------------------------------------
+
+def test_half_decoding_matches_numpy_for_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([c_oracle.half_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# --------------------------------------------------------------------------
+# the pages' worked numbers
+# --------------------------------------------------------------------------
+
+def test_locate_kv_worked_example():
+    g = _golden("locate_kv_example.json")
+    want = (g["expected_physical_block"], g["expected_offset"])
+    assert c_oracle.locate_kv(g["logical_token_idx"], g["block_table"], g["block_size"]) == want
+    assert numpy_oracle.locate_kv(g["logical_token_idx"], g["block_table"], g["block_size"]) == want
+
+
+def test_locate_kv_walks_every_slot_once():
+    table = [7, 42, 9, 103]
+    seen = [c_oracle.locate_kv(t, table, 16) for t in range(64)]
+    assert len(set(seen)) == 64
+    assert [b for b, _ in seen[::16]] == table
+    assert all(off == t % 16 for t, (_, off) in enumerate(seen))
+
+
+def test_byte_accounting_matches_the_pages():
+    g = _golden("kv_byte_sizes.json")
+    t = g["per_token_per_layer"]
+    per_tok = workloads.kv_bytes_per_token(t["num_kv_heads"], t["head_dim"], t["elem_bytes"])
+    assert per_tok == t["bytes_per_token_per_layer"]
+    assert per_tok * t["num_layers"] == t["kib_per_token_all_layers"] * 1024
+    unit = g["per_request_table"]["unit_bytes"]
+    for row in g["per_request_table"]["rows"]:
+        req = row["seq_len"] * per_tok * t["num_layers"] / unit
+        assert abs(req - row["per_request"]) <= 0.05 * row["per_request"]
+        assert abs(8 * req - row["batch8"]) <= 0.05 * row["batch8"]
+        assert abs(32 * req - row["batch32"]) <= 0.05 * row["batch32"]
+    b = g["per_block"]
+    half = b["block_size"] * workloads.kv_bytes_per_token(b["num_kv_heads"], b["head_dim"], b["elem_bytes"]) // 2
+    assert half == b["k_bytes"] == b["v_bytes"]
+    assert 2 * half == b["kv_bytes"]
+    bt = g["block_table_size"]
+    entries = bt["seq_len"] // bt["block_size"]
+    assert entries == bt["entries"]
+    assert entries * bt["entry_bytes"] == bt["bytes_per_request"]
+    assert abs(bt["requests"] * entries * bt["entry_bytes"] / 1e6 - bt["mb_100_requests"]) < 0.05
+    assert abs(bt["requests"] * 2 * entries * bt["entry_bytes"] / 1e6 - bt["mb_100_requests_block8"]) < 0.1
+    w = g["waste_bound"]
+    B = w["block_size"]
+    wastes = [(-n) % B for n in range(1, 10 * B + 1)]
+    assert max(wastes) == w["max_waste_tokens"] == B - 1
+    assert abs(np.mean(wastes) - (B - 1) / 2) < 1e-12
+    assert abs((B - 1) / 2 - w["mean_waste_tokens"]) <= 0.5
+    assert w["mean_waste_tokens"] * per_tok // 1024 == w["mean_waste_kib_at_4kib_per_token"]
+
+
+def test_algorithmic_bytes_of_the_tiny_batch():
+    b = workloads.tiny()
+    # 69 valid tokens x 4 KV heads x 64 dims x (K + V) x 2 bytes
+    assert workloads.algorithmic_kv_bytes(b) == 69 * 4 * 64 * 2 * 2
+
+
+# --------------------------------------------------------------------------
+# decode against an independent attention
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("group", [1, 4, 8])
+def test_identity_table_equals_library_attention(group):
+    rng = np.random.default_rng(11)
+    B, Hk, d = 16, 2, 64
+    H = Hk * group
+    ctx = [1, 15, 16, 17, 40]
+    nblk = [(c + B - 1) // B for c in ctx]
+    N = sum(nblk)
+    tables = np.full((len(ctx), max(nblk)), -1, np.int32)
+    start = 0
+    for s, n in enumerate(nblk):
+        tables[s, :n] = np.arange(start, start + n)
+        start += n
+    kc = rng.standard_normal((N, B, Hk, d), dtype=np.float32).astype(np.float16)
+    vc = rng.standard_normal((N, B, Hk, d), dtype=np.float32).astype(np.float16)
+    q = rng.standard_normal((len(ctx), H, d), dtype=np.float32).astype(np.float16)
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    got = c_oracle.decode(q, kc, vc, tables, np.array(ctx, np.int32), scale)
+    # identity table: a sequence's tokens are a contiguous run of the pool
+    flatk = kc.reshape(N * B, Hk, d).astype(np.float64)
+    flatv = vc.reshape(N * B, Hk, d).astype(np.float64)
+    start = 0
+    for s, c in enumerate(ctx):
+        ref = _sdpa_contiguous(q[s], flatk[start * B:start * B + c], flatv[start * B:start * B + c],
+                               scale, group)
+        np.testing.assert_allclose(got[s], ref, rtol=0, atol=1e-12)
+        start += nblk[s]
+
+
+def test_scattered_table_equals_library_attention_on_tiny_batch():
+    b = workloads.tiny()
+    kc, vc = _written(b)
+    got = c_oracle.decode(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+    for s in range(b.num_seqs):
+        c = int(b.context_lens[s])
+        rows_k = []
+        rows_v = []
+        for t in range(c):
+            blk = b.block_tables[s, t // b.block_size]
+            rows_k.append(kc[blk, t % b.block_size])
+            rows_v.append(vc[blk, t % b.block_size])
+        ref = _sdpa_contiguous(b.q[s], np.stack(rows_k).astype(np.float64),
+                               np.stack(rows_v).astype(np.float64), b.scale, b.group_size)
+        np.testing.assert_allclose(got[s], ref, rtol=0, atol=1e-12)
+
+
+def test_c_oracle_equals_bruteforce_on_tiny_batch():
+    b = workloads.tiny()
+    kc, vc = _written(b)
+    a = c_oracle.decode(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+    r = numpy_oracle.decode_bruteforce(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+    assert np.isfinite(a).all()
+    np.testing.assert_allclose(a, r, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# closed forms
+# --------------------------------------------------------------------------
+
+def _single_seq(K, V, q, B=16, scale=1.0, perm_seed=None):
+    """Place one sequence's [n, Hk, d] K/V into a scattered pool."""
+    n, Hk, d = K.shape
+    nb = (n + B - 1) // B
+    N = nb + 3
+    rng = np.random.default_rng(perm_seed if perm_seed is not None else 5)
+    ids = rng.permutation(N)[:nb].astype(np.int32)
+    kc = np.full((N, B, Hk, d), np.float16(np.nan), np.float16)
+    vc = np.full((N, B, Hk, d), np.float16(np.nan), np.float16)
+    for t in range(n):
+        kc[ids[t // B], t % B] = K[t]
+        vc[ids[t // B], t % B] = V[t]
+    return dict(q=q[None], k_cache=kc, v_cache=vc, block_tables=ids[None],
+                context_lens=np.array([n], np.int32), scale=scale)
+
+
+def test_single_token_returns_its_value_exactly():
+    b = workloads.tiny()
+    kc, vc = _written(b)
+    out = c_oracle.decode(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+    s = 0
+    assert b.context_lens[s] == 1
+    blk = b.block_tables[s, 0]
+    for h in range(b.num_heads):
+        np.testing.assert_array_equal(out[s, h], vc[blk, 0, h // b.group_size].astype(np.float64))
+
+
+def test_two_tokens_with_a_log3_score_gap_weigh_one_quarter_three_quarters():
+    d = 64
+    K = np.zeros((2, 1, d), np.float16)
+    K[1, 0, 0] = 1.0
+    V = np.zeros((2, 1, d), np.float16)
+    V[0, 0, 1] = 1.0
+    V[1, 0, 2] = 1.0
+    q = np.zeros((1, d), np.float16)
+    q[0, 0] = 1.0
+    scale = float(np.float32(math.log(3.0)))  # score gap ln 3 -> weights 1:3
+    case = _single_seq(K, V, q, scale=scale)
+    out = c_oracle.decode(**case)[0, 0]
+    assert abs(out[1] - 0.25) < 1e-7 and abs(out[2] - 0.75) < 1e-7
+    assert np.all(out[3:] == 0) and out[0] == 0
+    # the scale multiplies the score: with scale 0 both tokens weigh one half
+    case["scale"] = 0.0
+    out0 = c_oracle.decode(**case)[0, 0]
+    assert out0[1] == 0.5 and out0[2] == 0.5
+
+
+def test_query_heads_read_consecutive_kv_head_groups():
+    rng = np.random.default_rng(3)
+    Hk, G, d, n = 3, 4, 64, 37
+    K = rng.standard_normal((n, Hk, d), dtype=np.float32).astype(np.float16)
+    V = np.empty((n, Hk, d), np.float16)
+    for kvh in range(Hk):
+        V[:, kvh, :] = kvh + 1  # each KV head's values are the constant kvh + 1
+    q = rng.standard_normal((Hk * G, d), dtype=np.float32).astype(np.float16)
+    out = c_oracle.decode(**_single_seq(K, V, q, scale=0.125))[0]
+    for h in range(Hk * G):
+        np.testing.assert_allclose(out[h], h // G + 1, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("n", [1, 15, 16, 17, 33, 48])
+def test_equal_keys_give_the_mean_of_the_values(n):
+    rng = np.random.default_rng(n)
+    d = 64
+    krow = rng.standard_normal(d, dtype=np.float32).astype(np.float16)
+    K = np.broadcast_to(krow, (n, 1, d)).copy()
+    V = rng.standard_normal((n, 1, d), dtype=np.float32).astype(np.float16)
+    q = rng.standard_normal((1, d), dtype=np.float32).astype(np.float16)
+    out = c_oracle.decode(**_single_seq(K, V, q, scale=0.125))[0, 0]
+    np.testing.assert_allclose(out, V[:, 0].astype(np.float64).mean(axis=0), rtol=0, atol=1e-13)
+
+
+def test_a_dominant_score_selects_its_value():
+    rng = np.random.default_rng(9)
+    n, d, j = 40, 64, 23
+    K = rng.standard_normal((n, 1, d), dtype=np.float32).astype(np.float16) * np.float16(0.01)
+    q = np.ones((1, d), np.float16)
+    K[j, 0, :] = 4.0  # score of token j exceeds the others by > 250 logits at scale 1
+    V = rng.standard_normal((n, 1, d), dtype=np.float32).astype(np.float16)
+    out = c_oracle.decode(**_single_seq(K, V, q, scale=1.0))[0, 0]
+    np.testing.assert_allclose(out, V[j, 0].astype(np.float64), rtol=0, atol=1e-15)
+
+
+def test_empty_sequence_gives_zeros():
+    b = workloads.tiny()
+    kc, vc = _written(b)
+    cl = b.context_lens.copy()
+    cl[2] = 0
+    out = c_oracle.decode(b.q, kc, vc, b.block_tables, cl, b.scale)
+    assert np.all(out[2] == 0)
+
+
+# --------------------------------------------------------------------------
+# invariants of the paged layout
+# --------------------------------------------------------------------------
+
+def test_relabelling_physical_blocks_leaves_the_output_bit_identical():
+    b = workloads.llama3_8b(num_seqs=3, max_ctx=300, min_ctx=100)
+    kc, vc = _written(b)
+    base = c_oracle.decode(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+    pi = np.random.default_rng(1).permutation(b.num_blocks)
+    kc2 = np.empty_like(kc)
+    vc2 = np.empty_like(vc)
+    kc2[pi] = kc
+    vc2[pi] = vc
+    bt2 = np.where(b.block_tables >= 0, pi[np.maximum(b.block_tables, 0)], -1).astype(np.int32)
+    out = c_oracle.decode(b.q, kc2, vc2, bt2, b.context_lens, b.scale)
+    assert np.array_equal(out, base)
+
+
+def test_shared_prefix_equals_duplicated_blocks():
+    b = workloads.shared_prefix(num_prompts=2, samples=3, prompt_len=32, max_suffix=20)
+    kc, vc = _written(b)
+    shared = c_oracle.decode(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+    # give every sample its own copy of the prompt blocks
+    bt = b.block_tables.copy()
+    extra_k, extra_v = [], []
+    nxt = b.num_blocks
+    for s in range(b.num_seqs):
+        for i in range(32 // b.block_size):
+            extra_k.append(kc[bt[s, i]])
+            extra_v.append(vc[bt[s, i]])
+            bt[s, i] = nxt
+            nxt += 1
+    kc2 = np.concatenate([kc, np.stack(extra_k)])
+    vc2 = np.concatenate([vc, np.stack(extra_v)])
+    dup = c_oracle.decode(b.q, kc2, vc2, bt, b.context_lens, b.scale)
+    assert np.array_equal(shared, dup)
+    assert len(np.unique(bt[:, :2])) == bt.shape[0] * 2
+
+
+def test_poisoned_slots_never_reach_the_output():
+    for b in (workloads.tiny(), workloads.llama3_8b(num_seqs=4, max_ctx=200, min_ctx=130)):
+        kc, vc = _written(b)
+        out = c_oracle.decode(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+        assert np.isfinite(out).all()
+        # without the write, the new token's slot still holds NaN and leaks in
+        stale = c_oracle.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.context_lens, b.scale)
+        assert np.isnan(stale).all(axis=-1).any()
+
+
+# --------------------------------------------------------------------------
+# reshape_and_cache
+# --------------------------------------------------------------------------
+
+def test_reshape_and_cache_c_and_numpy_agree_bitwise():
+    b = workloads.llama3_8b(num_seqs=5, max_ctx=100, min_ctx=20)
+    ck, cv = c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
+    nk, nv = numpy_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
+    assert np.array_equal(ck.view(np.uint16), nk.view(np.uint16))
+    assert np.array_equal(cv.view(np.uint16), nv.view(np.uint16))
+
+
+def test_reshape_and_cache_writes_only_the_mapped_slots():
+    b = workloads.tiny()
+    sm = b.slot_mapping.copy()
+    sm[1] = -1  # padding token: skipped
+    ck, cv = c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, sm)
+    B = b.block_size
+    changed = np.any(ck.view(np.uint16) != b.k_cache.view(np.uint16), axis=(2, 3))
+    expect = np.zeros_like(changed)
+    for t, slot in enumerate(sm):
+        if slot >= 0:
+            expect[slot // B, slot % B] = True
+            assert np.array_equal(ck[slot // B, slot % B].view(np.uint16), b.key[t].view(np.uint16))
+            assert np.array_equal(cv[slot // B, slot % B].view(np.uint16), b.value[t].view(np.uint16))
+    assert np.array_equal(changed, expect)
+
+
+def test_reshape_and_cache_rejects_duplicate_and_out_of_range_slots():
+    b = workloads.tiny()
+    dup = b.slot_mapping.copy()
+    dup[1] = dup[0]
+    with pytest.raises(c_oracle.OracleError):
+        c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, dup)
+    bad = b.slot_mapping.copy()
+    bad[0] = b.num_blocks * b.block_size
+    with pytest.raises(c_oracle.OracleError):
+        c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, bad)
+
+
+def test_new_token_lands_at_the_last_context_position():
+    b = workloads.llama3_8b(num_seqs=4, max_ctx=100, min_ctx=20)
+    kc, vc = _written(b)
+    for s in range(b.num_seqs):
+        pos = int(b.context_lens[s]) - 1
+        blk, off = c_oracle.locate_kv(pos, b.block_tables[s], b.block_size)
+        assert np.array_equal(kc[blk, off].view(np.uint16), b.key[s].view(np.uint16))
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: each mutant of the loop-by-token oracle fails a pin
+# --------------------------------------------------------------------------
+
+def _run_pins(decode_fn):
+    """Return the names of the pins that the given decode function fails."""
+    failed = []
+    b = workloads.tiny()
+    kc, vc = numpy_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
+    out = decode_fn(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+    for s in range(b.num_seqs):
+        c = int(b.context_lens[s])
+        ks = np.stack([kc[b.block_tables[s, t // 16], t % 16] for t in range(c)]).astype(np.float64)
+        vs = np.stack([vc[b.block_tables[s, t // 16], t % 16] for t in range(c)]).astype(np.float64)
+        ref = _sdpa_contiguous(b.q[s], ks, vs, b.scale, b.group_size)
+        if not (np.isfinite(out[s]).all() and np.allclose(out[s], ref, rtol=0, atol=1e-9)):
+            failed.append("library-attention")
+            break
+    # GQA mapping
+    rng = np.random.default_rng(3)
+    K = rng.standard_normal((20, 2, 16), dtype=np.float32).astype(np.float16)
+    V = np.empty((20, 2, 16), np.float16)
+    V[:, 0] = 1
+    V[:, 1] = 2
+    q = rng.standard_normal((4, 16), dtype=np.float32).astype(np.float16)
+    case = _single_seq(K, V, q, scale=0.25)
+    o = decode_fn(case["q"], case["k_cache"], case["v_cache"], case["block_tables"],
+                  case["context_lens"], case["scale"])[0]
+    if not all(np.allclose(o[h], h // 2 + 1) for h in range(4)):
+        failed.append("gqa-mapping")
+    return failed
+
+
+def test_pins_pass_on_the_oracle_itself():
+    assert _run_pins(numpy_oracle.decode_bruteforce) == []
+
+
+@pytest.mark.parametrize("mutant", ["swap_block_and_offset", "drop_scale", "modulo_heads",
+                                    "context_off_by_one", "divide_scale"])
+def test_pins_catch_planted_mistakes(monkeypatch, mutant):
+    orig_locate = numpy_oracle.locate_kv
+    decode = numpy_oracle.decode_bruteforce
+    if mutant == "swap_block_and_offset":
+        monkeypatch.setattr(numpy_oracle, "locate_kv",
+                            lambda t, table, B: (int(table[t % len(table)]), t // len(table) % B))
+    elif mutant == "drop_scale":
+        def decode(q, kc, vc, bt, cl, scale):
+            return numpy_oracle.decode_bruteforce(q, kc, vc, bt, cl, 1.0)
+    elif mutant == "divide_scale":
+        def decode(q, kc, vc, bt, cl, scale):
+            return numpy_oracle.decode_bruteforce(q, kc, vc, bt, cl, 1.0 / scale)
+    elif mutant == "context_off_by_one":
+        def decode(q, kc, vc, bt, cl, scale):
+            return numpy_oracle.decode_bruteforce(q, kc, vc, bt, np.maximum(cl - 1, 1), scale)
+    elif mutant == "modulo_heads":
+        def decode(q, kc, vc, bt, cl, scale):
+            S, H, d = q.shape
+            Hk = kc.shape[2]
+            G = H // Hk
+            # read KV head h % Hk instead of h // G: query head h is moved to
+            # slot perm[h], which the correct mapping sends to KV head h % Hk
+            perm = [(h % Hk) * G + (h // Hk) for h in range(H)]
+            qn = np.empty_like(q)
+            qn[:, perm] = q
+            out = numpy_oracle.decode_bruteforce(qn, kc, vc, bt, cl, scale)
+            return out[:, perm]
+    assert orig_locate(37, [7, 42, 9, 103], 16) == (9, 5)
+    assert _run_pins(decode) != []

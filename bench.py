@@ -1,0 +1,491 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one decode step of one layer for a whole batch: reshape_and_cache
+(the new token of every sequence into its slot), split-K paged decode, and
+the log-sum-exp reduce.  Default workload: the Llama-3-8B-shaped decode layer
+(64 sequences, 32 q heads / 8 KV heads, head_dim 128, block_size 16,
+contexts uniform in [128, 2048], 1.25x pool with shuffled block ids).
+
+Prints one JSON line.  ``value`` is KV-read GB/s: the algorithmic KV bytes of
+a step (sum over sequences of ctx * K+V bytes per token) times the steps,
+divided by the device time of the K steps.  The inputs sit in HBM before the
+timed region; the KV pools rotate over replicas whose total is far larger
+than L2, so no step reads KV bytes that an earlier step left in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+``--impl reference`` times the float64 CPU oracle on the host cores on the
+same workload (a bounded sample of sequences per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV-read GB/s (% of GB300 HBM peak) and decode tokens/s"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_173_gb300", "csrc", "pa_kernels.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+# ----------------------------------------------------------------- workload
+def make_workload(name: str, seed: int, partition_size: int):
+    from paged_kv_cache_173_gb300 import workloads
+    if name == "llama3-8b":
+        b = workloads.llama3_8b(seed=seed, poison=False, partition_size=partition_size)
+        desc = ("llama3-8b decode layer: S=64, H=32, Hk=8, d=128, B=16, ctx~U[128,2048], "
+                "1.25x pool, shuffled ids, 1 new token/seq")
+    elif name in ("llama2-70b-b16", "llama2-70b-b32"):
+        bs = int(name[-2:])
+        b = workloads.llama2_70b(seed=seed, block_size=bs, poison=False, partition_size=partition_size)
+        desc = f"llama2-70b GQA decode: S=32, H=64, Hk=8, d=128, B={bs}, ctx=8192, 1.25x pool, shuffled"
+    elif name == "long-context":
+        b = workloads.long_context(seed=seed, poison=False, partition_size=partition_size)
+        desc = "long-context decode: S=4, ctx {32K,64K,96K,128K}, H=32, Hk=8, d=128, B=16"
+    elif name == "shared-prefix":
+        b = workloads.shared_prefix(seed=seed, poison=False, partition_size=partition_size)
+        desc = "shared-prefix sampling: 16 prompts x 8 samples, prompt 1024, suffix U[0,512], MHA 40, d=128"
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    return b, desc
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_sha() -> str:
+    h = hashlib.sha256()
+    for p in (DECODE_SRC, os.path.join(os.path.dirname(DECODE_SRC), "pa_ptx.cuh")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str):
+    """ncu DRAM bytes per decode launch, if taken on the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_sha") != decode_source_sha():
+        return None
+    return rec.get("per_workload", {}).get(workload)
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.period)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)  # let the first samples arrive before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = [l for (t, l) in self.lines if t0 <= t <= t1 + 0.05]
+        if not rows and self.lines:
+            # the region was shorter than the sampling period: take the nearest sample
+            rows = [min(self.lines, key=lambda x: abs(x[0] - (t0 + t1) / 2))[1]]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- GPU arm
+def run_gpu(args, rank: int, world: int):
+    import torch
+    from paged_kv_cache_173_gb300 import api, workloads
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    b, desc = make_workload(args.workload, args.seed + rank, args.partition_size)
+    kv_bytes = workloads.algorithmic_kv_bytes(b)
+    ps = b.partition_size
+    P = api.max_num_partitions_for(b.max_blocks_per_seq, b.block_size, ps)
+
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    pool_bytes = 2 * b.k_cache.nbytes
+    l2_bytes = 129 * 2 ** 20
+    R = max(2, min(8, math.ceil(4 * l2_bytes / max(1, kv_bytes)) + 1))
+    reps = []
+    k0, v0, q0 = t(b.k_cache), t(b.v_cache), t(b.q)
+    for r in range(R):
+        reps.append((k0.clone(), v0.clone(), q0.clone()) if r else (k0, v0, q0))
+    key, value, sm = t(b.key), t(b.value), t(b.slot_mapping)
+    bt, cl = t(b.block_tables), t(b.context_lens)
+    out = torch.empty_like(q0)
+    ws = api.alloc_splitk_workspace(b.num_seqs, b.num_heads, b.head_dim, P, dev)
+    M, B = b.max_blocks_per_seq, b.block_size
+
+    def step(r, ev=None):
+        kc, vc, q = reps[r % R]
+        if ev is not None:
+            ev[0].record()
+        api.pa_reshape_and_cache(key, value, kc, vc, sm)
+        if ev is not None:
+            ev[1].record()
+        api.pa_decode_splitk(out, q, kc, vc, bt, cl, b.scale, ps, ws, P)
+        if ev is not None:
+            ev[2].record()
+        api.pa_splitk_reduce(out, ws, cl, M, B, ps, P)
+        if ev is not None:
+            ev[3].record()
+
+    stream = torch.cuda.Stream(dev)
+    K, W = args.steps, args.warmup
+    G = min(K, 8 * R)  # steps per graph replay
+    with torch.cuda.stream(stream):
+        for i in range(max(W, 3)):  # warm-up (also sets kernel attributes before capture)
+            step(i)
+    torch.cuda.synchronize(dev)
+
+    g_plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_plain, stream=stream):
+        for i in range(G):
+            step(i)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(G)]
+    g_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_ev, stream=stream):
+        for i in range(G):
+            step(i, evs[i])
+    n_plain = (K - G) // G
+    tail = K - G - n_plain * G
+    g_tail = None
+    if tail:
+        g_tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_tail, stream=stream):
+            for i in range(tail):
+                step(i)
+    # untimed replays of each graph
+    with torch.cuda.stream(stream):
+        g_plain.replay()
+        g_ev.replay()
+        if g_tail:
+            g_tail.replay()
+    torch.cuda.synchronize(dev)
+
+    import torch.distributed as dist
+    distributed = world > 1 and dist.is_initialized()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    if distributed:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e_start.record()
+        for _ in range(n_plain):
+            g_plain.replay()
+        if g_tail:
+            g_tail.replay()
+        g_ev.replay()  # the last G steps carry per-kernel events
+        e_end.record()
+    torch.cuda.synchronize(dev)
+    if distributed:
+        dist.barrier()
+    wall1 = time.time()
+    clocks.stop()
+    ms = e_start.elapsed_time(e_end)
+    if distributed:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(G)])
+    t_reshape, t_decode, t_reduce = per.mean(axis=0)  # ms per launch
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream)
+
+    peak, peak_kind = load_peak()
+    value = kv_bytes * K * world / (ms * 1e-3) / 1e9
+    step_ms = ms / K
+    achieved = kv_bytes / (t_decode * 1e-3) / 1e9
+    traffic = load_traffic(args.workload)
+    res = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": desc,
+            "kv_bytes_per_step": kv_bytes,
+            "partition_size": ps,
+            "l2": f"{R} rotating pool replicas ({R * pool_bytes / 1e9:.2f} GB) > 129 MB L2; steps back to back",
+            "steps_per_graph": G,
+        },
+        "hbm_frac_of_step": round(value / world / peak, 4),
+        "hbm_peak_gbs": peak,
+        "hbm_peak_kind": peak_kind,
+        "tokens_per_s": round(b.num_seqs * world / (step_ms * 1e-3), 1),
+        "kernel_ms": {"reshape_and_cache": round(t_reshape, 5), "paged_decode_splitk": round(t_decode, 5),
+                      "splitk_reduce": round(t_reduce, 5)},
+        "roofline": {
+            "kernel": "paged_decode_kernel (split-K)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "peak_kind": f"{peak_kind} (copy GB/s)",
+        },
+        "gpu_launches": 3 * K,
+        "e2e": e2e,
+        "clocks": clocks.summary(wall0, wall1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(b, kv_bytes, budget_s=args.cpu_seconds)
+    return res
+
+
+def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream):
+    """Same step through the public API with pinned host inputs and output."""
+    import torch
+    from paged_kv_cache_173_gb300 import api
+
+    host = {k: torch.from_numpy(np.ascontiguousarray(getattr(b, k))).pin_memory()
+            for k in ("q", "key", "value", "slot_mapping", "block_tables", "context_lens")}
+    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out = torch.empty_like(devb["q"])
+    out_h = torch.empty_like(host["q"]).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    M, B, ps, R = b.max_blocks_per_seq, b.block_size, b.partition_size, len(reps)
+
+    def step(i):
+        kc, vc, _ = reps[i % R]
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        api.pa_reshape_and_cache(devb["key"], devb["value"], kc, vc, devb["slot_mapping"])
+        api.pa_decode_splitk(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"], b.scale,
+                             ps, ws, P)
+        api.pa_splitk_reduce(out, ws, devb["context_lens"], M, B, ps, P)
+        out_h.copy_(out, non_blocking=True)
+
+    n = max(3, min(args.steps, args.e2e_steps))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            step(i)
+        e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    return {"value": round(kv_bytes * n / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
+            "ms_per_step": round(ms / n, 5)}
+
+
+# ------------------------------------------------------------ CPU oracle
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def oracle_step_runner(b):
+    """Returns (run(n_seqs, offset) -> kv_bytes, cores): one oracle decode step
+    (reshape_and_cache + decode) over a cyclic sample of n_seqs sequences."""
+    from oracle import c_oracle
+    cores = c_oracle.max_threads()
+    S = b.num_seqs
+    per_tok = 2 * b.num_kv_heads * b.head_dim * 2
+    kc, vc = b.k_cache.copy(), b.v_cache.copy()  # working pools, written in place each step
+
+    def run(n, off):
+        idx = (np.arange(n) + off) % S
+        c_oracle.reshape_and_cache(b.key[idx], b.value[idx], kc, vc, b.slot_mapping[idx], inplace=True)
+        c_oracle.decode(b.q[idx], kc, vc, b.block_tables[idx], b.context_lens[idx], b.scale)
+        return int(np.sum(b.context_lens[idx].astype(np.int64))) * per_tok
+
+    return run, cores
+
+
+def cpu_baseline(b, kv_bytes, budget_s: float):
+    run, cores = oracle_step_runner(b)
+    t0 = time.perf_counter()
+    nbytes = run(1, 0)
+    one = time.perf_counter() - t0
+    n = int(max(1, min(b.num_seqs, budget_s / max(one, 1e-6) / 3)))
+    done, elapsed, off = 0, 0.0, 1
+    while elapsed < budget_s:
+        t0 = time.perf_counter()
+        done += run(n, off)
+        elapsed += time.perf_counter() - t0
+        off += n
+    return {"value": round(done / elapsed / 1e9, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"float64 C oracle (reshape_and_cache + decode), {n} of {b.num_seqs} sequences per "
+                      f"call, {elapsed:.1f} s, {done / 1e9:.2f} GB of KV, host {_cpu_model()}"}
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return None
+    b, desc = make_workload(args.workload, args.seed, args.partition_size)
+    run, cores = oracle_step_runner(b)
+    t0 = time.perf_counter()
+    run(1, 0)
+    one = time.perf_counter() - t0
+    budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    n = int(max(1, min(b.num_seqs, budget / max(one, 1e-6))))
+    off = 0
+    for _ in range(args.warmup):
+        run(n, off)
+        off += n
+    done = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        done += run(n, off)
+        off += n
+    el = time.perf_counter() - t0
+    value = done / el / 1e9
+    sample = (f"float64 C oracle, {n} of {b.num_seqs} sequences per step (cycling), {args.steps} steps, "
+              f"{el:.1f} s, host {_cpu_model()}")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / max(1, args.steps) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": desc, "kv_bytes_per_step": done // max(1, args.steps)},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------ main
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[1])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="llama3-8b")
+    p.add_argument("--partition-size", type=int, default=512)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=2000)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--reference-seconds", type=float, default=90.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    res = run_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

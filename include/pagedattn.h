@@ -1,0 +1,201 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn.so: PagedAttention decode for GB300
+ * (sm_103a).
+ *
+ * The KV cache of one layer lives in two preallocated pools of fixed-size
+ * blocks, one for keys and one for values, each laid out
+ *
+ *     [num_blocks][block_size][num_kv_heads][head_dim]      (row-major)
+ *
+ * A sequence's tokens are scattered over physical blocks; its block table
+ * row maps logical block i to a physical block id, and its context length
+ * bounds the valid slots of its last block.  ("PagedAttention: when the KV
+ * cache meets OS paging", section 3.1; "Efficient Memory Management for LLM
+ * Serving with PagedAttention -- in-depth reading", sections 2.3 and 3.2.)
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller.  The library allocates
+ *    nothing and keeps no state between calls except a per-thread text of
+ *    the last error (pa_last_error) and a per-device record of which kernel
+ *    attributes it has already set.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL means the legacy default stream).  The caller synchronises.
+ *  - The return value is a pa_status.  Arguments are checked on the host
+ *    before any launch; on an error nothing is launched.  Values that live in
+ *    device memory (slot ids, block ids, context lengths) cannot be read by
+ *    the host without a synchronisation, so the kernels check them instead
+ *    and never read or write outside the buffers whose sizes the call states:
+ *    the documented outcome of a bad device value is given with each call.
+ *  - Tensor pointers must be 16-byte aligned and the tensors contiguous in
+ *    the layouts given.  Element type: dtype = PA_FP16 (IEEE binary16).
+ *    All arithmetic after the loads is float32.
+ *  - Supported shapes: head_dim in {64, 128}; block_size in {16, 32};
+ *    num_heads a multiple of num_kv_heads with num_heads / num_kv_heads <= 16;
+ *    num_seqs <= 65535.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = -1, /* null/misaligned pointer, inconsistent sizes  */
+  PA_ERR_UNSUPPORTED = -2, /* a shape or dtype outside the supported set  */
+  PA_ERR_CUDA = -3         /* a CUDA runtime error; see pa_last_error()   */
+} pa_status;
+
+typedef enum pa_dtype { PA_FP16 = 0 } pa_dtype;
+
+/*
+ * pa_reshape_and_cache -- write each new token's key and value into its slot.
+ *
+ * Defined by the cache write of "vLLM PagedAttention source walk-through",
+ * section 3.2 (append_token computes block_idx = pos / block_size and
+ * block_offset = pos % block_size and writes the token's KV there) and
+ * "in-depth reading", section 3.4, step 1.  The slot is passed flattened:
+ *
+ *     slot = physical_block * block_size + block_offset
+ *
+ * For every token t < num_tokens with slot_mapping[t] >= 0 and every KV head
+ * h:  k_cache[slot / block_size][slot % block_size][h][:] = key[t][h][:],
+ * likewise v_cache from value.  The copy is bit-exact.
+ *
+ *   key, value     [num_tokens][num_kv_heads][head_dim], read only
+ *   k_cache,
+ *   v_cache        [num_blocks][block_size][num_kv_heads][head_dim], written
+ *                  in place at the mapped slots only
+ *   slot_mapping   [num_tokens] int64.  Negative: padding, skipped.  A slot
+ *                  >= num_blocks * block_size is a caller error; it is
+ *                  skipped (nothing is written out of bounds).  Slots must be
+ *                  distinct: with duplicates the surviving value is undefined.
+ *   num_tokens     >= 0 (0 is a no-op)
+ *
+ * Copy-on-write of a block shared by several sequences is the caller's job
+ * (the write goes to whatever block the slot names).
+ */
+int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                         int block_size, int num_kv_heads, int head_dim, int dtype,
+                         void* stream);
+
+/*
+ * pa_decode -- single-pass paged decode attention, one query token per
+ * sequence.
+ *
+ * Defined by "vLLM PagedAttention source walk-through", section 3.4 (walk the
+ * block table, load each block's K and V, score q against K scaled by
+ * `scale`, mask the slots past the context, online softmax with a running
+ * maximum and sum, accumulate the probabilities times V, normalise by the
+ * running sum) and "PagedAttention: when the KV cache meets OS paging",
+ * section 3.2.  The result equals ordinary softmax attention over the
+ * sequence's first context_lens[s] tokens:
+ *
+ *   out[s][h][:] = sum_i softmax_i(scale * q[s][h] . K_i) * V_i,
+ *   K_i, V_i     = pool rows of token i of sequence s, KV head h / G,
+ *   G            = num_heads / num_kv_heads (consecutive query heads share a
+ *                  KV head).
+ *
+ *   out            [num_seqs][num_heads][head_dim], written (fp16, rounded
+ *                  to nearest even)
+ *   q              [num_seqs][num_heads][head_dim]
+ *   k_cache,
+ *   v_cache        [num_blocks][block_size][num_kv_heads][head_dim]
+ *   block_tables   [num_seqs][max_blocks_per_seq] int32 physical block ids;
+ *                  only the first ceil(context_lens[s] / block_size) entries
+ *                  of a row are read
+ *   context_lens   [num_seqs] int32, the number of valid tokens, including
+ *                  the token being decoded
+ *
+ * Device-value outcomes: context_lens[s] == 0 gives out[s] = 0;
+ * context_lens[s] < 0 or > max_blocks_per_seq * block_size, or a block id
+ * read from the table outside [0, num_blocks), gives NaN in out for the
+ * affected (sequence, KV-head group).  Nothing is read out of bounds.
+ */
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+              int num_blocks, float scale, int dtype, void* stream);
+
+/*
+ * pa_splitk_workspace_bytes -- size of the split-K workspace.
+ *
+ * The workspace holds, per (sequence, query head, partition), the
+ * partition's normalised output o_p [head_dim] and its log-sum-exp pair
+ * (m_p, l_p), all float32:  num_seqs * num_heads * max_num_partitions *
+ * (head_dim + 2) * 4 bytes.  Returns 0 for non-positive arguments.
+ */
+size_t pa_splitk_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_num_partitions);
+
+/*
+ * pa_decode_splitk -- the same attention as pa_decode, with each sequence's
+ * context cut into partitions of partition_size tokens that run in parallel.
+ *
+ * Partition p of sequence s covers tokens [p * partition_size,
+ * min((p + 1) * partition_size, context_lens[s])).  Each runs the online
+ * softmax of "vLLM PagedAttention source walk-through", section 3.4 over its
+ * tokens and stores o_p = acc_p / l_p together with its running maximum m_p
+ * (in log2 units: m_p = max_i scale * log2(e) * q . K_i) and sum
+ * l_p = sum_i 2^(scale * log2(e) * q . K_i - m_p).  pa_splitk_reduce merges
+ * the partitions with the same correction factor the walk-through's online
+ * softmax applies between blocks.
+ *
+ * Sequences with at most one partition are finished here: out[s] is written
+ * directly and they leave nothing in the workspace.  Calling
+ * pa_splitk_reduce afterwards is always required and always correct.
+ *
+ *   partition_size      tokens per partition, a positive multiple of
+ *                       block_size
+ *   max_num_partitions  >= ceil(max_blocks_per_seq * block_size /
+ *                       partition_size)
+ *   workspace           device buffer of workspace_bytes >=
+ *                       pa_splitk_workspace_bytes(num_seqs, num_heads,
+ *                       head_dim, max_num_partitions); scratch owned by the
+ *                       caller, contents on entry ignored
+ *
+ * Other arguments and device-value outcomes as pa_decode.
+ */
+int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                     int head_dim, int block_size, int num_blocks, float scale, int dtype,
+                     int partition_size, int max_num_partitions, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
+ * pa_splitk_reduce -- merge the partitions left by pa_decode_splitk.
+ *
+ * For each (s, h) whose sequence has P = ceil(context_lens[s] /
+ * partition_size) >= 2 partitions:
+ *
+ *   M = max_p m_p,  w_p = l_p * 2^(m_p - M),
+ *   out[s][h][:] = fp16( sum_p w_p * o_p[:] / sum_p w_p ).
+ *
+ * This is the correction factor exp(old_max - new_max) of the online softmax
+ * in "vLLM PagedAttention source walk-through", section 3.4, applied between
+ * partitions instead of between blocks.  Sequences with P <= 1, or with an
+ * out-of-range context length, are left untouched (pa_decode_splitk already
+ * wrote them).  The arguments must match the pa_decode_splitk call that
+ * filled the workspace, on the same stream (or ordered after it).
+ */
+int pa_splitk_reduce(void* out, const void* workspace, size_t workspace_bytes,
+                     const int32_t* context_lens, int max_blocks_per_seq, int block_size,
+                     int num_seqs, int num_heads, int head_dim, int partition_size,
+                     int max_num_partitions, int dtype, void* stream);
+
+/* Fixed text naming a status code. */
+const char* pa_status_string(int status);
+
+/* Text of the last error raised on the calling thread ("" if none). */
+const char* pa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -68,11 +68,16 @@ def locate_kv(logical_token_idx: int, block_table, block_size: int) -> Tuple[int
 
 
 def reshape_and_cache(key: np.ndarray, value: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
-                      slot_mapping: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
-    """Return updated copies of the pools (inputs are left untouched)."""
+                      slot_mapping: np.ndarray, inplace: bool = False) -> Tuple[np.ndarray, np.ndarray]:
+    """Return the pools after the write: updated copies (inputs untouched), or
+    the given pools themselves, written in place, with ``inplace=True``."""
     assert key.dtype == np.float16 and value.dtype == np.float16
-    kc = np.ascontiguousarray(k_cache).copy()
-    vc = np.ascontiguousarray(v_cache).copy()
+    if inplace:
+        assert k_cache.flags["C_CONTIGUOUS"] and v_cache.flags["C_CONTIGUOUS"]
+        kc, vc = k_cache, v_cache
+    else:
+        kc = np.ascontiguousarray(k_cache).copy()
+        vc = np.ascontiguousarray(v_cache).copy()
     N, B, Hk, d = kc.shape
     key = np.ascontiguousarray(key)
     value = np.ascontiguousarray(value)

@@ -1,0 +1,140 @@
+"""Python binding of the C ABI, one function per entry point, same names.
+
+Argument marshalling only: shapes are read from the tensors, pointers and the
+current CUDA stream are passed to ``libpagedattn.so``, and a non-zero status
+raises ``PagedAttnError``.  Every step of the computation runs in the
+library's kernels; PyTorch provides device memory and streams.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import PA_FP16, PagedAttnError  # noqa: F401  (re-exported)
+
+
+def _stream_ptr(t: torch.Tensor, stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    return int(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return int(t.data_ptr())
+
+
+def _cuda_device(t: torch.Tensor) -> torch.device:
+    if not t.is_cuda:
+        raise ValueError("paged attention tensors must live on a CUDA device")
+    return t.device
+
+
+def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Write key/value [T, Hk, d] into the pools [N, B, Hk, d] at slot_mapping [T] (int64)."""
+    dev = _cuda_device(k_cache)
+    N, B, Hk, d = k_cache.shape
+    T = key.shape[0]
+    if key.shape != (T, Hk, d) or value.shape != (T, Hk, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("key/value must be [T, Hk, d] matching the pools [N, B, Hk, d]")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [T]")
+    st = _lib.lib().pa_reshape_and_cache(
+        _need(key, "key", torch.float16, dev), _need(value, "value", torch.float16, dev),
+        _need(k_cache, "k_cache", torch.float16, dev), _need(v_cache, "v_cache", torch.float16, dev),
+        _need(slot_mapping, "slot_mapping", torch.int64, dev), T, N, B, Hk, d, PA_FP16,
+        _stream_ptr(k_cache, stream))
+    _lib.check("pa_reshape_and_cache", st)
+
+
+def _decode_common(out, q, k_cache, v_cache, block_tables, context_lens):
+    dev = _cuda_device(q)
+    S, H, d = q.shape
+    N, B, Hk, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("q/out [S, H, d] must match the pools [N, B, Hk, d]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, M] and context_lens [S]")
+    ptrs = (_need(out, "out", torch.float16, dev), _need(q, "q", torch.float16, dev),
+            _need(k_cache, "k_cache", torch.float16, dev), _need(v_cache, "v_cache", torch.float16, dev),
+            _need(block_tables, "block_tables", torch.int32, dev))
+    cl = _need(context_lens, "context_lens", torch.int32, dev)
+    return dev, S, H, d, N, B, Hk, int(block_tables.shape[1]), ptrs, cl
+
+
+def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+              block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+              stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Single-pass paged decode: out[S, H, d] = attention of q over each sequence's paged KV."""
+    dev, S, H, d, N, B, Hk, M, (po, pq, pk, pv, pbt), pcl = _decode_common(
+        out, q, k_cache, v_cache, block_tables, context_lens)
+    st = _lib.lib().pa_decode(po, pq, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N, float(scale), PA_FP16,
+                              _stream_ptr(q, stream))
+    _lib.check("pa_decode", st)
+
+
+def pa_splitk_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int,
+                              max_num_partitions: int) -> int:
+    return int(_lib.lib().pa_splitk_workspace_bytes(num_seqs, num_heads, head_dim, max_num_partitions))
+
+
+def max_num_partitions_for(max_blocks_per_seq: int, block_size: int, partition_size: int) -> int:
+    return -(-(max_blocks_per_seq * block_size) // partition_size)
+
+
+def pa_decode_splitk(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                     partition_size: int, workspace: torch.Tensor,
+                     max_num_partitions: Optional[int] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Split-K paged decode; follow with pa_splitk_reduce on the same stream."""
+    dev, S, H, d, N, B, Hk, M, (po, pq, pk, pv, pbt), pcl = _decode_common(
+        out, q, k_cache, v_cache, block_tables, context_lens)
+    P = max_num_partitions or max_num_partitions_for(M, B, partition_size)
+    ws = _need(workspace, "workspace", workspace.dtype, dev)
+    st = _lib.lib().pa_decode_splitk(po, pq, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N, float(scale),
+                                     PA_FP16, int(partition_size), int(P), ws,
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream_ptr(q, stream))
+    _lib.check("pa_decode_splitk", st)
+
+
+def pa_splitk_reduce(out: torch.Tensor, workspace: torch.Tensor, context_lens: torch.Tensor,
+                     max_blocks_per_seq: int, block_size: int, partition_size: int,
+                     max_num_partitions: Optional[int] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Merge the partitions of pa_decode_splitk into out[S, H, d]."""
+    dev = _cuda_device(out)
+    S, H, d = out.shape
+    P = max_num_partitions or max_num_partitions_for(max_blocks_per_seq, block_size, partition_size)
+    st = _lib.lib().pa_splitk_reduce(
+        _need(out, "out", torch.float16, dev), _need(workspace, "workspace", workspace.dtype, dev),
+        workspace.numel() * workspace.element_size(), _need(context_lens, "context_lens", torch.int32, dev),
+        int(max_blocks_per_seq), int(block_size), S, H, d, int(partition_size), int(P), PA_FP16,
+        _stream_ptr(out, stream))
+    _lib.check("pa_splitk_reduce", st)
+
+
+def pa_status_string(status: int) -> str:
+    return _lib.status_name(status)
+
+
+def pa_last_error() -> str:
+    return _lib.last_error()
+
+
+def alloc_splitk_workspace(num_seqs: int, num_heads: int, head_dim: int, max_num_partitions: int,
+                           device) -> torch.Tensor:
+    """A float32 device buffer of the size pa_splitk_workspace_bytes states."""
+    nbytes = pa_splitk_workspace_bytes(num_seqs, num_heads, head_dim, max_num_partitions)
+    return torch.empty(max(1, nbytes // 4), dtype=torch.float32, device=device)

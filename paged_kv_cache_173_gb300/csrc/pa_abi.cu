@@ -1,0 +1,244 @@
+// pa_abi.cu -- the extern "C" entry points of libpagedattn.so.
+//
+// Host-side argument checks, then one launch per kernel on the caller's
+// stream.  Semantics and argument layouts are stated in include/pagedattn.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdint>
+
+#include "pa_launch.h"
+#include "pagedattn.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int ok() {
+  g_last_error[0] = '\0';
+  return PA_OK;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape checks shared by every decode entry point.
+int check_decode(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                 int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                 int num_blocks, float scale, int dtype) {
+  if (dtype != PA_FP16) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 only)", dtype);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (64 or 128)", head_dim);
+  if (block_size < 16 || block_size > 256 || block_size % 16 != 0)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d is not supported (a multiple of 16, at most 256)",
+                block_size);
+  if (num_heads <= 0 || num_kv_heads <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_heads (%d) and num_kv_heads (%d) must be positive", num_heads,
+                num_kv_heads);
+  if (num_heads % num_kv_heads != 0)
+    return fail(PA_ERR_UNSUPPORTED, "num_heads %d is not a multiple of num_kv_heads %d", num_heads,
+                num_kv_heads);
+  if (num_heads / num_kv_heads > 16)
+    return fail(PA_ERR_UNSUPPORTED, "query group size %d exceeds 16", num_heads / num_kv_heads);
+  if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs %d is negative", num_seqs);
+  if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535", num_seqs);
+  if (max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq %d must be positive", max_blocks_per_seq);
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "max_blocks_per_seq * block_size exceeds 2^31 - 1");
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks %d must be positive", num_blocks);
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned");
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return fail(PA_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
+  return PA_OK;
+}
+
+int needed_partitions(int max_blocks_per_seq, int block_size, int partition_size) {
+  const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+  return static_cast<int>((cap + partition_size - 1) / partition_size);
+}
+
+int check_splitk(int max_blocks_per_seq, int block_size, int partition_size, int max_num_partitions,
+                 const void* workspace, size_t workspace_bytes, int num_seqs, int num_heads,
+                 int head_dim) {
+  if (partition_size <= 0 || partition_size % block_size != 0)
+    return fail(PA_ERR_INVALID_ARG, "partition_size %d must be a positive multiple of block_size %d",
+                partition_size, block_size);
+  const int need = needed_partitions(max_blocks_per_seq, block_size, partition_size);
+  if (max_num_partitions < need)
+    return fail(PA_ERR_INVALID_ARG, "max_num_partitions %d < ceil(max_blocks_per_seq * block_size / "
+                "partition_size) = %d", max_num_partitions, need);
+  if (max_num_partitions > 65535)
+    return fail(PA_ERR_UNSUPPORTED, "max_num_partitions %d exceeds 65535", max_num_partitions);
+  if (num_seqs == 0) return PA_OK;
+  const size_t bytes = pa_splitk_workspace_bytes(num_seqs, num_heads, head_dim, max_num_partitions);
+  if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned(workspace, 16)) return fail(PA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (workspace_bytes < bytes)
+    return fail(PA_ERR_INVALID_ARG, "workspace_bytes %zu < %zu required", workspace_bytes, bytes);
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    default: return "PA_UNKNOWN_STATUS";
+  }
+}
+
+const char* pa_last_error(void) { return g_last_error; }
+
+size_t pa_splitk_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_num_partitions) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_num_partitions <= 0) return 0;
+  const size_t rows = pa::ws_rows(num_seqs, num_heads, max_num_partitions);
+  return rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
+}
+
+int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                         int block_size, int num_kv_heads, int head_dim, int dtype, void* stream) {
+  if (dtype != PA_FP16) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 only)", dtype);
+  if (head_dim <= 0 || head_dim % 8 != 0 || head_dim > 1024)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (a multiple of 8, at most 1024)",
+                head_dim);
+  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens %d is negative", num_tokens);
+  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_blocks, block_size and num_kv_heads must be positive");
+  if (static_cast<int64_t>(num_tokens) * num_kv_heads > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "num_tokens * num_kv_heads exceeds 2^31 - 1");
+  if (num_tokens == 0) return ok();
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return fail(PA_ERR_INVALID_ARG, "key, value and the caches must be 16-byte aligned, "
+                "slot_mapping 8-byte aligned");
+  pa::ReshapeArgs a{key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                    num_blocks, block_size, num_kv_heads, head_dim};
+  return cuda_status(pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream)),
+                     "reshape_and_cache launch");
+}
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+              int num_blocks, float scale, int dtype, void* stream) {
+  int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                        dtype);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0) return ok();
+  pa::DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.ws = nullptr;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.partition_size = max_blocks_per_seq * block_size;  // one partition per sequence
+  a.max_num_partitions = 1;
+  return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)), "decode launch");
+}
+
+int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                     int head_dim, int block_size, int num_blocks, float scale, int dtype,
+                     int partition_size, int max_num_partitions, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                        dtype);
+  if (st != PA_OK) return st;
+  st = check_splitk(max_blocks_per_seq, block_size, partition_size, max_num_partitions, workspace,
+                    workspace_bytes, num_seqs, num_heads, head_dim);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0) return ok();
+  pa::DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.ws = static_cast<float*>(workspace);
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.partition_size = partition_size;
+  a.max_num_partitions = max_num_partitions;
+  return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)),
+                     "split-K decode launch");
+}
+
+int pa_splitk_reduce(void* out, const void* workspace, size_t workspace_bytes,
+                     const int32_t* context_lens, int max_blocks_per_seq, int block_size,
+                     int num_seqs, int num_heads, int head_dim, int partition_size,
+                     int max_num_partitions, int dtype, void* stream) {
+  if (dtype != PA_FP16) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 only)", dtype);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (64 or 128)", head_dim);
+  if (block_size < 16 || block_size > 256 || block_size % 16 != 0)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d is not supported", block_size);
+  if (num_seqs < 0 || num_heads <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0 and num_heads > 0");
+  if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535", num_seqs);
+  if (max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq %d must be positive", max_blocks_per_seq);
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "max_blocks_per_seq * block_size exceeds 2^31 - 1");
+  int st = check_splitk(max_blocks_per_seq, block_size, partition_size, max_num_partitions, workspace,
+                        workspace_bytes, num_seqs, num_heads, head_dim);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0) return ok();
+  if (!out || !context_lens) return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned(out, 16) || !aligned(context_lens, 4))
+    return fail(PA_ERR_INVALID_ARG, "out must be 16-byte aligned, context_lens 4-byte aligned");
+  pa::ReduceArgs a{out, static_cast<const float*>(workspace), context_lens, max_blocks_per_seq,
+                   block_size, num_seqs, num_heads, head_dim, partition_size, max_num_partitions};
+  return cuda_status(pa::launch_splitk_reduce(a, static_cast<cudaStream_t>(stream)),
+                     "split-K reduce launch");
+}
+
+}  // extern "C"

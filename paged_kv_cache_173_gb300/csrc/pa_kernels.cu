@@ -1,0 +1,542 @@
+// pa_kernels.cu -- the paged decode hot path for GB300 (sm_103a).
+//
+//  reshape_and_cache_kernel   scatter new tokens' K/V rows into their slots
+//  paged_decode_kernel        one CTA per (KV head, partition, sequence);
+//                             each warp streams 16-token chunks of its share
+//                             of the partition through a private ring of
+//                             shared-memory stages filled by bulk async copies,
+//                             scores the G query heads of the group against
+//                             K with m16n8k16 MMAs, runs the online softmax in
+//                             float32 and accumulates P.V with MMAs; the warps
+//                             are merged in shared memory at the end
+//  splitk_reduce_kernel       log-sum-exp merge of the partitions
+//
+// The method: "vLLM PagedAttention source walk-through", section 3.4 (block
+// walk, mask, online softmax with correction factor exp(old_max - new_max));
+// "PagedAttention: when the KV cache meets OS paging", sections 3.2 and 5.1
+// (the kernel translates logical to physical blocks itself; table entries are
+// prefetched so the lookups hide under memory latency); "Unveiling the NVIDIA
+// driver stack: GPU page tables and vLLM PagedAttention", sections 6 and 7.3
+// (address arithmetic from the physical block id; adjacent threads read
+// adjacent bytes).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <cmath>
+
+#include "pa_launch.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+constexpr int CHUNK = 16;                       // tokens per pipeline stage
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000;  // 2 s: a stage that takes longer is an error
+
+// ============================================================ reshape_and_cache
+struct ReshapeParams {
+  const uint4* key;
+  const uint4* value;
+  uint4* k_cache;
+  uint4* v_cache;
+  const int64_t* slot_mapping;
+  int64_t num_slots;  // num_blocks * block_size
+  int num_tokens;
+  int num_kv_heads;
+  int row_vecs;  // head_dim * 2 / 16
+};
+
+// One warp per (token, KV head): lanes 0-15 copy the K row, lanes 16-31 the V
+// row, 16 bytes per lane per step.
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_constant__ ReshapeParams p) {
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.num_tokens * p.num_kv_heads) return;
+  const int t = wid / p.num_kv_heads;
+  const int h = wid - t * p.num_kv_heads;
+  const int64_t slot = __ldg(p.slot_mapping + t);
+  if (slot < 0 || slot >= p.num_slots) return;  // padding, or out of the pool
+  const bool is_v = lane >= 16;
+  const uint4* src = (is_v ? p.value : p.key) + (static_cast<int64_t>(t) * p.num_kv_heads + h) * p.row_vecs;
+  uint4* dst = (is_v ? p.v_cache : p.k_cache) + (slot * p.num_kv_heads + h) * p.row_vecs;
+  for (int i = lane & 15; i < p.row_vecs; i += 16) dst[i] = __ldg(src + i);
+}
+
+// ================================================================ decode
+struct DecodeParams {
+  __half* out;
+  const __half* q;
+  const __half* k_cache;
+  const __half* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* ws_o;
+  float* ws_m;
+  float* ws_l;
+  int max_blocks_per_seq;
+  int num_heads;
+  int num_kv_heads;
+  int group;
+  int block_size;
+  int chunks_per_block;
+  int num_blocks;
+  int partition_chunks;
+  int max_num_partitions;
+  float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+};
+
+template <int HEAD_DIM, int NT, int WARPS, int STAGES>
+struct DecodeCfg {
+  static constexpr int ROW_BYTES = HEAD_DIM * 2;
+  static constexpr int PITCH = ROW_BYTES + 16;  // padded row: ldmatrix rows hit distinct banks
+  static constexpr int HALF_BYTES = CHUNK * PITCH;
+  static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
+  static constexpr int RING_BYTES = WARPS * STAGES * STAGE_BYTES;
+  static constexpr int GMAX = NT * 8;
+  static constexpr int MO_PITCH = HEAD_DIM + 4;  // floats; spreads the merge writes over banks
+  static constexpr int MERGE_BYTES = WARPS * GMAX * MO_PITCH * 4 + 2 * WARPS * GMAX * 4 + WARPS * 4;
+  static constexpr int BAR_BYTES = 128 * ((WARPS * STAGES * 8 + 127) / 128);
+  static constexpr int SMEM_BYTES = BAR_BYTES + (RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES);
+};
+
+template <int HEAD_DIM, int NT, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32)
+paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
+  constexpr int KSTEPS = HEAD_DIM / 16;
+  constexpr int PITCH = Cfg::PITCH;
+  constexpr int GMAX = Cfg::GMAX;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint8_t* ring = smem + Cfg::BAR_BYTES;
+
+  const int kvh = blockIdx.x;
+  const int part = blockIdx.y;
+  const int s = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;   // fragment row group
+  const int c4 = lane & 3;   // fragment column pair
+  const int G = p.group;
+  const int H = p.num_heads;
+
+  const int ctx = __ldg(p.context_lens + s);
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  const bool ctx_bad = ctx < 0 || ctx > cap;
+  const int nchunks = ctx_bad ? 0 : (ctx + CHUNK - 1) / CHUNK;
+  const int nparts = (nchunks + p.partition_chunks - 1) / p.partition_chunks;
+
+  if (nchunks == 0) {
+    // Empty sequence -> zeros; impossible context length -> NaN.  Written once.
+    if (part == 0) {
+      const __half v = ctx_bad ? __float2half(NAN) : __float2half(0.f);
+      __half* o = p.out + (static_cast<size_t>(s) * H + kvh * G) * HEAD_DIM;
+      for (int i = threadIdx.x; i < G * HEAD_DIM; i += WARPS * 32) o[i] = v;
+    }
+    return;
+  }
+  if (part >= nparts) return;
+  const bool single = nparts == 1;
+  const int c0 = part * p.partition_chunks;
+  const int c1 = min(c0 + p.partition_chunks, nchunks);
+
+  // ---- per-warp pipeline over chunks first, first + WARPS, ...
+  uint64_t* wbar = bars + warp * STAGES;
+  uint8_t* wring = ring + warp * STAGES * Cfg::STAGE_BYTES;
+  if (lane == 0) {
+    for (int i = 0; i < STAGES; ++i) mbar_init(&wbar[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const int first = c0 + warp;
+  const int nk = first < c1 ? (c1 - first + WARPS - 1) / WARPS : 0;
+
+  // ---- query fragments (B operand of S = K Q^T): lane holds head nt*8+g,
+  //      dims ks*16 + {2c4, 2c4+1} and ks*16 + {2c4+8, 2c4+9}
+  uint32_t qf[KSTEPS][NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hq = nt * 8 + g;
+    const bool hv = hq < G;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        p.q + (static_cast<size_t>(s) * H + kvh * G + (hv ? hq : 0)) * HEAD_DIM);
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+      qf[ks][nt][0] = hv ? __ldg(qrow + ks * 8 + c4) : 0u;
+      qf[ks][nt][1] = hv ? __ldg(qrow + ks * 8 + c4 + 4) : 0u;
+    }
+  }
+
+  // ---- block-table window: lane j holds the physical block of this warp's
+  //      chunk (kbase + j); the next window is fetched 32 chunks ahead
+  const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
+  const int cpb = p.chunks_per_block;
+  auto win_load = [&](int kbase) -> int {
+    const int k = kbase + lane;
+    if (k >= nk) return 0;
+    return __ldg(bt + (first + k * WARPS) / cpb);
+  };
+  int win_cur = win_load(0);
+  int win_nxt = win_load(32);
+  int issued = 0;
+  bool bad = false;
+
+  auto issue_next = [&]() {
+    const int k = issued;
+    if (k > 0 && (k & 31) == 0) {
+      win_cur = win_nxt;
+      win_nxt = win_load(k + 32);
+    }
+    int phys = __shfl_sync(FULL_MASK, win_cur, k & 31);
+    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
+      bad = true;  // never read outside the pool; the result becomes NaN
+      phys = 0;
+    }
+    const int ch = first + k * WARPS;
+    const int row0 = (ch - (ch / cpb) * cpb) * CHUNK;
+    const int slot = k % STAGES;
+    uint8_t* dst = wring + slot * Cfg::STAGE_BYTES;
+    if (lane == 0) mbar_arrive_expect_tx(&wbar[slot], 2 * CHUNK * Cfg::ROW_BYTES);
+    __syncwarp();
+    const int r = lane & 15;
+    const bool is_v = lane >= 16;
+    const size_t row = (static_cast<size_t>(phys) * p.block_size + row0 + r) * p.num_kv_heads + kvh;
+    bulk_copy_g2s(dst + (is_v ? Cfg::HALF_BYTES : 0) + r * PITCH,
+                  (is_v ? p.v_cache : p.k_cache) + row * HEAD_DIM, Cfg::ROW_BYTES, &wbar[slot]);
+    ++issued;
+  };
+
+#pragma unroll 1
+  for (int i = 0; i < STAGES && i < nk; ++i) issue_next();
+
+  float m_run[NT][2], l_run[NT][2];
+  float oacc[KSTEPS][NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt][0] = m_run[nt][1] = -INFINITY;
+    l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+    for (int dm = 0; dm < KSTEPS; ++dm)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) oacc[dm][nt][i] = 0.f;
+  }
+  const float sl2 = p.scale_log2;
+
+  int consumed = 0;
+  bool timed_out = false;
+#pragma unroll 1
+  for (; consumed < nk; ++consumed) {
+    const int k = consumed;
+    const int slot = k % STAGES;
+    const bool ok = mbar_wait_bounded(&wbar[slot], (k / STAGES) & 1, WAIT_LIMIT_NS);
+    if (!__all_sync(FULL_MASK, ok)) {  // a warp-uniform decision
+      timed_out = true;
+      break;
+    }
+    const int ch = first + k * WARPS;
+    const int valid = min(CHUNK, ctx - ch * CHUNK);
+    const uint32_t kb = smem_addr(wring + slot * Cfg::STAGE_BYTES);
+    const uint32_t vb = kb + Cfg::HALF_BYTES;
+
+    // S[16 tokens][8*NT heads] = K Q^T
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    const uint32_t ka = kb + (lane & 15) * PITCH + (lane >> 4) * 16;
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(a, ka + ks * 32);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+    }
+
+    // online softmax (base 2); slots past the context are excluded by select
+    const bool v0 = g < valid;
+    const bool v1 = g + 8 < valid;
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float x0 = v0 ? sacc[nt][0] * sl2 : -INFINITY;
+      const float x1 = v0 ? sacc[nt][1] * sl2 : -INFINITY;
+      const float x2 = v1 ? sacc[nt][2] * sl2 : -INFINITY;
+      const float x3 = v1 ? sacc[nt][3] * sl2 : -INFINITY;
+      float mx0 = fmaxf(x0, x2);
+      float mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, off));
+      }
+      const float mn0 = fmaxf(m_run[nt][0], mx0);
+      const float mn1 = fmaxf(m_run[nt][1], mx1);
+      const float cr0 = ex2(m_run[nt][0] - mn0);
+      const float cr1 = ex2(m_run[nt][1] - mn1);
+      m_run[nt][0] = mn0;
+      m_run[nt][1] = mn1;
+      const uint32_t lo = pack_half2(ex2(x0 - mn0), ex2(x1 - mn1));  // token g
+      const uint32_t hi = pack_half2(ex2(x2 - mn0), ex2(x3 - mn1));  // token g + 8
+      const float2 flo = unpack_half2(lo);
+      const float2 fhi = unpack_half2(hi);
+      // the running sum adds the same rounded weights that multiply V
+      l_run[nt][0] = l_run[nt][0] * cr0 + (flo.x + fhi.x);
+      l_run[nt][1] = l_run[nt][1] * cr1 + (flo.y + fhi.y);
+#pragma unroll
+      for (int dm = 0; dm < KSTEPS; ++dm) {
+        oacc[dm][nt][0] *= cr0;
+        oacc[dm][nt][1] *= cr1;
+        oacc[dm][nt][2] *= cr0;
+        oacc[dm][nt][3] *= cr1;
+      }
+      pb[nt][0] = movmatrix_trans(lo);  // P^T tokens 0-7 as the B fragment
+      pb[nt][1] = movmatrix_trans(hi);  // P^T tokens 8-15
+    }
+
+    // O^T[d][heads] += V^T P^T; V rows past the context are zeroed by select
+    const int t0 = 2 * c4;
+    const uint32_t mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+    const uint32_t mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+    const uint32_t va = vb + ((lane & 7) + ((lane >> 4) << 3)) * PITCH + ((lane >> 3) & 1) * 16;
+#pragma unroll
+    for (int dm = 0; dm < KSTEPS; ++dm) {
+      uint32_t a[4];
+      ldsm_x4_trans(a, va + dm * 32);
+      a[0] &= mlo;
+      a[1] &= mlo;
+      a[2] &= mhi;
+      a[3] &= mhi;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(oacc[dm][nt], a, pb[nt][0], pb[nt][1]);
+    }
+
+    __syncwarp();
+    if (issued < nk) {
+      fence_proxy_async_smem();  // our reads of this slot precede the copy that refills it
+      issue_next();
+    }
+  }
+
+  if (timed_out) {
+    bad = true;
+    // let the copies still in flight land before the shared memory is reused
+    for (int k = consumed; k < issued; ++k)
+      (void)mbar_wait_bounded(&wbar[k % STAGES], (k / STAGES) & 1, WAIT_LIMIT_NS);
+  }
+
+  // ---- per-warp running sums: reduce the per-lane partials over the 8 row groups
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) l_run[nt][j] += __shfl_xor_sync(FULL_MASK, l_run[nt][j], off);
+
+  __syncthreads();  // every warp is done with its ring: reuse it for the merge
+  float* mo = reinterpret_cast<float*>(ring);
+  float* mm = mo + WARPS * GMAX * Cfg::MO_PITCH;
+  float* ml = mm + WARPS * GMAX;
+  int* mbad = reinterpret_cast<int*>(ml + WARPS * GMAX);
+#pragma unroll
+  for (int dm = 0; dm < KSTEPS; ++dm)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int head = nt * 8 + 2 * c4 + (i & 1);
+        const int d = dm * 16 + g + (i >> 1) * 8;
+        mo[(warp * GMAX + head) * Cfg::MO_PITCH + d] = oacc[dm][nt][i];
+      }
+  if (g == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        mm[warp * GMAX + nt * 8 + 2 * c4 + j] = m_run[nt][j];
+        ml[warp * GMAX + nt * 8 + 2 * c4 + j] = l_run[nt][j];
+      }
+  }
+  if (lane == 0) mbad[warp] = bad ? 1 : 0;
+  __syncthreads();
+
+  bool any_bad = false;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w) any_bad |= mbad[w] != 0;
+
+  for (int idx = threadIdx.x; idx < G * HEAD_DIM; idx += WARPS * 32) {
+    const int head = idx / HEAD_DIM;
+    const int d = idx - head * HEAD_DIM;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, mm[w * GMAX + head]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const float f = ex2(mm[w * GMAX + head] - M);  // warps without chunks: 2^-inf = 0
+      L += ml[w * GMAX + head] * f;
+      O += mo[(w * GMAX + head) * Cfg::MO_PITCH + d] * f;
+    }
+    const float r = any_bad ? NAN : O / L;
+    const size_t qrow = static_cast<size_t>(s) * H + kvh * G + head;
+    if (single) {
+      p.out[qrow * HEAD_DIM + d] = __float2half_rn(r);
+    } else {
+      const size_t row = qrow * p.max_num_partitions + part;
+      p.ws_o[row * HEAD_DIM + d] = r;
+      if (d == 0) {
+        p.ws_m[row] = any_bad ? 0.f : M;
+        p.ws_l[row] = any_bad ? 1.f : L;
+      }
+    }
+  }
+}
+
+// ================================================================ reduce
+struct ReduceParams {
+  __half* out;
+  const float* ws_o;
+  const float* ws_m;
+  const float* ws_l;
+  const int32_t* context_lens;
+  int cap;  // max_blocks_per_seq * block_size
+  int num_heads;
+  int partition_size;
+  int max_num_partitions;
+};
+
+// One CTA per (query head, sequence), one thread per output dimension.
+template <int HEAD_DIM>
+__global__ void __launch_bounds__(HEAD_DIM) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
+  const int h = blockIdx.x;
+  const int s = blockIdx.y;
+  const int d = threadIdx.x;
+  const int ctx = __ldg(p.context_lens + s);
+  if (ctx <= 0 || ctx > p.cap) return;
+  const int nparts = (ctx + p.partition_size - 1) / p.partition_size;
+  if (nparts <= 1) return;  // finished by the partition kernel
+  const size_t row0 = (static_cast<size_t>(s) * p.num_heads + h) * p.max_num_partitions;
+  float M = -INFINITY;
+  for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldg(p.ws_m + row0 + q));
+  float L = 0.f, O = 0.f;
+#pragma unroll 4
+  for (int q = 0; q < nparts; ++q) {
+    const float w = __ldg(p.ws_l + row0 + q) * ex2(__ldg(p.ws_m + row0 + q) - M);
+    L += w;
+    O += w * __ldg(p.ws_o + (row0 + q) * HEAD_DIM + d);
+  }
+  p.out[(static_cast<size_t>(s) * p.num_heads + h) * HEAD_DIM + d] = __float2half_rn(O / L);
+}
+
+// ================================================================ launchers
+template <typename Kernel>
+cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done_mask.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+template <int HEAD_DIM, int NT>
+cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int WARPS = 4;
+  constexpr int STAGES = 3;
+  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
+  auto kern = paged_decode_kernel<HEAD_DIM, NT, WARPS, STAGES>;
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
+  if (e != cudaSuccess) return e;
+
+  DecodeParams p;
+  p.out = static_cast<__half*>(a.out);
+  p.q = static_cast<const __half*>(a.q);
+  p.k_cache = static_cast<const __half*>(a.k_cache);
+  p.v_cache = static_cast<const __half*>(a.v_cache);
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  const size_t rows = ws_rows(a.num_seqs, a.num_heads, a.max_num_partitions);
+  p.ws_o = a.ws;
+  p.ws_m = a.ws ? a.ws + rows * HEAD_DIM : nullptr;
+  p.ws_l = a.ws ? a.ws + rows * HEAD_DIM + rows : nullptr;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_heads = a.num_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_heads / a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.chunks_per_block = a.block_size / CHUNK;
+  p.num_blocks = a.num_blocks;
+  p.partition_chunks = a.partition_size / CHUNK;
+  p.max_num_partitions = a.max_num_partitions;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+
+  dim3 grid(a.num_kv_heads, a.max_num_partitions, a.num_seqs);
+  kern<<<grid, WARPS * 32, Cfg::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int HEAD_DIM>
+cudaError_t launch_reduce_t(const ReduceArgs& a, cudaStream_t stream) {
+  ReduceParams p;
+  const size_t rows = ws_rows(a.num_seqs, a.num_heads, a.max_num_partitions);
+  p.out = static_cast<__half*>(a.out);
+  p.ws_o = a.ws;
+  p.ws_m = a.ws + rows * HEAD_DIM;
+  p.ws_l = a.ws + rows * HEAD_DIM + rows;
+  p.context_lens = a.context_lens;
+  p.cap = a.max_blocks_per_seq * a.block_size;
+  p.num_heads = a.num_heads;
+  p.partition_size = a.partition_size;
+  p.max_num_partitions = a.max_num_partitions;
+  dim3 grid(a.num_heads, a.num_seqs);
+  splitk_reduce_kernel<HEAD_DIM><<<grid, HEAD_DIM, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) {
+  if (a.num_tokens == 0) return cudaSuccess;
+  ReshapeParams p;
+  p.key = static_cast<const uint4*>(a.key);
+  p.value = static_cast<const uint4*>(a.value);
+  p.k_cache = static_cast<uint4*>(a.k_cache);
+  p.v_cache = static_cast<uint4*>(a.v_cache);
+  p.slot_mapping = a.slot_mapping;
+  p.num_slots = static_cast<int64_t>(a.num_blocks) * a.block_size;
+  p.num_tokens = a.num_tokens;
+  p.num_kv_heads = a.num_kv_heads;
+  p.row_vecs = a.head_dim * 2 / 16;
+  const int64_t warps = static_cast<int64_t>(a.num_tokens) * a.num_kv_heads;
+  const int blocks = static_cast<int>((warps + 7) / 8);
+  reshape_and_cache_kernel<<<blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  const int G = a.num_heads / a.num_kv_heads;
+  const bool two = G > 8;
+  switch (a.head_dim) {
+    case 64: return two ? launch_decode_t<64, 2>(a, stream) : launch_decode_t<64, 1>(a, stream);
+    case 128: return two ? launch_decode_t<128, 2>(a, stream) : launch_decode_t<128, 1>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_splitk_reduce(const ReduceArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  switch (a.head_dim) {
+    case 64: return launch_reduce_t<64>(a, stream);
+    case 128: return launch_reduce_t<128>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pa

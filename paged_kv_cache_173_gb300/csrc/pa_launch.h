@@ -1,0 +1,67 @@
+// pa_launch.h -- internal interface between the C entry points (pa_abi.cu)
+// and the kernel launchers (pa_kernels.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct ReshapeArgs {
+  const void* key;
+  const void* value;
+  void* k_cache;
+  void* v_cache;
+  const int64_t* slot_mapping;
+  int num_tokens;
+  int num_blocks;
+  int block_size;
+  int num_kv_heads;
+  int head_dim;
+};
+
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* ws;  // split-K workspace (nullptr for single-pass decode)
+  int max_blocks_per_seq;
+  int num_seqs;
+  int num_heads;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int num_blocks;
+  float scale;
+  int partition_size;      // tokens; single-pass decode uses max_blocks_per_seq * block_size
+  int max_num_partitions;  // grid extent along partitions (1 for single-pass)
+};
+
+struct ReduceArgs {
+  void* out;
+  const float* ws;
+  const int32_t* context_lens;
+  int max_blocks_per_seq;
+  int block_size;
+  int num_seqs;
+  int num_heads;
+  int head_dim;
+  int partition_size;
+  int max_num_partitions;
+};
+
+cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const ReduceArgs& a, cudaStream_t stream);
+
+// Workspace geometry shared by the partition kernel and the reduce kernel:
+// o [S][H][P][d], then m [S][H][P], then l [S][H][P], float32.
+inline size_t ws_rows(int num_seqs, int num_heads, int max_num_partitions) {
+  return static_cast<size_t>(num_seqs) * num_heads * max_num_partitions;
+}
+
+}  // namespace pa

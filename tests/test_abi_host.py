@@ -1,0 +1,123 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host (no kernel is launched, so no GPU is needed)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_173_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(pa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from paged_kv_cache_173_gb300.build import build_library
+    build_library()
+    return _lib.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared_functions()
+    assert {"pa_reshape_and_cache", "pa_decode", "pa_decode_splitk", "pa_splitk_reduce",
+            "pa_splitk_workspace_bytes", "pa_status_string", "pa_last_error"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in _lib.SIGNATURES, f"{n} has no binding signature"
+
+
+def test_status_strings(L):
+    assert _lib.status_name(0) == "PA_OK"
+    assert _lib.status_name(-1) == "PA_ERR_INVALID_ARG"
+    assert _lib.status_name(-2) == "PA_ERR_UNSUPPORTED"
+    assert _lib.status_name(-3) == "PA_ERR_CUDA"
+    assert _lib.status_name(7) == "PA_UNKNOWN_STATUS"
+
+
+def test_workspace_size(L):
+    assert L.pa_splitk_workspace_bytes(4, 32, 128, 256) == 4 * 32 * 256 * (128 + 2) * 4
+    assert L.pa_splitk_workspace_bytes(0, 32, 128, 256) == 0
+    assert L.pa_splitk_workspace_bytes(4, 32, 128, -1) == 0
+
+
+A = 1 << 20  # a fake, 16-byte aligned "device" address: never dereferenced on these paths
+
+
+def _decode(L, **kw):
+    args = dict(out=A, q=A, k=A, v=A, bt=A, M=8, cl=A, S=2, H=8, Hk=2, d=128, B=16, N=32,
+                scale=0.1, dtype=0, stream=None)
+    args.update(kw)
+    return L.pa_decode(args["out"], args["q"], args["k"], args["v"], args["bt"], args["M"], args["cl"],
+                       args["S"], args["H"], args["Hk"], args["d"], args["B"], args["N"], args["scale"],
+                       args["dtype"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), _lib.PA_ERR_UNSUPPORTED),
+    (dict(dtype=1), _lib.PA_ERR_UNSUPPORTED),
+    (dict(H=6, Hk=4), _lib.PA_ERR_UNSUPPORTED),
+    (dict(H=64, Hk=2), _lib.PA_ERR_UNSUPPORTED),
+    (dict(B=8), _lib.PA_ERR_UNSUPPORTED),
+    (dict(B=24), _lib.PA_ERR_UNSUPPORTED),
+    (dict(S=-1), _lib.PA_ERR_INVALID_ARG),
+    (dict(S=70000), _lib.PA_ERR_UNSUPPORTED),
+    (dict(M=0), _lib.PA_ERR_INVALID_ARG),
+    (dict(N=0), _lib.PA_ERR_INVALID_ARG),
+    (dict(q=None), _lib.PA_ERR_INVALID_ARG),
+    (dict(bt=None), _lib.PA_ERR_INVALID_ARG),
+    (dict(out=A + 2), _lib.PA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), _lib.PA_ERR_INVALID_ARG),
+])
+def test_decode_rejects_bad_arguments(L, kw, status):
+    assert _decode(L, **kw) == status
+    assert _lib.last_error() != ""
+
+
+def test_empty_batch_is_a_no_op(L):
+    assert _decode(L, S=0, q=None, out=None) == _lib.PA_OK
+    assert L.pa_reshape_and_cache(A, A, A, A, A, 0, 8, 16, 2, 128, 0, None) == _lib.PA_OK
+
+
+def _splitk(L, **kw):
+    args = dict(ps=64, P=2, ws=A, wsb=10 ** 9, B=16, M=8)
+    args.update(kw)
+    return L.pa_decode_splitk(A, A, A, A, A, args["M"], A, 2, 8, 2, 128, args["B"], 32, 0.1, 0,
+                              args["ps"], args["P"], args["ws"], args["wsb"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(ps=40), dict(ps=0), dict(P=1), dict(ws=None), dict(wsb=100),
+                                dict(ws=A + 4), dict(P=70000)])
+def test_splitk_rejects_bad_arguments(L, kw):
+    assert _splitk(L, **kw) in (_lib.PA_ERR_INVALID_ARG, _lib.PA_ERR_UNSUPPORTED)
+
+
+def test_reduce_rejects_bad_arguments(L):
+    bad_ps = L.pa_splitk_reduce(A, A, 10 ** 9, A, 8, 16, 2, 8, 128, 40, 8, 0, None)
+    assert bad_ps == _lib.PA_ERR_INVALID_ARG
+    small_ws = L.pa_splitk_reduce(A, A, 16, A, 8, 16, 2, 8, 128, 64, 2, 0, None)
+    assert small_ws == _lib.PA_ERR_INVALID_ARG
+    assert "workspace" in _lib.last_error()
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, A, A, A, A, 4, 8, 16, 2, 100, 0, None), _lib.PA_ERR_UNSUPPORTED),   # head_dim % 8
+    ((A, A, A, A, A, -1, 8, 16, 2, 128, 0, None), _lib.PA_ERR_INVALID_ARG),  # negative T
+    ((A, A, A, A, None, 4, 8, 16, 2, 128, 0, None), _lib.PA_ERR_INVALID_ARG),
+    ((A, A, A + 8, A, A, 4, 8, 16, 2, 128, 0, None), _lib.PA_ERR_INVALID_ARG),
+    ((A, A, A, A, A, 4, 8, 16, 2, 128, 3, None), _lib.PA_ERR_UNSUPPORTED),
+])
+def test_reshape_rejects_bad_arguments(L, args, status):
+    assert L.pa_reshape_and_cache(*args) == status

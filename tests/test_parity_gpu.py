@@ -1,0 +1,262 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+* reshape_and_cache: the whole pools, byte for byte, after the write.
+* decode (single pass and split-K + reduce): max abs error <= 2e-3 against the
+  float64 oracle (fp16 inputs, fp32 accumulation, fp16 output).
+* invariants that must hold bit for bit on the GPU: relabelled physical
+  blocks, shared vs duplicated prefix, ctx = 1 returns V, run-to-run
+  determinism; poisoned (NaN) slots never reach the output.
+* device-value outcomes: ctx = 0 gives zeros, an impossible ctx or block id
+  gives NaN for the affected group only.
+
+Small cases span several 16-token chunks, warps and partitions with a ragged
+tail; the full-size workloads are checked on a sample of sequences that the
+oracle computes one by one.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import c_oracle
+from paged_kv_cache_173_gb300 import api, workloads
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def T(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+
+
+class Dev:
+    """A batch moved to the GPU, with the cache write applied."""
+
+    def __init__(self, b: workloads.PagedBatch, write: bool = True):
+        self.b = b
+        self.k_cache = T(b.k_cache)
+        self.v_cache = T(b.v_cache)
+        self.q = T(b.q)
+        self.bt = T(b.block_tables)
+        self.cl = T(b.context_lens)
+        if write:
+            api.pa_reshape_and_cache(T(b.key), T(b.value), self.k_cache, self.v_cache, T(b.slot_mapping))
+
+    def decode(self, cl=None, bt=None):
+        out = torch.empty_like(self.q)
+        api.pa_decode(out, self.q, self.k_cache, self.v_cache, self.bt if bt is None else bt,
+                      self.cl if cl is None else cl, self.b.scale)
+        return out
+
+    def splitk(self, ps, cl=None, bt=None):
+        b = self.b
+        P = api.max_num_partitions_for(b.max_blocks_per_seq, b.block_size, ps)
+        ws = api.alloc_splitk_workspace(b.num_seqs, b.num_heads, b.head_dim, P, dev())
+        ws.fill_(float("nan"))  # the reduce must read only what the partitions wrote
+        out = torch.empty_like(self.q)
+        cl = self.cl if cl is None else cl
+        api.pa_decode_splitk(out, self.q, self.k_cache, self.v_cache, self.bt if bt is None else bt, cl,
+                             b.scale, ps, ws, P)
+        api.pa_splitk_reduce(out, ws, cl, b.max_blocks_per_seq, b.block_size, ps, P)
+        return out
+
+
+def oracle_out(b, seqs=None):
+    kc, vc = c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
+    if seqs is None:
+        return c_oracle.decode(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+    seqs = np.asarray(seqs)
+    return c_oracle.decode(b.q[seqs], kc, vc, b.block_tables[seqs], b.context_lens[seqs], b.scale)
+
+
+def max_err(gpu_out, ref):
+    g = gpu_out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(g).all(), "non-finite output"
+    return float(np.max(np.abs(g - ref)))
+
+
+SMALL = {
+    "tiny": lambda: workloads.tiny(),
+    "llama3-8b-s8": lambda: workloads.llama3_8b(num_seqs=8),
+    "llama2-70b-b16": lambda: workloads.llama2_70b(num_seqs=2, ctx=3000, block_size=16),
+    "llama2-70b-b32": lambda: workloads.llama2_70b(num_seqs=2, ctx=3001, block_size=32),
+    "long-context-s": lambda: workloads.long_context(ctxs=(1000, 4097, 7000)),
+    "shared-prefix-s": lambda: workloads.shared_prefix(num_prompts=2, samples=4, prompt_len=256,
+                                                       max_suffix=100),
+    "mha-d64-b64": lambda: workloads.build_batch(name="d64", seed=4, context_lens=[5, 64, 65, 700, 1],
+                                                 num_heads=6, num_kv_heads=6, head_dim=64,
+                                                 block_size=64),
+    "gqa16-d128-b256": lambda: workloads.build_batch(name="g16", seed=5, context_lens=[300, 513, 1],
+                                                     num_heads=32, num_kv_heads=2, head_dim=128,
+                                                     block_size=256),
+    "gqa3-d64-b16": lambda: workloads.build_batch(name="g3", seed=6, context_lens=[17, 250, 31],
+                                                  num_heads=9, num_kv_heads=3, head_dim=64,
+                                                  block_size=16),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_reshape_and_cache_is_bit_exact(name):
+    b = SMALL[name]()
+    d = Dev(b)
+    ref_k, ref_v = c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
+    torch.cuda.synchronize()
+    assert np.array_equal(d.k_cache.cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
+    assert np.array_equal(d.v_cache.cpu().numpy().view(np.uint16), ref_v.view(np.uint16))
+
+
+def test_reshape_and_cache_skips_padding_and_out_of_range_slots():
+    b = workloads.llama3_8b(num_seqs=6, max_ctx=200)
+    sm = b.slot_mapping.copy()
+    sm[1] = -1
+    sm[3] = b.num_blocks * b.block_size + 5  # outside the pool: not written
+    d = Dev(b, write=False)
+    api.pa_reshape_and_cache(T(b.key), T(b.value), d.k_cache, d.v_cache, T(sm))
+    ok = sm.copy()
+    ok[3] = -1
+    ref_k, ref_v = c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, ok)
+    torch.cuda.synchronize()
+    assert np.array_equal(d.k_cache.cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
+    assert np.array_equal(d.v_cache.cpu().numpy().view(np.uint16), ref_v.view(np.uint16))
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_decode_matches_oracle(name):
+    b = SMALL[name]()
+    ref = oracle_out(b)
+    d = Dev(b)
+    assert max_err(d.decode(), ref) <= TOL
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("ps_blocks", [1, 3, 8, 32])
+def test_splitk_matches_oracle(name, ps_blocks):
+    b = SMALL[name]()
+    ref = oracle_out(b)
+    d = Dev(b)
+    assert max_err(d.splitk(ps_blocks * b.block_size), ref) <= TOL
+
+
+def test_ctx_one_returns_v_exactly():
+    b = workloads.tiny()
+    d = Dev(b)
+    out = d.decode().cpu().numpy()
+    sk = d.splitk(16).cpu().numpy()
+    vc = d.v_cache.cpu().numpy()
+    blk = b.block_tables[0, 0]
+    for h in range(b.num_heads):
+        want = vc[blk, 0, h // b.group_size].view(np.uint16)
+        assert np.array_equal(out[0, h].view(np.uint16), want)
+        assert np.array_equal(sk[0, h].view(np.uint16), want)
+
+
+def test_relabelled_blocks_and_determinism_are_bitwise():
+    b = workloads.llama3_8b(num_seqs=6, max_ctx=900)
+    d = Dev(b)
+    base = d.decode().cpu().numpy()
+    base_sk = d.splitk(128).cpu().numpy()
+    assert np.array_equal(d.decode().cpu().numpy().view(np.uint16), base.view(np.uint16))
+    pi = np.random.default_rng(2).permutation(b.num_blocks)
+    pit = torch.from_numpy(pi).to(dev())
+    k2 = torch.empty_like(d.k_cache)
+    v2 = torch.empty_like(d.v_cache)
+    k2[pit] = d.k_cache
+    v2[pit] = d.v_cache
+    bt2 = torch.where(d.bt >= 0, pit[d.bt.clamp(min=0).long()].int(), d.bt)
+    d.k_cache, d.v_cache = k2, v2
+    out = d.decode(bt=bt2).cpu().numpy()
+    sk = d.splitk(128, bt=bt2).cpu().numpy()
+    assert np.array_equal(out.view(np.uint16), base.view(np.uint16))
+    assert np.array_equal(sk.view(np.uint16), base_sk.view(np.uint16))
+
+
+def test_shared_prefix_equals_duplicated_blocks_bitwise():
+    b = workloads.shared_prefix(num_prompts=2, samples=4, prompt_len=128, max_suffix=60)
+    d = Dev(b)
+    shared = d.decode().cpu().numpy()
+    npre = 128 // b.block_size
+    bt = b.block_tables.copy()
+    kc = d.k_cache.cpu().numpy()
+    vc = d.v_cache.cpu().numpy()
+    ek, ev = [], []
+    nxt = b.num_blocks
+    for s in range(b.num_seqs):
+        for i in range(npre):
+            ek.append(kc[bt[s, i]])
+            ev.append(vc[bt[s, i]])
+            bt[s, i] = nxt
+            nxt += 1
+    d.k_cache = T(np.concatenate([kc, np.stack(ek)]))
+    d.v_cache = T(np.concatenate([vc, np.stack(ev)]))
+    dup = d.decode(bt=T(bt)).cpu().numpy()
+    assert np.array_equal(shared.view(np.uint16), dup.view(np.uint16))
+
+
+def test_device_value_outcomes():
+    b = workloads.llama3_8b(num_seqs=5, max_ctx=400)
+    d = Dev(b)
+    ref = oracle_out(b)
+    cl = b.context_lens.copy()
+    cl[1] = 0                                   # empty sequence -> zeros
+    cl[2] = b.max_blocks_per_seq * b.block_size + 1  # impossible -> NaN
+    bt = b.block_tables.copy()
+    bt[3, 0] = b.num_blocks + 7                 # block id outside the pool -> NaN for seq 3
+    for out in (d.decode(cl=T(cl), bt=T(bt)), d.splitk(64, cl=T(cl), bt=T(bt))):
+        o = out.float().cpu().numpy()
+        assert np.all(o[1] == 0)
+        assert np.isnan(o[2]).all()
+        assert np.isnan(o[3]).all()
+        for s in (0, 4):
+            assert np.max(np.abs(o[s] - ref[s])) <= TOL
+
+
+def test_empty_batch():
+    b = workloads.tiny()
+    d = Dev(b)
+    out = torch.empty((0, b.num_heads, b.head_dim), dtype=torch.float16, device=dev())
+    api.pa_decode(out, d.q[:0], d.k_cache, d.v_cache, d.bt[:0], d.cl[:0], b.scale)
+
+
+# ------------------------------------------------------------------ full size
+FULL = {
+    "llama3-8b": (lambda: workloads.llama3_8b(), 512, [0, 17, 40, 63]),
+    "llama2-70b-b16": (lambda: workloads.llama2_70b(block_size=16), 512, [0, 31]),
+    "llama2-70b-b32": (lambda: workloads.llama2_70b(block_size=32), 512, [5]),
+    "long-context": (lambda: workloads.long_context(), 512, [0, 3]),
+    "shared-prefix": (lambda: workloads.shared_prefix(), 512, [0, 7, 64, 127]),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_workloads_on_sampled_sequences(name):
+    make, ps, seqs = FULL[name]
+    b = make()
+    d = Dev(b)
+    sk = d.splitk(ps).float().cpu().numpy()
+    single = d.decode().float().cpu().numpy()
+    assert np.isfinite(sk).all() and np.isfinite(single).all()
+    ref = oracle_out(b, seqs)
+    for i, s in enumerate(seqs):
+        assert np.max(np.abs(sk[s] - ref[i])) <= TOL
+        assert np.max(np.abs(single[s] - ref[i])) <= TOL
+    # sequences not sampled: split-K and single pass agree with each other
+    assert np.max(np.abs(sk - single)) <= TOL
+    # the cache write at full size, byte for byte
+    ref_k, ref_v = c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
+    assert np.array_equal(d.k_cache.cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
+    assert np.array_equal(d.v_cache.cpu().numpy().view(np.uint16), ref_v.view(np.uint16))

@@ -214,11 +214,11 @@ def run_gpu(args, rank: int, world: int):
     with torch.cuda.graph(g_plain, stream=stream):
         for i in range(G):
             step(i)
+    # The last G steps of the timed region run eagerly with an event between
+    # kernels (events recorded inside a captured graph cannot be timed).  The
+    # host enqueues them while the GPU is still replaying the graphs, so the
+    # device runs them back to back.
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(G)]
-    g_ev = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_ev, stream=stream):
-        for i in range(G):
-            step(i, evs[i])
     n_plain = (K - G) // G
     tail = K - G - n_plain * G
     g_tail = None
@@ -230,9 +230,10 @@ def run_gpu(args, rank: int, world: int):
     # untimed replays of each graph
     with torch.cuda.stream(stream):
         g_plain.replay()
-        g_ev.replay()
         if g_tail:
             g_tail.replay()
+        for i in range(G):
+            step(i, evs[i])
     torch.cuda.synchronize(dev)
 
     import torch.distributed as dist
@@ -251,7 +252,8 @@ def run_gpu(args, rank: int, world: int):
             g_plain.replay()
         if g_tail:
             g_tail.replay()
-        g_ev.replay()  # the last G steps carry per-kernel events
+        for i in range(G):  # the last G steps carry per-kernel events
+            step(i, evs[i])
         e_end.record()
     torch.cuda.synchronize(dev)
     if distributed:

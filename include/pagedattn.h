@@ -16,8 +16,9 @@
  * Conventions for every entry point:
  *  - Pointers are DEVICE pointers owned by the caller.  The library allocates
  *    nothing and keeps no state between calls except a per-thread text of
- *    the last error (pa_last_error) and a per-device record of which kernel
- *    attributes it has already set.
+ *    the last error (pa_last_error), a per-device record of which kernel
+ *    attributes it has already set, and the fixed device array that
+ *    pa_decode_splitk_static uses as its workspace.
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL means the legacy default stream).  The caller synchronises.
  *  - The return value is a pa_status.  Arguments are checked on the host
@@ -187,6 +188,42 @@ int pa_splitk_reduce(void* out, const void* workspace, size_t workspace_bytes,
                      const int32_t* context_lens, int max_blocks_per_seq, int block_size,
                      int num_seqs, int num_heads, int head_dim, int partition_size,
                      int max_num_partitions, int dtype, void* stream);
+
+/*
+ * pa_decode_splitk_static -- pa_decode_splitk followed by pa_splitk_reduce,
+ * with the split-K workspace taken from a fixed array inside the library
+ * instead of from the caller.  The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory -- a serving
+ * runtime that has reserved nearly all device memory for its KV-cache pool
+ * and hands out no scratch, a host program that reaches the library only
+ * through this C ABI and owns no GPU allocator, or a decode loop that must
+ * not call cudaMalloc (which can synchronise the device).  It allocates
+ * nothing: the caller passes inputs and outputs as for pa_decode_splitk
+ * (with max_num_partitions = ceil(max_blocks_per_seq * block_size /
+ * partition_size)), and the partials go to a file-scope device array of
+ * PA_STATIC_SCRATCH_BYTES, which every GPU that loads the library holds
+ * until the process exits.
+ *
+ *  - A batch whose workspace (pa_splitk_workspace_bytes) exceeds
+ *    PA_STATIC_SCRATCH_BYTES is rejected with PA_ERR_UNSUPPORTED and a
+ *    message; nothing is launched.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and remembers it;
+ *    make that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its partials
+ *    there.  Nothing in it needs to start at zero: each call writes every
+ *    row it later reads.  Calls whose kernels overlap on the GPU (different
+ *    streams, or concurrent host threads) race on the array: order them.
+ *
+ * Result, arguments and device-value outcomes as pa_decode_splitk + reduce.
+ */
+#define PA_STATIC_SCRATCH_BYTES ((size_t)32 * 1024 * 1024)
+
+int pa_decode_splitk_static(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int num_heads,
+                            int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                            float scale, int dtype, int partition_size, void* stream);
 
 /* Fixed text naming a status code. */
 const char* pa_status_string(int status);

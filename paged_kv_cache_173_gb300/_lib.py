@@ -31,6 +31,8 @@ SIGNATURES = {
     "pa_decode_splitk": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I,
                               _P, _SZ, _P]),
     "pa_splitk_reduce": (_I, [_P, _P, _SZ, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "pa_decode_splitk_static": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                                     _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
     "pa_last_error": (ctypes.c_char_p, []),
 }

@@ -125,6 +125,22 @@ def pa_splitk_reduce(out: torch.Tensor, workspace: torch.Tensor, context_lens: t
     _lib.check("pa_splitk_reduce", st)
 
 
+def pa_decode_splitk_static(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, scale: float, partition_size: int,
+                            stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Split-K decode + reduce for callers that cannot allocate device memory:
+    the partials go to a fixed array inside the library (at most
+    PA_STATIC_SCRATCH_BYTES, 32 MiB).  Calls that overlap on the GPU race on
+    that array; the first call on a device should precede any stream capture."""
+    dev, S, H, d, N, B, Hk, M, (po, pq, pk, pv, pbt), pcl = _decode_common(
+        out, q, k_cache, v_cache, block_tables, context_lens)
+    st = _lib.lib().pa_decode_splitk_static(po, pq, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N,
+                                            float(scale), PA_FP16, int(partition_size),
+                                            _stream_ptr(q, stream))
+    _lib.check("pa_decode_splitk_static", st)
+
+
 def pa_status_string(status: int) -> str:
     return _lib.status_name(status)
 

@@ -101,6 +101,18 @@ int check_splitk(int max_blocks_per_seq, int block_size, int partition_size, int
 
 }  // namespace
 
+namespace pa {
+
+int set_last_error(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+}  // namespace pa
+
 extern "C" {
 
 const char* pa_status_string(int status) {

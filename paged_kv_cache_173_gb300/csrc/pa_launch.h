@@ -54,6 +54,9 @@ struct ReduceArgs {
   int max_num_partitions;
 };
 
+// Record a formatted message as the calling thread's last error; returns status.
+int set_last_error(int status, const char* fmt, ...);
+
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceArgs& a, cudaStream_t stream);

@@ -30,7 +30,8 @@
  *  - Tensor pointers must be 16-byte aligned and the tensors contiguous in
  *    the layouts given.  Element type: dtype = PA_FP16 (IEEE binary16).
  *    All arithmetic after the loads is float32.
- *  - Supported shapes: head_dim in {64, 128}; block_size in {16, 32};
+ *  - Supported shapes: head_dim in {64, 128}; block_size in {16, 32, 64,
+ *    128, 256};
  *    num_heads a multiple of num_kv_heads with num_heads / num_kv_heads <= 16;
  *    num_seqs <= 65535.
  */

@@ -36,6 +36,9 @@ int cuda_status(cudaError_t e, const char* what) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// 16, 32, 64, 128 or 256 tokens per block.
+bool block_size_supported(int b) { return b >= 16 && b <= 256 && (b & (b - 1)) == 0; }
+
 // Shape checks shared by every decode entry point.
 int check_decode(const void* out, const void* q, const void* k_cache, const void* v_cache,
                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
@@ -44,8 +47,8 @@ int check_decode(const void* out, const void* q, const void* k_cache, const void
   if (dtype != PA_FP16) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 only)", dtype);
   if (head_dim != 64 && head_dim != 128)
     return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (64 or 128)", head_dim);
-  if (block_size < 16 || block_size > 256 || block_size % 16 != 0)
-    return fail(PA_ERR_UNSUPPORTED, "block_size %d is not supported (a multiple of 16, at most 256)",
+  if (!block_size_supported(block_size))
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d is not supported (16, 32, 64, 128 or 256)",
                 block_size);
   if (num_heads <= 0 || num_kv_heads <= 0)
     return fail(PA_ERR_INVALID_ARG, "num_heads (%d) and num_kv_heads (%d) must be positive", num_heads,
@@ -231,7 +234,7 @@ int pa_splitk_reduce(void* out, const void* workspace, size_t workspace_bytes,
   if (dtype != PA_FP16) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 only)", dtype);
   if (head_dim != 64 && head_dim != 128)
     return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (64 or 128)", head_dim);
-  if (block_size < 16 || block_size > 256 || block_size % 16 != 0)
+  if (!block_size_supported(block_size))
     return fail(PA_ERR_UNSUPPORTED, "block_size %d is not supported", block_size);
   if (num_seqs < 0 || num_heads <= 0)
     return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0 and num_heads > 0");

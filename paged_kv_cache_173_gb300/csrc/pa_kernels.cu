@@ -82,7 +82,7 @@ struct DecodeParams {
   int num_kv_heads;
   int group;
   int block_size;
-  int chunks_per_block;
+  int chunks_per_block_log2;  // block_size / 16 is a power of two
   int num_blocks;
   int partition_chunks;
   int max_num_partitions;
@@ -125,36 +125,15 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int G = p.group;
   const int H = p.num_heads;
 
+  // Loads that do not depend on the context length go out first, so that
+  // their latencies overlap with the one of context_lens[s].
   const int ctx = __ldg(p.context_lens + s);
-  const int cap = p.max_blocks_per_seq * p.block_size;
-  const bool ctx_bad = ctx < 0 || ctx > cap;
-  const int nchunks = ctx_bad ? 0 : (ctx + CHUNK - 1) / CHUNK;
-  const int nparts = (nchunks + p.partition_chunks - 1) / p.partition_chunks;
-
-  if (nchunks == 0) {
-    // Empty sequence -> zeros; impossible context length -> NaN.  Written once.
-    if (part == 0) {
-      const __half v = ctx_bad ? __float2half(NAN) : __float2half(0.f);
-      __half* o = p.out + (static_cast<size_t>(s) * H + kvh * G) * HEAD_DIM;
-      for (int i = threadIdx.x; i < G * HEAD_DIM; i += WARPS * 32) o[i] = v;
-    }
-    return;
-  }
-  if (part >= nparts) return;
-  const bool single = nparts == 1;
   const int c0 = part * p.partition_chunks;
-  const int c1 = min(c0 + p.partition_chunks, nchunks);
-
-  // ---- per-warp pipeline over chunks first, first + WARPS, ...
-  uint64_t* wbar = bars + warp * STAGES;
-  uint8_t* wring = ring + warp * STAGES * Cfg::STAGE_BYTES;
-  if (lane == 0) {
-    for (int i = 0; i < STAGES; ++i) mbar_init(&wbar[i], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
+  const int cpb_log2 = p.chunks_per_block_log2;
+  const int table_chunks = p.max_blocks_per_seq << cpb_log2;
+  const int cmax = min(c0 + p.partition_chunks, table_chunks);  // chunks the table can hold
   const int first = c0 + warp;
-  const int nk = first < c1 ? (c1 - first + WARPS - 1) / WARPS : 0;
+  const int nk_cap = first < cmax ? (cmax - first + WARPS - 1) / WARPS : 0;
 
   // ---- query fragments (B operand of S = K Q^T): lane holds head nt*8+g,
   //      dims ks*16 + {2c4, 2c4+1} and ks*16 + {2c4+8, 2c4+9}
@@ -173,16 +152,45 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   }
 
   // ---- block-table window: lane j holds the physical block of this warp's
-  //      chunk (kbase + j); the next window is fetched 32 chunks ahead
+  //      chunk (kbase + j); the next window is fetched 32 chunks ahead.  Only
+  //      entries inside the table row are read; those past the context are
+  //      fetched but never used.
   const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
-  const int cpb = p.chunks_per_block;
   auto win_load = [&](int kbase) -> int {
     const int k = kbase + lane;
-    if (k >= nk) return 0;
-    return __ldg(bt + (first + k * WARPS) / cpb);
+    if (k >= nk_cap) return 0;
+    return __ldg(bt + ((first + k * WARPS) >> cpb_log2));
   };
   int win_cur = win_load(0);
   int win_nxt = win_load(32);
+
+  uint64_t* wbar = bars + warp * STAGES;
+  uint8_t* wring = ring + warp * STAGES * Cfg::STAGE_BYTES;
+  if (lane == 0) {
+    for (int i = 0; i < STAGES; ++i) mbar_init(&wbar[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  const bool ctx_bad = ctx < 0 || ctx > cap;
+  const int nchunks = ctx_bad ? 0 : (ctx + CHUNK - 1) / CHUNK;
+  const int nparts = (nchunks + p.partition_chunks - 1) / p.partition_chunks;
+
+  if (nchunks == 0) {
+    // Empty sequence -> zeros; impossible context length -> NaN.  Written once.
+    if (part == 0) {
+      const __half v = ctx_bad ? __float2half(NAN) : __float2half(0.f);
+      __half* o = p.out + (static_cast<size_t>(s) * H + kvh * G) * HEAD_DIM;
+      for (int i = threadIdx.x; i < G * HEAD_DIM; i += WARPS * 32) o[i] = v;
+    }
+    return;
+  }
+  if (part >= nparts) return;
+  const bool single = nparts == 1;
+  const int c1 = min(c0 + p.partition_chunks, nchunks);
+  const int nk = first < c1 ? (c1 - first + WARPS - 1) / WARPS : 0;  // <= nk_cap
+
   int issued = 0;
   bool bad = false;
 
@@ -198,7 +206,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
       phys = 0;
     }
     const int ch = first + k * WARPS;
-    const int row0 = (ch - (ch / cpb) * cpb) * CHUNK;
+    const int row0 = (ch & ((1 << cpb_log2) - 1)) * CHUNK;
     const int slot = k % STAGES;
     uint8_t* dst = wring + slot * Cfg::STAGE_BYTES;
     if (lane == 0) mbar_arrive_expect_tx(&wbar[slot], 2 * CHUNK * Cfg::ROW_BYTES);
@@ -243,18 +251,26 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     const uint32_t kb = smem_addr(wring + slot * Cfg::STAGE_BYTES);
     const uint32_t vb = kb + Cfg::HALF_BYTES;
 
-    // S[16 tokens][8*NT heads] = K Q^T
-    float sacc[NT][4];
+    // S[16 tokens][8*NT heads] = K Q^T, as two independent MMA chains (even
+    // and odd k-steps) that are added at the end
+    float sacc[NT][4], sacc2[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sacc[nt][i] = sacc2[nt][i] = 0.f;
     const uint32_t ka = kb + (lane & 15) * PITCH + (lane >> 4) * 16;
 #pragma unroll
     for (int ks = 0; ks < KSTEPS; ++ks) {
       uint32_t a[4];
       ldsm_x4(a, ka + ks * 32);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+      for (int nt = 0; nt < NT; ++nt)
+        mma_f16_16816((ks & 1) ? sacc2[nt] : sacc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sacc[nt][i] += sacc2[nt][i];
 
     // online softmax (base 2); slots past the context are excluded by select
     const bool v0 = g < valid;
@@ -277,6 +293,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
       const float mn1 = fmaxf(m_run[nt][1], mx1);
       const float cr0 = ex2(m_run[nt][0] - mn0);
       const float cr1 = ex2(m_run[nt][1] - mn1);
+      const bool grew = __any_sync(FULL_MASK, (mn0 != m_run[nt][0]) | (mn1 != m_run[nt][1]));
       m_run[nt][0] = mn0;
       m_run[nt][1] = mn1;
       const uint32_t lo = pack_half2(ex2(x0 - mn0), ex2(x1 - mn1));  // token g
@@ -286,12 +303,14 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
       // the running sum adds the same rounded weights that multiply V
       l_run[nt][0] = l_run[nt][0] * cr0 + (flo.x + fhi.x);
       l_run[nt][1] = l_run[nt][1] * cr1 + (flo.y + fhi.y);
+      if (grew) {  // a running maximum moved: rescale the accumulators
 #pragma unroll
-      for (int dm = 0; dm < KSTEPS; ++dm) {
-        oacc[dm][nt][0] *= cr0;
-        oacc[dm][nt][1] *= cr1;
-        oacc[dm][nt][2] *= cr0;
-        oacc[dm][nt][3] *= cr1;
+        for (int dm = 0; dm < KSTEPS; ++dm) {
+          oacc[dm][nt][0] *= cr0;
+          oacc[dm][nt][1] *= cr1;
+          oacc[dm][nt][2] *= cr0;
+          oacc[dm][nt][3] *= cr1;
+        }
       }
       pb[nt][0] = movmatrix_trans(lo);  // P^T tokens 0-7 as the B fragment
       pb[nt][1] = movmatrix_trans(hi);  // P^T tokens 8-15
@@ -302,16 +321,26 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     const uint32_t mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
     const uint32_t mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
     const uint32_t va = vb + ((lane & 7) + ((lane >> 4) << 3)) * PITCH + ((lane >> 3) & 1) * 16;
+    if (valid == CHUNK) {
 #pragma unroll
-    for (int dm = 0; dm < KSTEPS; ++dm) {
-      uint32_t a[4];
-      ldsm_x4_trans(a, va + dm * 32);
-      a[0] &= mlo;
-      a[1] &= mlo;
-      a[2] &= mhi;
-      a[3] &= mhi;
+      for (int dm = 0; dm < KSTEPS; ++dm) {
+        uint32_t a[4];
+        ldsm_x4_trans(a, va + dm * 32);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(oacc[dm][nt], a, pb[nt][0], pb[nt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(oacc[dm][nt], a, pb[nt][0], pb[nt][1]);
+      }
+    } else {  // the last chunk of the sequence
+#pragma unroll
+      for (int dm = 0; dm < KSTEPS; ++dm) {
+        uint32_t a[4];
+        ldsm_x4_trans(a, va + dm * 32);
+        a[0] &= mlo;
+        a[1] &= mlo;
+        a[2] &= mhi;
+        a[3] &= mhi;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(oacc[dm][nt], a, pb[nt][0], pb[nt][1]);
+      }
     }
 
     __syncwarp();
@@ -419,14 +448,19 @@ __global__ void __launch_bounds__(HEAD_DIM) splitk_reduce_kernel(const __grid_co
   const int nparts = (ctx + p.partition_size - 1) / p.partition_size;
   if (nparts <= 1) return;  // finished by the partition kernel
   const size_t row0 = (static_cast<size_t>(s) * p.num_heads + h) * p.max_num_partitions;
-  float M = -INFINITY;
-  for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldg(p.ws_m + row0 + q));
-  float L = 0.f, O = 0.f;
+  // one pass: a running maximum M, with the sums rescaled when it grows
+  float M = -INFINITY, L = 0.f, O = 0.f;
 #pragma unroll 4
   for (int q = 0; q < nparts; ++q) {
-    const float w = __ldg(p.ws_l + row0 + q) * ex2(__ldg(p.ws_m + row0 + q) - M);
-    L += w;
-    O += w * __ldg(p.ws_o + (row0 + q) * HEAD_DIM + d);
+    const float m = __ldg(p.ws_m + row0 + q);
+    const float l = __ldg(p.ws_l + row0 + q);
+    const float o = __ldg(p.ws_o + (row0 + q) * HEAD_DIM + d);
+    const float Mn = fmaxf(M, m);
+    const float a = ex2(M - Mn);  // 0 on the first partition
+    const float w = l * ex2(m - Mn);
+    L = L * a + w;
+    O = O * a + w * o;
+    M = Mn;
   }
   p.out[(static_cast<size_t>(s) * p.num_heads + h) * HEAD_DIM + d] = __float2half_rn(O / L);
 }
@@ -444,10 +478,17 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
   return e;
 }
 
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4
+#endif
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 2
+#endif
+
 template <int HEAD_DIM, int NT>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
-  constexpr int WARPS = 4;
-  constexpr int STAGES = 3;
+  constexpr int WARPS = PA_DECODE_WARPS;
+  constexpr int STAGES = PA_DECODE_STAGES;
   using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
   auto kern = paged_decode_kernel<HEAD_DIM, NT, WARPS, STAGES>;
   static std::atomic<uint64_t> smem_set{0};
@@ -470,7 +511,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   p.num_kv_heads = a.num_kv_heads;
   p.group = a.num_heads / a.num_kv_heads;
   p.block_size = a.block_size;
-  p.chunks_per_block = a.block_size / CHUNK;
+  p.chunks_per_block_log2 = __builtin_ctz(static_cast<unsigned>(a.block_size / CHUNK));
   p.num_blocks = a.num_blocks;
   p.partition_chunks = a.partition_size / CHUNK;
   p.max_num_partitions = a.max_num_partitions;

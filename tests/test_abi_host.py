@@ -72,6 +72,8 @@ def _decode(L, **kw):
     (dict(H=64, Hk=2), _lib.PA_ERR_UNSUPPORTED),
     (dict(B=8), _lib.PA_ERR_UNSUPPORTED),
     (dict(B=24), _lib.PA_ERR_UNSUPPORTED),
+    (dict(B=48), _lib.PA_ERR_UNSUPPORTED),
+    (dict(B=512), _lib.PA_ERR_UNSUPPORTED),
     (dict(S=-1), _lib.PA_ERR_INVALID_ARG),
     (dict(S=70000), _lib.PA_ERR_UNSUPPORTED),
     (dict(M=0), _lib.PA_ERR_INVALID_ARG),

@@ -65,6 +65,8 @@ int check_decode(const void* out, const void* q, const void* k_cache, const void
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT32_MAX)
     return fail(PA_ERR_UNSUPPORTED, "max_blocks_per_seq * block_size exceeds 2^31 - 1");
   if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks %d must be positive", num_blocks);
+  if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "num_blocks * block_size exceeds 2^31 - 1 token slots");
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)

@@ -19,6 +19,7 @@
 // driver stack: GPU page tables and vLLM PagedAttention", sections 6 and 7.3
 // (address arithmetic from the physical block id; adjacent threads read
 // adjacent bytes).
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -68,10 +69,12 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_con
 
 // ================================================================ decode
 struct DecodeParams {
+  // Tensor maps over the K and V pools viewed as [N*B rows][Hk][d] (3-D,
+  // innermost first: d, Hk, rows) with a 64 x 1 x 16 box, 128-byte swizzle.
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
   __half* out;
   const __half* q;
-  const __half* k_cache;
-  const __half* v_cache;
   const int32_t* block_tables;
   const int32_t* context_lens;
   float* ws_o;
@@ -89,18 +92,26 @@ struct DecodeParams {
   float scale_log2;  // scale * log2(e): scores are kept in base-2 units
 };
 
+// Shared-memory stage of one 16-token chunk of one KV head: TMA boxes of 16
+// rows x 64 dims (128 bytes per row, 2 KB per box), 128-byte swizzled: the
+// 16-byte unit u of row r sits at unit u ^ (r % 8).  K boxes first (dims
+// 0-63, 64-127, ...), then V boxes.
+constexpr int BOX_DIMS = 64;
+constexpr int BOX_BYTES = CHUNK * BOX_DIMS * 2;
+
 template <int HEAD_DIM, int NT, int WARPS, int STAGES>
 struct DecodeCfg {
-  static constexpr int ROW_BYTES = HEAD_DIM * 2;
-  static constexpr int PITCH = ROW_BYTES + 16;  // padded row: ldmatrix rows hit distinct banks
-  static constexpr int HALF_BYTES = CHUNK * PITCH;
+  static constexpr int DBOX = HEAD_DIM / BOX_DIMS;  // boxes per row of K (or V)
+  static constexpr int HALF_BYTES = DBOX * BOX_BYTES;
   static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
   static constexpr int RING_BYTES = WARPS * STAGES * STAGE_BYTES;
   static constexpr int GMAX = NT * 8;
   static constexpr int MO_PITCH = HEAD_DIM + 4;  // floats; spreads the merge writes over banks
   static constexpr int MERGE_BYTES = WARPS * GMAX * MO_PITCH * 4 + 2 * WARPS * GMAX * 4 + WARPS * 4;
-  static constexpr int BAR_BYTES = 128 * ((WARPS * STAGES * 8 + 127) / 128);
-  static constexpr int SMEM_BYTES = BAR_BYTES + (RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES);
+  static constexpr int BAR_BYTES = 1024;  // the ring that follows is 1024-byte aligned
+  static_assert(WARPS * STAGES * 8 <= BAR_BYTES, "barrier area");
+  // + 1024 so that the ring can be aligned whatever the base alignment is
+  static constexpr int SMEM_BYTES = 1024 + BAR_BYTES + (RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES);
 };
 
 template <int HEAD_DIM, int NT, int WARPS, int STAGES>
@@ -108,10 +119,11 @@ __global__ void __launch_bounds__(WARPS * 32)
 paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
   constexpr int KSTEPS = HEAD_DIM / 16;
-  constexpr int PITCH = Cfg::PITCH;
   constexpr int GMAX = Cfg::GMAX;
 
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // swizzled TMA destinations must be 1024-byte aligned
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* ring = smem + Cfg::BAR_BYTES;
 
@@ -208,14 +220,16 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     const int ch = first + k * WARPS;
     const int row0 = (ch & ((1 << cpb_log2) - 1)) * CHUNK;
     const int slot = k % STAGES;
-    uint8_t* dst = wring + slot * Cfg::STAGE_BYTES;
-    if (lane == 0) mbar_arrive_expect_tx(&wbar[slot], 2 * CHUNK * Cfg::ROW_BYTES);
-    __syncwarp();
-    const int r = lane & 15;
-    const bool is_v = lane >= 16;
-    const size_t row = (static_cast<size_t>(phys) * p.block_size + row0 + r) * p.num_kv_heads + kvh;
-    bulk_copy_g2s(dst + (is_v ? Cfg::HALF_BYTES : 0) + r * PITCH,
-                  (is_v ? p.v_cache : p.k_cache) + row * HEAD_DIM, Cfg::ROW_BYTES, &wbar[slot]);
+    if (lane == 0) {
+      uint8_t* dst = wring + slot * Cfg::STAGE_BYTES;
+      const int y = phys * p.block_size + row0;  // pool row of the chunk's first token
+      mbar_arrive_expect_tx(&wbar[slot], Cfg::STAGE_BYTES);
+#pragma unroll
+      for (int b = 0; b < Cfg::DBOX; ++b) {
+        tma_load_3d(dst + b * BOX_BYTES, &p.tmap_k, b * BOX_DIMS, kvh, y, &wbar[slot]);
+        tma_load_3d(dst + Cfg::HALF_BYTES + b * BOX_BYTES, &p.tmap_v, b * BOX_DIMS, kvh, y, &wbar[slot]);
+      }
+    }
     ++issued;
   };
 
@@ -258,11 +272,14 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) sacc[nt][i] = sacc2[nt][i] = 0.f;
-    const uint32_t ka = kb + (lane & 15) * PITCH + (lane >> 4) * 16;
+    // lane supplies row (lane & 15) at 16-byte unit 2*(ks%4) + lane/16 of box ks/4
+    const uint32_t ka = kb + (lane & 15) * 128;
+    const uint32_t kx = lane & 7;
 #pragma unroll
     for (int ks = 0; ks < KSTEPS; ++ks) {
       uint32_t a[4];
-      ldsm_x4(a, ka + ks * 32);
+      const uint32_t unit = ((ks & 3) * 2 + (lane >> 4)) ^ kx;
+      ldsm_x4(a, ka + (ks >> 2) * BOX_BYTES + unit * 16);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
         mma_f16_16816((ks & 1) ? sacc2[nt] : sacc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
@@ -320,12 +337,15 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     const int t0 = 2 * c4;
     const uint32_t mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
     const uint32_t mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
-    const uint32_t va = vb + ((lane & 7) + ((lane >> 4) << 3)) * PITCH + ((lane >> 3) & 1) * 16;
+    // lane supplies token row (lane & 7) + 8*(lane/16) at unit 2*(dm%4) + (lane/8)%2
+    const uint32_t va = vb + ((lane & 7) + ((lane >> 4) << 3)) * 128;
+    const uint32_t vsel = (lane >> 3) & 1;
+    const uint32_t vx = lane & 7;
     if (valid == CHUNK) {
 #pragma unroll
       for (int dm = 0; dm < KSTEPS; ++dm) {
         uint32_t a[4];
-        ldsm_x4_trans(a, va + dm * 32);
+        ldsm_x4_trans(a, va + (dm >> 2) * BOX_BYTES + ((((dm & 3) * 2) + vsel) ^ vx) * 16);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_f16_16816(oacc[dm][nt], a, pb[nt][0], pb[nt][1]);
       }
@@ -333,7 +353,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
       for (int dm = 0; dm < KSTEPS; ++dm) {
         uint32_t a[4];
-        ldsm_x4_trans(a, va + dm * 32);
+        ldsm_x4_trans(a, va + (dm >> 2) * BOX_BYTES + ((((dm & 3) * 2) + vsel) ^ vx) * 16);
         a[0] &= mlo;
         a[1] &= mlo;
         a[2] &= mhi;
@@ -343,11 +363,9 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
       }
     }
 
+    fence_proxy_async_smem();  // this lane's reads of the slot precede the refill's writes
     __syncwarp();
-    if (issued < nk) {
-      fence_proxy_async_smem();  // our reads of this slot precede the copy that refills it
-      issue_next();
-    }
+    if (issued < nk) issue_next();
   }
 
   if (timed_out) {
@@ -466,6 +484,48 @@ __global__ void __launch_bounds__(HEAD_DIM) splitk_reduce_kernel(const __grid_co
 }
 
 // ================================================================ launchers
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled, resolved through the runtime once (the library does
+// not link the driver library directly).
+cudaError_t encode_fn(EncodeTiledFn* out) {
+  static std::atomic<EncodeTiledFn> cached{nullptr};
+  EncodeTiledFn f = cached.load(std::memory_order_acquire);
+  if (f == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || ptr == nullptr) return cudaErrorNotSupported;
+    f = reinterpret_cast<EncodeTiledFn>(ptr);
+    cached.store(f, std::memory_order_release);
+  }
+  *out = f;
+  return cudaSuccess;
+}
+
+// A KV pool [N][B][Hk][d] seen as rows x heads x dims, boxes of 16 rows x 1
+// head x 64 dims, 128-byte swizzled.
+cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int head_dim, int num_kv_heads,
+                          int64_t rows) {
+  EncodeTiledFn enc = nullptr;
+  cudaError_t e = encode_fn(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+  const cuuint32_t box[3] = {BOX_DIMS, 1, CHUNK};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(pool), dims, strides, box,
+                         estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <typename Kernel>
 cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
   int dev = 0;
@@ -496,10 +556,13 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
 
   DecodeParams p;
+  const int64_t pool_rows = static_cast<int64_t>(a.num_blocks) * a.block_size;
+  e = make_pool_map(&p.tmap_k, a.k_cache, HEAD_DIM, a.num_kv_heads, pool_rows);
+  if (e != cudaSuccess) return e;
+  e = make_pool_map(&p.tmap_v, a.v_cache, HEAD_DIM, a.num_kv_heads, pool_rows);
+  if (e != cudaSuccess) return e;
   p.out = static_cast<__half*>(a.out);
   p.q = static_cast<const __half*>(a.q);
-  p.k_cache = static_cast<const __half*>(a.k_cache);
-  p.v_cache = static_cast<const __half*>(a.v_cache);
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   const size_t rows = ws_rows(a.num_seqs, a.num_heads, a.max_num_partitions);

@@ -2,8 +2,10 @@
 """Benchmark of the paged decode hot path on GB300.
 
 One step = one decode step of one layer for a whole batch: reshape_and_cache
-(the new token of every sequence into its slot), split-K paged decode, and
-the log-sum-exp reduce.  Default workload: the Llama-3-8B-shaped decode layer
+(the new token of every sequence into its slot), then paged decode, either as
+one pa_decode launch (which merges partial results across the CTAs of a
+cluster itself) or as pa_decode_splitk followed by the log-sum-exp reduce.
+Both are timed; the faster is the headline and both appear under "paths".  Default workload: the Llama-3-8B-shaped decode layer
 (64 sequences, 32 q heads / 8 KV heads, head_dim 128, block_size 16,
 contexts uniform in [128, 2048], 1.25x pool with shuffled block ids).
 
@@ -83,8 +85,9 @@ def decode_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(workload: str):
-    """ncu DRAM bytes per decode launch, if taken on the current kernel source."""
+def load_traffic(workload: str, kernel: str):
+    """ncu DRAM bytes (read + write) per decode launch, if they were taken on
+    the current kernel source for this workload and kernel."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
@@ -92,7 +95,7 @@ def load_traffic(workload: str):
         return None
     if rec.get("source_sha") != decode_source_sha():
         return None
-    return rec.get("per_workload", {}).get(workload)
+    return rec.get("per_workload", {}).get(f"{workload}/{kernel}")
 
 
 # ------------------------------------------------------------------- clocks
@@ -163,6 +166,100 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- GPU arm
+def _make_event(torch, external: bool):
+    if external:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    return torch.cuda.Event(enable_timing=True)
+
+
+def time_path(torch, dev, stream, kernels, nrep: int, K: int, W: int, clocks=None, dist=None):
+    """Time exactly K steps of one path; a step calls each of `kernels` (name,
+    fn(r)) in order on replica r % nrep.  Steps run as CUDA-graph replays; the
+    last G steps carry an event between kernels.  Those events are recorded
+    inside the graph when torch supports external events, otherwise the last
+    G steps run eagerly (the host enqueues them while the GPU still replays the
+    graphs).  Returns total ms, per-kernel mean ms, wall times and the timing mode."""
+    G = min(K, 8 * nrep)
+
+    def step(r, ev=None):
+        for j, (_, fn) in enumerate(kernels):
+            if ev is not None:
+                ev[j].record()
+            fn(r)
+        if ev is not None:
+            ev[len(kernels)].record()
+
+    with torch.cuda.stream(stream):
+        for i in range(max(W, 3)):  # warm-up; also sets kernel attributes before any capture
+            step(i)
+    torch.cuda.synchronize(dev)
+
+    def capture(n, evs=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i, evs[i] if evs is not None else None)
+        return g
+
+    n_plain = (K - G) // G
+    tail = K - G - n_plain * G
+    g_plain = capture(G) if n_plain else None
+    g_tail = capture(tail) if tail else None
+    mode = "graph-events"
+    evs = None
+    g_ev = None
+    try:
+        evs = [[_make_event(torch, True) for _ in range(len(kernels) + 1)] for _ in range(G)]
+        g_ev = capture(G, evs)
+        with torch.cuda.stream(stream):
+            g_ev.replay()
+        torch.cuda.synchronize(dev)
+        evs[0][0].elapsed_time(evs[0][1])
+    except Exception:
+        mode = "eager-events"
+        g_ev = None
+        evs = [[_make_event(torch, False) for _ in range(len(kernels) + 1)] for _ in range(G)]
+    with torch.cuda.stream(stream):  # untimed pass over every graph
+        if g_plain:
+            g_plain.replay()
+        if g_tail:
+            g_tail.replay()
+        if g_ev is None:
+            for i in range(G):
+                step(i, evs[i])
+    torch.cuda.synchronize(dev)
+
+    if clocks:
+        clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(n_plain):
+            g_plain.replay()
+        if g_tail:
+            g_tail.replay()
+        if g_ev is not None:
+            g_ev.replay()
+        else:
+            for i in range(G):
+                step(i, evs[i])
+        e1.record()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    wall1 = time.time()
+    if clocks:
+        clocks.stop()
+    ms = e0.elapsed_time(e1)
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(len(kernels))] for i in range(G)])
+    return ms, per.mean(axis=0), (wall0, wall1), mode, G
+
+
 def run_gpu(args, rank: int, world: int):
     import torch
     from paged_kv_cache_173_gb300 import api, workloads
@@ -188,95 +285,54 @@ def run_gpu(args, rank: int, world: int):
     ws = api.alloc_splitk_workspace(b.num_seqs, b.num_heads, b.head_dim, P, dev)
     M, B = b.max_blocks_per_seq, b.block_size
 
-    def step(r, ev=None):
-        kc, vc, q = reps[r % R]
-        if ev is not None:
-            ev[0].record()
+    def reshape(r):
+        kc, vc, _ = reps[r % R]
         api.pa_reshape_and_cache(key, value, kc, vc, sm)
-        if ev is not None:
-            ev[1].record()
-        api.pa_decode_splitk(out, q, kc, vc, bt, cl, b.scale, ps, ws, P)
-        if ev is not None:
-            ev[2].record()
-        api.pa_splitk_reduce(out, ws, cl, M, B, ps, P)
-        if ev is not None:
-            ev[3].record()
 
+    def decode(r):
+        kc, vc, q = reps[r % R]
+        api.pa_decode(out, q, kc, vc, bt, cl, b.scale)
+
+    def decode_splitk(r):
+        kc, vc, q = reps[r % R]
+        api.pa_decode_splitk(out, q, kc, vc, bt, cl, b.scale, ps, ws, P)
+
+    def reduce(r):
+        api.pa_splitk_reduce(out, ws, cl, M, B, ps, P)
+
+    paths = {
+        "decode": [("reshape_and_cache", reshape), ("paged_decode", decode)],
+        "splitk": [("reshape_and_cache", reshape), ("paged_decode_splitk", decode_splitk),
+                   ("splitk_reduce", reduce)],
+    }
+    want = list(paths) if args.path == "auto" else [args.path]
     stream = torch.cuda.Stream(dev)
     K, W = args.steps, args.warmup
-    G = min(K, 8 * R)  # steps per graph replay
-    with torch.cuda.stream(stream):
-        for i in range(max(W, 3)):  # warm-up (also sets kernel attributes before capture)
-            step(i)
-    torch.cuda.synchronize(dev)
-
-    g_plain = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_plain, stream=stream):
-        for i in range(G):
-            step(i)
-    # The last G steps of the timed region run eagerly with an event between
-    # kernels (events recorded inside a captured graph cannot be timed).  The
-    # host enqueues them while the GPU is still replaying the graphs, so the
-    # device runs them back to back.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(G)]
-    n_plain = (K - G) // G
-    tail = K - G - n_plain * G
-    g_tail = None
-    if tail:
-        g_tail = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_tail, stream=stream):
-            for i in range(tail):
-                step(i)
-    # untimed replays of each graph
-    with torch.cuda.stream(stream):
-        g_plain.replay()
-        if g_tail:
-            g_tail.replay()
-        for i in range(G):
-            step(i, evs[i])
-    torch.cuda.synchronize(dev)
-
     import torch.distributed as dist
-    distributed = world > 1 and dist.is_initialized()
-    clocks = ClockSampler(dev.index)
-    clocks.start()
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    if distributed:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    wall0 = time.time()
-    with torch.cuda.stream(stream):
-        e_start.record()
-        for _ in range(n_plain):
-            g_plain.replay()
-        if g_tail:
-            g_tail.replay()
-        for i in range(G):  # the last G steps carry per-kernel events
-            step(i, evs[i])
-        e_end.record()
-    torch.cuda.synchronize(dev)
-    if distributed:
-        dist.barrier()
-    wall1 = time.time()
-    clocks.stop()
-    ms = e_start.elapsed_time(e_end)
-    if distributed:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    dist_g = dist if (world > 1 and dist.is_initialized()) else None
+    results = {}
+    for name in want:
+        clocks = ClockSampler(dev.index)
+        ms, per, walls, mode, G = time_path(torch, dev, stream, paths[name], R, K, W, clocks, dist_g)
+        if dist_g is not None:
+            tt = torch.tensor([ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms = float(tt.item())
+        results[name] = dict(ms=ms, per=per, clocks=clocks.summary(*walls), mode=mode, G=G)
+    best = min(results, key=lambda n: results[n]["ms"])
+    r0 = results[best]
+    kern = paths[best]
+    decode_name = kern[1][0]
+    t_decode = float(r0["per"][1])
 
-    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(G)])
-    t_reshape, t_decode, t_reduce = per.mean(axis=0)  # ms per launch
-
-    # ---- end to end through the public API with host buffers
-    e2e = run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream)
+    e2e = run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, best)
 
     peak, peak_kind = load_peak()
+    ms = r0["ms"]
     value = kv_bytes * K * world / (ms * 1e-3) / 1e9
     step_ms = ms / K
     achieved = kv_bytes / (t_decode * 1e-3) / 1e9
-    traffic = load_traffic(args.workload)
+    traffic = load_traffic(args.workload, decode_name)
     res = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -293,18 +349,20 @@ def run_gpu(args, rank: int, world: int):
         "config": {
             "workload": desc,
             "kv_bytes_per_step": kv_bytes,
-            "partition_size": ps,
+            "path": best,
+            "step": " -> ".join(n for n, _ in kern),
+            "partition_size": ps if best == "splitk" else None,
             "l2": f"{R} rotating pool replicas ({R * pool_bytes / 1e9:.2f} GB) > 129 MB L2; steps back to back",
-            "steps_per_graph": G,
+            "steps_per_graph": r0["G"],
+            "kernel_timing": r0["mode"],
         },
         "hbm_frac_of_step": round(value / world / peak, 4),
         "hbm_peak_gbs": peak,
         "hbm_peak_kind": peak_kind,
         "tokens_per_s": round(b.num_seqs * world / (step_ms * 1e-3), 1),
-        "kernel_ms": {"reshape_and_cache": round(t_reshape, 5), "paged_decode_splitk": round(t_decode, 5),
-                      "splitk_reduce": round(t_reduce, 5)},
+        "kernel_ms": {n: round(float(v), 5) for (n, _), v in zip(kern, r0["per"])},
         "roofline": {
-            "kernel": "paged_decode_kernel (split-K)",
+            "kernel": decode_name,
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -313,16 +371,20 @@ def run_gpu(args, rank: int, world: int):
             "traffic": traffic,
             "peak_kind": f"{peak_kind} (copy GB/s)",
         },
-        "gpu_launches": 3 * K,
+        "gpu_launches": len(kern) * K,
         "e2e": e2e,
-        "clocks": clocks.summary(wall0, wall1),
+        "clocks": r0["clocks"],
+        "paths": {n: {"ms_per_step": round(v["ms"] / K, 5),
+                      "value": round(kv_bytes * K * world / (v["ms"] * 1e-3) / 1e9, 1),
+                      "kernel_ms": {kn: round(float(x), 5) for (kn, _), x in zip(paths[n], v["per"])}}
+                  for n, v in results.items()},
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(b, kv_bytes, budget_s=args.cpu_seconds)
     return res
 
 
-def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream):
+def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, path):
     """Same step through the public API with pinned host inputs and output."""
     import torch
     from paged_kv_cache_173_gb300 import api
@@ -341,9 +403,12 @@ def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream):
         for k in host:
             devb[k].copy_(host[k], non_blocking=True)
         api.pa_reshape_and_cache(devb["key"], devb["value"], kc, vc, devb["slot_mapping"])
-        api.pa_decode_splitk(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"], b.scale,
-                             ps, ws, P)
-        api.pa_splitk_reduce(out, ws, devb["context_lens"], M, B, ps, P)
+        if path == "decode":
+            api.pa_decode(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"], b.scale)
+        else:
+            api.pa_decode_splitk(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"],
+                                 b.scale, ps, ws, P)
+            api.pa_splitk_reduce(out, ws, devb["context_lens"], M, B, ps, P)
         out_h.copy_(out, non_blocking=True)
 
     n = max(3, min(args.steps, args.e2e_steps))
@@ -454,6 +519,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="llama3-8b")
     p.add_argument("--partition-size", type=int, default=512)
+    p.add_argument("--path", choices=["auto", "decode", "splitk"], default="auto",
+                   help="decode: reshape + pa_decode; splitk: reshape + pa_decode_splitk + reduce; "
+                        "auto: time both, report the faster")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=2000)
     p.add_argument("--cpu-seconds", type=float, default=12.0)

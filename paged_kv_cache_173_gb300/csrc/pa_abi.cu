@@ -188,7 +188,11 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   a.block_size = block_size;
   a.num_blocks = num_blocks;
   a.scale = scale;
-  a.partition_size = max_blocks_per_seq * block_size;  // one partition per sequence
+  // One CTA per (sequence, KV head) when the pairs fill the GPU; otherwise a
+  // cluster of up to 8 CTAs per pair that split the sequence and merge
+  // through distributed shared memory (chosen by the launcher).
+  a.cluster_size = -1;
+  a.partition_size = max_blocks_per_seq * block_size;
   a.max_num_partitions = 1;
   return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)), "decode launch");
 }
@@ -225,6 +229,7 @@ int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* 
   a.scale = scale;
   a.partition_size = partition_size;
   a.max_num_partitions = max_num_partitions;
+  a.cluster_size = 0;
   return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)),
                      "split-K decode launch");
 }

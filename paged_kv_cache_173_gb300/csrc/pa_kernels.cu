@@ -11,6 +11,11 @@
 //                             are merged in shared memory at the end
 //  splitk_reduce_kernel       log-sum-exp merge of the partitions
 //
+//  The same decode kernel also runs as thread-block clusters (pa_decode): the
+//  C CTAs of a cluster split one (sequence, KV head) evenly and merge their
+//  partial results through distributed shared memory, with the log-sum-exp
+//  rule of the reduce, so a single launch needs no workspace.
+//
 // The method: "vLLM PagedAttention source walk-through", section 3.4 (block
 // walk, mask, online softmax with correction factor exp(old_max - new_max));
 // "PagedAttention: when the KV cache meets OS paging", sections 3.2 and 5.1
@@ -24,8 +29,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cooperative_groups.h>
+
 #include <atomic>
 #include <cmath>
+#include <algorithm>
+#include <type_traits>
 
 #include "pa_launch.h"
 #include "pa_ptx.cuh"
@@ -54,6 +63,8 @@ struct ReshapeParams {
 // One warp per (token, KV head): lanes 0-15 copy the K row, lanes 16-31 the V
 // row, 16 bytes per lane per step.
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_constant__ ReshapeParams p) {
+  grid_dependency_wait();     // inputs may come from the previous kernel on the stream
+  allow_dependent_launch();   // the decode may start its prologue; it waits for this grid
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wid >= p.num_tokens * p.num_kv_heads) return;
@@ -108,13 +119,23 @@ struct DecodeCfg {
   static constexpr int GMAX = NT * 8;
   static constexpr int MO_PITCH = HEAD_DIM + 4;  // floats; spreads the merge writes over banks
   static constexpr int MERGE_BYTES = WARPS * GMAX * MO_PITCH * 4 + 2 * WARPS * GMAX * 4 + WARPS * 4;
+  // CTA result shared with the other CTAs of a cluster: o [GMAX][HEAD_DIM], m, l [GMAX]
+  static constexpr int CTA_OFFSET = (MERGE_BYTES + 15) / 16 * 16;
+  static constexpr int CTA_BYTES = GMAX * HEAD_DIM * 4 + 2 * GMAX * 4;
+  static constexpr int TAIL_BYTES = CTA_OFFSET + CTA_BYTES;
   static constexpr int BAR_BYTES = 1024;  // the ring that follows is 1024-byte aligned
   static_assert(WARPS * STAGES * 8 <= BAR_BYTES, "barrier area");
   // + 1024 so that the ring can be aligned whatever the base alignment is
-  static constexpr int SMEM_BYTES = 1024 + BAR_BYTES + (RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES);
+  static constexpr int SMEM_BYTES = 1024 + BAR_BYTES + (RING_BYTES > TAIL_BYTES ? RING_BYTES : TAIL_BYTES);
 };
 
-template <int HEAD_DIM, int NT, int WARPS, int STAGES>
+// CLUSTER = false: CTA (kvh, part, s) covers partition `part` of
+//   partition_chunks chunks; a sequence with one partition writes `out`,
+//   otherwise the partition's (o, m, l) go to the split-K workspace.
+// CLUSTER = true: gridDim.y CTAs form a cluster per (kvh, s); CTA `part`
+//   takes chunks [part * n / C, (part + 1) * n / C) of the sequence's n chunks
+//   and the cluster merges the C results into `out`.
+template <int HEAD_DIM, int NT, int WARPS, int STAGES, bool CLUSTER>
 __global__ void __launch_bounds__(WARPS * 32)
 paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
@@ -137,13 +158,25 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int G = p.group;
   const int H = p.num_heads;
 
+  // The previous kernel on the stream (typically the cache write) may still
+  // be running: everything up to here overlapped with its tail.
+  grid_dependency_wait();
+
   // Loads that do not depend on the context length go out first, so that
   // their latencies overlap with the one of context_lens[s].
   const int ctx = __ldg(p.context_lens + s);
-  const int c0 = part * p.partition_chunks;
   const int cpb_log2 = p.chunks_per_block_log2;
   const int table_chunks = p.max_blocks_per_seq << cpb_log2;
-  const int cmax = min(c0 + p.partition_chunks, table_chunks);  // chunks the table can hold
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  const bool ctx_bad = ctx < 0 || ctx > cap;
+  const int nchunks = ctx_bad ? 0 : (ctx + CHUNK - 1) / CHUNK;
+  const int nclu = CLUSTER ? static_cast<int>(gridDim.y) : 1;
+  // The split-K chunk range is known before the context length arrives; the
+  // cluster split depends on it.
+  const int c0 = CLUSTER ? static_cast<int>((static_cast<int64_t>(part) * nchunks) / nclu)
+                         : part * p.partition_chunks;
+  const int cmax = CLUSTER ? static_cast<int>((static_cast<int64_t>(part + 1) * nchunks) / nclu)
+                           : min(c0 + p.partition_chunks, table_chunks);  // chunks the table can hold
   const int first = c0 + warp;
   const int nk_cap = first < cmax ? (cmax - first + WARPS - 1) / WARPS : 0;
 
@@ -184,10 +217,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   }
   __syncwarp();
 
-  const int cap = p.max_blocks_per_seq * p.block_size;
-  const bool ctx_bad = ctx < 0 || ctx > cap;
-  const int nchunks = ctx_bad ? 0 : (ctx + CHUNK - 1) / CHUNK;
-  const int nparts = (nchunks + p.partition_chunks - 1) / p.partition_chunks;
+  const int nparts = CLUSTER ? nclu : (nchunks + p.partition_chunks - 1) / p.partition_chunks;
 
   if (nchunks == 0) {
     // Empty sequence -> zeros; impossible context length -> NaN.  Written once.
@@ -196,11 +226,15 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
       __half* o = p.out + (static_cast<size_t>(s) * H + kvh * G) * HEAD_DIM;
       for (int i = threadIdx.x; i < G * HEAD_DIM; i += WARPS * 32) o[i] = v;
     }
+    allow_dependent_launch();
+    return;  // in a cluster every CTA takes this exit together
+  }
+  if (!CLUSTER && part >= nparts) {
+    allow_dependent_launch();
     return;
   }
-  if (part >= nparts) return;
-  const bool single = nparts == 1;
-  const int c1 = min(c0 + p.partition_chunks, nchunks);
+  const bool single = !CLUSTER && nparts == 1;
+  const int c1 = CLUSTER ? cmax : min(c0 + p.partition_chunks, nchunks);
   const int nk = first < c1 ? (c1 - first + WARPS - 1) / WARPS : 0;  // <= nk_cap
 
   int issued = 0;
@@ -421,15 +455,25 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
     for (int w = 0; w < WARPS; ++w) M = fmaxf(M, mm[w * GMAX + head]);
     float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {  // only a cluster CTA can have no chunk at all
 #pragma unroll
-    for (int w = 0; w < WARPS; ++w) {
-      const float f = ex2(mm[w * GMAX + head] - M);  // warps without chunks: 2^-inf = 0
-      L += ml[w * GMAX + head] * f;
-      O += mo[(w * GMAX + head) * Cfg::MO_PITCH + d] * f;
+      for (int w = 0; w < WARPS; ++w) {
+        const float f = ex2(mm[w * GMAX + head] - M);  // warps without chunks: 2^-inf = 0
+        L += ml[w * GMAX + head] * f;
+        O += mo[(w * GMAX + head) * Cfg::MO_PITCH + d] * f;
+      }
     }
-    const float r = any_bad ? NAN : O / L;
+    const float r = any_bad ? NAN : (L > 0.f ? O / L : 0.f);
     const size_t qrow = static_cast<size_t>(s) * H + kvh * G + head;
-    if (single) {
+    if (CLUSTER) {
+      // an empty CTA publishes m = -inf, l = 0: weight 0 in the cluster merge
+      float* cta = reinterpret_cast<float*>(ring + Cfg::CTA_OFFSET);
+      cta[head * HEAD_DIM + d] = r;
+      if (d == 0) {
+        cta[GMAX * HEAD_DIM + head] = any_bad ? 0.f : M;
+        cta[GMAX * HEAD_DIM + GMAX + head] = any_bad ? 1.f : L;
+      }
+    } else if (single) {
       p.out[qrow * HEAD_DIM + d] = __float2half_rn(r);
     } else {
       const size_t row = qrow * p.max_num_partitions + part;
@@ -440,6 +484,35 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
       }
     }
   }
+
+  if constexpr (CLUSTER) {
+    // Merge the cluster's CTA results (o_r, m_r, l_r) read from each CTA's
+    // shared memory: M = max m_r, w_r = l_r 2^(m_r - M), out = sum w_r o_r / sum w_r.
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();  // every CTA's result is in its shared memory
+    float* cta = reinterpret_cast<float*>(ring + Cfg::CTA_OFFSET);
+    const int rank = static_cast<int>(cluster.block_rank());
+    for (int idx = rank * (WARPS * 32) + threadIdx.x; idx < G * HEAD_DIM; idx += nclu * WARPS * 32) {
+      const int head = idx / HEAD_DIM;
+      const int d = idx - head * HEAD_DIM;
+      float M = -INFINITY;
+      for (int r = 0; r < nclu; ++r) {
+        const float* peer = cluster.map_shared_rank(cta, r);
+        M = fmaxf(M, peer[GMAX * HEAD_DIM + head]);
+      }
+      float L = 0.f, O = 0.f;
+      for (int r = 0; r < nclu; ++r) {
+        const float* peer = cluster.map_shared_rank(cta, r);
+        const float w = peer[GMAX * HEAD_DIM + GMAX + head] * ex2(peer[GMAX * HEAD_DIM + head] - M);
+        L += w;
+        O += w * peer[head * HEAD_DIM + d];
+      }
+      p.out[(static_cast<size_t>(s) * H + kvh * G + head) * HEAD_DIM + d] = __float2half_rn(O / L);
+    }
+    cluster.sync();  // no CTA leaves while the others still read its shared memory
+  }
+  allow_dependent_launch();
 }
 
 // ================================================================ reduce
@@ -455,32 +528,179 @@ struct ReduceParams {
   int max_num_partitions;
 };
 
-// One CTA per (query head, sequence), one thread per output dimension.
-template <int HEAD_DIM>
-__global__ void __launch_bounds__(HEAD_DIM) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
-  const int h = blockIdx.x;
+// At most PMAX partitions: one warp per (sequence, head), 8 per CTA.  Every
+// load is issued at once -- the context length, lane q's (m_q, l_q) and each
+// lane's HEAD_DIM / 32 dims of all PMAX partition outputs -- so the kernel
+// waits for memory once.  Rows past the sequence's partitions hold stale data
+// and are dropped by select, never multiplied by a zero weight.
+template <int HEAD_DIM, int PMAX>
+__global__ void __launch_bounds__(256) splitk_reduce_small_kernel(const __grid_constant__ ReduceParams p) {
+  constexpr int VEC = HEAD_DIM / 32;
+  using VecT = typename std::conditional<VEC == 4, float4, float2>::type;
+  grid_dependency_wait();  // the partitions come from the decode kernel just before
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.x * 8 + warp;
   const int s = blockIdx.y;
-  const int d = threadIdx.x;
-  const int ctx = __ldg(p.context_lens + s);
-  if (ctx <= 0 || ctx > p.cap) return;
-  const int nparts = (ctx + p.partition_size - 1) / p.partition_size;
-  if (nparts <= 1) return;  // finished by the partition kernel
+  if (h >= p.num_heads) return;
   const size_t row0 = (static_cast<size_t>(s) * p.num_heads + h) * p.max_num_partitions;
-  // one pass: a running maximum M, with the sums rescaled when it grows
-  float M = -INFINITY, L = 0.f, O = 0.f;
-#pragma unroll 4
-  for (int q = 0; q < nparts; ++q) {
-    const float m = __ldg(p.ws_m + row0 + q);
-    const float l = __ldg(p.ws_l + row0 + q);
-    const float o = __ldg(p.ws_o + (row0 + q) * HEAD_DIM + d);
-    const float Mn = fmaxf(M, m);
-    const float a = ex2(M - Mn);  // 0 on the first partition
-    const float w = l * ex2(m - Mn);
-    L = L * a + w;
-    O = O * a + w * o;
-    M = Mn;
+  const int ctx = __ldg(p.context_lens + s);
+  VecT o[PMAX];
+#pragma unroll
+  for (int q = 0; q < PMAX; ++q)
+    o[q] = q < p.max_num_partitions ? __ldg(reinterpret_cast<const VecT*>(p.ws_o + (row0 + q) * HEAD_DIM) + lane)
+                                   : VecT{};
+  const bool mine = lane < p.max_num_partitions;
+  const float m = mine ? __ldg(p.ws_m + row0 + lane) : -INFINITY;
+  const float l = mine ? __ldg(p.ws_l + row0 + lane) : 0.f;
+  const int nparts = (ctx <= 0 || ctx > p.cap) ? 0 : (ctx + p.partition_size - 1) / p.partition_size;
+  if (nparts <= 1) return;  // finished by the decode kernel
+  const float mv = lane < nparts ? m : -INFINITY;
+  float M = mv;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float w = lane < nparts ? l * ex2(m - M) : 0.f;
+  float L = w;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  float acc[VEC];
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+#pragma unroll
+  for (int q = 0; q < PMAX; ++q) {
+    const float wq = __shfl_sync(0xffffffffu, w, q);
+    if (q < nparts) {
+      acc[0] += wq * o[q].x;
+      acc[1] += wq * o[q].y;
+      if constexpr (VEC == 4) {
+        acc[2] += wq * o[q].z;
+        acc[3] += wq * o[q].w;
+      }
+    }
   }
-  p.out[(static_cast<size_t>(s) * p.num_heads + h) * HEAD_DIM + d] = __float2half_rn(O / L);
+  __half* dst = p.out + (static_cast<size_t>(s) * p.num_heads + h) * HEAD_DIM + lane * VEC;
+  const float inv = 1.f / L;
+  if constexpr (VEC == 4) {
+    __half2 a = __floats2half2_rn(acc[0] * inv, acc[1] * inv);
+    __half2 b = __floats2half2_rn(acc[2] * inv, acc[3] * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst) = u;
+  } else {
+    *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+// Warps per (sequence, head): WPH warps split the partitions (q = sub, sub +
+// WPH, ...); each lane owns HEAD_DIM / 32 consecutive output dims and reads
+// them as one vector per partition.  A CTA has 8 warps = 8 / WPH heads.
+template <int HEAD_DIM, int WPH>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
+  constexpr int VEC = HEAD_DIM / 32;
+  constexpr int HPC = 8 / WPH;
+  using VecT = typename std::conditional<VEC == 4, float4, float2>::type;
+  __shared__ float sm_m[8], sm_l[8];
+  __shared__ VecT sm_o[8][32];
+  grid_dependency_wait();  // the partitions come from the decode kernel just before
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.x * HPC + warp / WPH;
+  const int sub = warp % WPH;
+  const int s = blockIdx.y;
+  const int ctx = __ldg(p.context_lens + s);
+  const int nparts = (ctx <= 0 || ctx > p.cap) ? 0 : (ctx + p.partition_size - 1) / p.partition_size;
+  const bool active = h < p.num_heads && nparts > 1;  // one partition: finished by the decode kernel
+  const size_t row0 = (static_cast<size_t>(s) * p.num_heads + (active ? h : 0)) * p.max_num_partitions;
+  const int cnt = active ? (nparts - sub + WPH - 1) / WPH : 0;  // this warp's partitions
+
+  // maximum over this warp's partitions
+  float Mw = -INFINITY;
+  for (int i = lane; i < cnt; i += 32) Mw = fmaxf(Mw, __ldg(p.ws_m + row0 + sub + i * WPH));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
+
+  // weights w_q = l_q 2^(m_q - Mw), broadcast 32 at a time; weighted sum of o_q
+  float Lw = 0.f;
+  float acc[VEC];
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+  for (int base = 0; base < cnt; base += 32) {
+    const int i = base + lane;
+    float w = 0.f;
+    if (i < cnt) {
+      const size_t r = row0 + sub + static_cast<size_t>(i) * WPH;
+      w = __ldg(p.ws_l + r) * ex2(__ldg(p.ws_m + r) - Mw);
+    }
+    Lw += w;
+    const int n = min(32, cnt - base);
+#pragma unroll 8
+    for (int j = 0; j < n; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const size_t r = row0 + sub + static_cast<size_t>(base + j) * WPH;
+      const VecT o = __ldg(reinterpret_cast<const VecT*>(p.ws_o + r * HEAD_DIM) + lane);
+      acc[0] += wj * o.x;
+      acc[1] += wj * o.y;
+      if constexpr (VEC == 4) {
+        acc[2] += wj * o.z;
+        acc[3] += wj * o.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Lw += __shfl_xor_sync(0xffffffffu, Lw, off);
+
+  if constexpr (WPH > 1) {
+    // combine the WPH warps of each head
+    if (lane == 0) {
+      sm_m[warp] = Mw;
+      sm_l[warp] = Lw;
+    }
+    VecT o;
+    o.x = acc[0];
+    o.y = acc[1];
+    if constexpr (VEC == 4) {
+      o.z = acc[2];
+      o.w = acc[3];
+    }
+    sm_o[warp][lane] = o;
+    __syncthreads();
+    if (sub != 0 || !active) return;
+    const int w0 = warp;
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < WPH; ++k) M = fmaxf(M, sm_m[w0 + k]);
+    float L = 0.f;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+#pragma unroll
+    for (int k = 0; k < WPH; ++k) {
+      const float f = ex2(sm_m[w0 + k] - M);  // a warp without partitions: 2^-inf = 0
+      L += sm_l[w0 + k] * f;
+      const VecT ok = sm_o[w0 + k][lane];
+      acc[0] += f * ok.x;
+      acc[1] += f * ok.y;
+      if constexpr (VEC == 4) {
+        acc[2] += f * ok.z;
+        acc[3] += f * ok.w;
+      }
+    }
+    Lw = L;
+  } else {
+    if (!active) return;
+  }
+  __half* dst = p.out + (static_cast<size_t>(s) * p.num_heads + h) * HEAD_DIM + lane * VEC;
+  const float inv = 1.f / Lw;
+  if constexpr (VEC == 4) {
+    __half2 a = __floats2half2_rn(acc[0] * inv, acc[1] * inv);
+    __half2 b = __floats2half2_rn(acc[2] * inv, acc[3] * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst) = u;
+  } else {
+    *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(acc[0] * inv, acc[1] * inv);
+  }
 }
 
 // ================================================================ launchers
@@ -545,12 +765,12 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
 #define PA_DECODE_STAGES 2
 #endif
 
-template <int HEAD_DIM, int NT>
+template <int HEAD_DIM, int NT, bool CLUSTER>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   constexpr int WARPS = PA_DECODE_WARPS;
   constexpr int STAGES = PA_DECODE_STAGES;
   using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
-  auto kern = paged_decode_kernel<HEAD_DIM, NT, WARPS, STAGES>;
+  auto kern = paged_decode_kernel<HEAD_DIM, NT, WARPS, STAGES, CLUSTER>;
   static std::atomic<uint64_t> smem_set{0};
   cudaError_t e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return e;
@@ -580,9 +800,92 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   p.max_num_partitions = a.max_num_partitions;
   p.scale_log2 = a.scale * 1.4426950408889634f;
 
-  dim3 grid(a.num_kv_heads, a.max_num_partitions, a.num_seqs);
-  kern<<<grid, WARPS * 32, Cfg::SMEM_BYTES, stream>>>(p);
+  dim3 grid(a.num_kv_heads, CLUSTER ? a.cluster_size : a.max_num_partitions, a.num_seqs);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if constexpr (CLUSTER) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = a.cluster_size;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Resident decode CTAs the device holds at once (SMs x CTAs per SM), cached
+// per device.
+template <int HEAD_DIM, int NT>
+cudaError_t decode_slots(int* slots) {
+  constexpr int WARPS = PA_DECODE_WARPS;
+  constexpr int STAGES = PA_DECODE_STAGES;
+  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_acquire);
+    if (c > 0) {
+      *slots = c;
+      return cudaSuccess;
+    }
+  }
+  auto kern = paged_decode_kernel<HEAD_DIM, NT, WARPS, STAGES, false>;
+  static std::atomic<uint64_t> smem_set{0};
+  e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
+  if (e != cudaSuccess) return e;
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, WARPS * 32, Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int v = sms * (per_sm > 0 ? per_sm : 1);
+  if (dev < 64) cache[dev].store(v, std::memory_order_release);
+  *slots = v;
+  return cudaSuccess;
+}
+
+// Cluster size for single-launch decode: one CTA per (sequence, KV head) when
+// those fill the resident slots; otherwise up to 8 CTAs per pair, each with
+// at least 512 tokens of capacity.
+template <int HEAD_DIM, int NT>
+cudaError_t auto_cluster_size(const DecodeArgs& a, int* c) {
+  int slots = 0;
+  cudaError_t e = decode_slots<HEAD_DIM, NT>(&slots);
+  if (e != cudaSuccess) return e;
+  const int64_t pairs = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
+  int64_t k = pairs > 0 ? slots / pairs : 1;
+  const int64_t cap = static_cast<int64_t>(a.max_blocks_per_seq) * a.block_size;
+  k = std::min<int64_t>(k, (cap + 511) / 512);
+  *c = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(8, k)));
+  return cudaSuccess;
+}
+
+template <int HEAD_DIM, int NT>
+cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.cluster_size >= 0) {
+    return a.cluster_size > 0 ? launch_decode_t<HEAD_DIM, NT, true>(a, stream)
+                              : launch_decode_t<HEAD_DIM, NT, false>(a, stream);
+  }
+  DecodeArgs b = a;
+  cudaError_t e = auto_cluster_size<HEAD_DIM, NT>(a, &b.cluster_size);
+  if (e != cudaSuccess) return e;
+  if (b.cluster_size == 1) {  // a plain single pass: one CTA per (sequence, KV head)
+    b.cluster_size = 0;
+    return launch_decode_t<HEAD_DIM, NT, false>(b, stream);
+  }
+  return launch_decode_t<HEAD_DIM, NT, true>(b, stream);
 }
 
 template <int HEAD_DIM>
@@ -598,8 +901,26 @@ cudaError_t launch_reduce_t(const ReduceArgs& a, cudaStream_t stream) {
   p.num_heads = a.num_heads;
   p.partition_size = a.partition_size;
   p.max_num_partitions = a.max_num_partitions;
-  dim3 grid(a.num_heads, a.num_seqs);
-  splitk_reduce_kernel<HEAD_DIM><<<grid, HEAD_DIM, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (a.max_num_partitions <= 8) {  // one warp per (sequence, head), one memory round trip
+    cfg.gridDim = dim3((a.num_heads + 7) / 8, a.num_seqs);
+    e = cudaLaunchKernelEx(&cfg, splitk_reduce_small_kernel<HEAD_DIM, 8>, p);
+  } else if (a.max_num_partitions <= 32) {  // one warp per (sequence, head)
+    cfg.gridDim = dim3((a.num_heads + 7) / 8, a.num_seqs);
+    e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<HEAD_DIM, 1>, p);
+  } else {  // four warps per (sequence, head)
+    cfg.gridDim = dim3((a.num_heads + 1) / 2, a.num_seqs);
+    e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<HEAD_DIM, 4>, p);
+  }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -619,7 +940,17 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) 
   p.row_vecs = a.head_dim * 2 / 16;
   const int64_t warps = static_cast<int64_t>(a.num_tokens) * a.num_kv_heads;
   const int blocks = static_cast<int>((warps + 7) / 8);
-  reshape_and_cache_kernel<<<blocks, 256, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, reshape_and_cache_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -628,8 +959,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int G = a.num_heads / a.num_kv_heads;
   const bool two = G > 8;
   switch (a.head_dim) {
-    case 64: return two ? launch_decode_t<64, 2>(a, stream) : launch_decode_t<64, 1>(a, stream);
-    case 128: return two ? launch_decode_t<128, 2>(a, stream) : launch_decode_t<128, 1>(a, stream);
+    case 64: return two ? launch_decode_auto<64, 2>(a, stream) : launch_decode_auto<64, 1>(a, stream);
+    case 128: return two ? launch_decode_auto<128, 2>(a, stream) : launch_decode_auto<128, 1>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

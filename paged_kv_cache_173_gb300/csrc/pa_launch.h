@@ -38,7 +38,9 @@ struct DecodeArgs {
   int num_blocks;
   float scale;
   int partition_size;      // tokens; single-pass decode uses max_blocks_per_seq * block_size
-  int max_num_partitions;  // grid extent along partitions (1 for single-pass)
+  int max_num_partitions;  // grid extent along partitions (split-K)
+  int cluster_size;        // > 0: one cluster of this many CTAs per (sequence, KV head);
+                           // 0: plain grid; < 0: chosen from occupancy
 };
 
 struct ReduceArgs {

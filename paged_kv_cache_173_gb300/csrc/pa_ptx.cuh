@@ -138,6 +138,16 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// ------------------------------------------------ programmatic dependent launch --
+// Block until the grids this one depends on have completed and their memory
+// is visible (returns at once when the launch had no such dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid on the stream to start launching.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- math --
 // 2^x with the hardware's approximate base-2 exponential (ex2.approx.ftz.f32);
 // 2^-inf = 0.

@@ -225,6 +225,37 @@ def test_device_value_outcomes():
             assert np.max(np.abs(o[s] - ref[s])) <= TOL
 
 
+def _few_pairs(ctx, seed=7):
+    # few (sequence, KV head) pairs and a large table capacity: pa_decode runs
+    # clusters of 8 CTAs per pair, so short sequences leave CTAs without chunks
+    return workloads.build_batch(name="few", seed=seed, context_lens=ctx, num_heads=4, num_kv_heads=1,
+                                 head_dim=128, block_size=16, max_blocks_per_seq=256)
+
+
+def test_cluster_decode_with_empty_ctas():
+    b = _few_pairs([1, 5, 17, 100, 1000, 4096])
+    ref = oracle_out(b)
+    d = Dev(b)
+    assert max_err(d.decode(), ref) <= TOL
+    assert max_err(d.splitk(64), ref) <= TOL
+
+
+def test_cluster_device_value_outcomes():
+    b = _few_pairs([300, 40, 2000, 77])
+    d = Dev(b)
+    ref = oracle_out(b)
+    cl = b.context_lens.copy()
+    cl[0] = 0
+    cl[1] = b.max_blocks_per_seq * b.block_size + 3
+    bt = b.block_tables.copy()
+    bt[2, 100] = -5
+    o = d.decode(cl=T(cl), bt=T(bt)).float().cpu().numpy()
+    assert np.all(o[0] == 0)
+    assert np.isnan(o[1]).all()
+    assert np.isnan(o[2]).all()
+    assert np.max(np.abs(o[3] - ref[3])) <= TOL
+
+
 def test_empty_batch():
     b = workloads.tiny()
     d = Dev(b)

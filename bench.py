@@ -43,7 +43,7 @@ METRIC = "paged decode attention KV-read GB/s (% of GB300 HBM peak) and decode t
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_173_gb300", "csrc", "pa_kernels.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.md")
 
 
 # ----------------------------------------------------------------- workload
@@ -90,7 +90,8 @@ def load_traffic(workload: str, kernel: str):
     the current kernel source for this workload and kernel."""
     try:
         with open(TRAFFIC_FILE) as f:
-            rec = json.load(f)
+            text = f.read()
+        rec = json.loads(text.split("```json", 1)[1].split("```", 1)[0])
     except Exception:
         return None
     if rec.get("source_sha") != decode_source_sha():

@@ -129,6 +129,202 @@ struct DecodeCfg {
   static constexpr int SMEM_BYTES = 1024 + BAR_BYTES + (RING_BYTES > TAIL_BYTES ? RING_BYTES : TAIL_BYTES);
 };
 
+// ------------------------------------------------- per-warp attention state
+// One warp's running softmax state for the 8*NT query heads of a KV head:
+// maxima m and sums l (base 2) per head, and the unnormalised output O^T as
+// m16n8k16 accumulator fragments (rows = dims, columns = heads).
+template <int HEAD_DIM, int NT>
+struct WarpAcc {
+  static constexpr int KSTEPS = HEAD_DIM / 16;
+  float m[NT][2];
+  float l[NT][2];
+  float o[KSTEPS][NT][4];
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int dm = 0; dm < KSTEPS; ++dm)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[dm][nt][i] = 0.f;
+    }
+  }
+};
+
+// Query fragments (B operand of S = K Q^T): lane holds head nt*8 + lane/4,
+// dims ks*16 + {2c, 2c+1} and ks*16 + {2c+8, 2c+9} with c = lane % 4;
+// heads past the group are zero.
+template <int HEAD_DIM, int NT>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HEAD_DIM / 16][NT][2], const __half* q,
+                                             int s, int H, int kvh, int G, int lane) {
+  const int g = lane >> 2;
+  const int c4 = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hq = nt * 8 + g;
+    const bool hv = hq < G;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        q + (static_cast<size_t>(s) * H + kvh * G + (hv ? hq : 0)) * HEAD_DIM);
+#pragma unroll
+    for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
+      qf[ks][nt][0] = hv ? __ldg(qrow + ks * 8 + c4) : 0u;
+      qf[ks][nt][1] = hv ? __ldg(qrow + ks * 8 + c4 + 4) : 0u;
+    }
+  }
+}
+
+// Attend one 16-token chunk held in shared memory at `kb` (K boxes, then V
+// boxes at kb + half_bytes; 128-byte swizzle), of which the first `valid`
+// tokens belong to the sequence.  Updates the warp's running state.
+template <int HEAD_DIM, int NT>
+__device__ __forceinline__ void attend_chunk(WarpAcc<HEAD_DIM, NT>& acc,
+                                             const uint32_t (&qf)[HEAD_DIM / 16][NT][2], uint32_t kb,
+                                             uint32_t half_bytes, int valid, float sl2, int lane) {
+  constexpr int KSTEPS = HEAD_DIM / 16;
+  const int g = lane >> 2;
+  const int c4 = lane & 3;
+  const uint32_t vb = kb + half_bytes;
+
+  // S[16 tokens][8*NT heads] = K Q^T, as two independent MMA chains (even
+  // and odd k-steps) that are added at the end
+  float sacc[NT][4], sacc2[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[nt][i] = sacc2[nt][i] = 0.f;
+  // lane supplies row (lane & 15) at 16-byte unit 2*(ks%4) + lane/16 of box ks/4
+  const uint32_t ka = kb + (lane & 15) * 128;
+  const uint32_t kx = lane & 7;
+#pragma unroll
+  for (int ks = 0; ks < KSTEPS; ++ks) {
+    uint32_t a[4];
+    const uint32_t unit = ((ks & 3) * 2 + (lane >> 4)) ^ kx;
+    ldsm_x4(a, ka + (ks >> 2) * BOX_BYTES + unit * 16);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      mma_f16_16816((ks & 1) ? sacc2[nt] : sacc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[nt][i] += sacc2[nt][i];
+
+  // online softmax (base 2); slots past the context are excluded by select
+  const bool v0 = g < valid;
+  const bool v1 = g + 8 < valid;
+  uint32_t pb[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float x0 = v0 ? sacc[nt][0] * sl2 : -INFINITY;
+    const float x1 = v0 ? sacc[nt][1] * sl2 : -INFINITY;
+    const float x2 = v1 ? sacc[nt][2] * sl2 : -INFINITY;
+    const float x3 = v1 ? sacc[nt][3] * sl2 : -INFINITY;
+    float mx0 = fmaxf(x0, x2);
+    float mx1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, off));
+    }
+    const float mn0 = fmaxf(acc.m[nt][0], mx0);
+    const float mn1 = fmaxf(acc.m[nt][1], mx1);
+    const float cr0 = ex2(acc.m[nt][0] - mn0);
+    const float cr1 = ex2(acc.m[nt][1] - mn1);
+    const bool grew = __any_sync(FULL_MASK, (mn0 != acc.m[nt][0]) | (mn1 != acc.m[nt][1]));
+    acc.m[nt][0] = mn0;
+    acc.m[nt][1] = mn1;
+    const uint32_t lo = pack_half2(ex2(x0 - mn0), ex2(x1 - mn1));  // token g
+    const uint32_t hi = pack_half2(ex2(x2 - mn0), ex2(x3 - mn1));  // token g + 8
+    const float2 flo = unpack_half2(lo);
+    const float2 fhi = unpack_half2(hi);
+    // the running sum adds the same rounded weights that multiply V
+    acc.l[nt][0] = acc.l[nt][0] * cr0 + (flo.x + fhi.x);
+    acc.l[nt][1] = acc.l[nt][1] * cr1 + (flo.y + fhi.y);
+    if (grew) {  // a running maximum moved: rescale the accumulators
+#pragma unroll
+      for (int dm = 0; dm < KSTEPS; ++dm) {
+        acc.o[dm][nt][0] *= cr0;
+        acc.o[dm][nt][1] *= cr1;
+        acc.o[dm][nt][2] *= cr0;
+        acc.o[dm][nt][3] *= cr1;
+      }
+    }
+    pb[nt][0] = movmatrix_trans(lo);  // P^T tokens 0-7 as the B fragment
+    pb[nt][1] = movmatrix_trans(hi);  // P^T tokens 8-15
+  }
+
+  // O^T[d][heads] += V^T P^T; V rows past the context are zeroed by select
+  const int t0 = 2 * c4;
+  const uint32_t mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+  const uint32_t mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+  // lane supplies token row (lane & 7) + 8*(lane/16) at unit 2*(dm%4) + (lane/8)%2
+  const uint32_t va = vb + ((lane & 7) + ((lane >> 4) << 3)) * 128;
+  const uint32_t vsel = (lane >> 3) & 1;
+  const uint32_t vx = lane & 7;
+  if (valid == CHUNK) {
+#pragma unroll
+    for (int dm = 0; dm < KSTEPS; ++dm) {
+      uint32_t a[4];
+      ldsm_x4_trans(a, va + (dm >> 2) * BOX_BYTES + ((((dm & 3) * 2) + vsel) ^ vx) * 16);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(acc.o[dm][nt], a, pb[nt][0], pb[nt][1]);
+    }
+  } else {  // the last chunk of the sequence
+#pragma unroll
+    for (int dm = 0; dm < KSTEPS; ++dm) {
+      uint32_t a[4];
+      ldsm_x4_trans(a, va + (dm >> 2) * BOX_BYTES + ((((dm & 3) * 2) + vsel) ^ vx) * 16);
+      a[0] &= mlo;
+      a[1] &= mlo;
+      a[2] &= mhi;
+      a[3] &= mhi;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(acc.o[dm][nt], a, pb[nt][0], pb[nt][1]);
+    }
+  }
+}
+
+// Sum the per-lane partial running sums over the 8 row groups of the warp.
+template <int HEAD_DIM, int NT>
+__device__ __forceinline__ void reduce_warp_sums(WarpAcc<HEAD_DIM, NT>& acc) {
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) acc.l[nt][j] += __shfl_xor_sync(FULL_MASK, acc.l[nt][j], off);
+}
+
+// Store one warp's state in the merge area: o [GMAX][mo_pitch] floats, m and
+// l [GMAX] (call after reduce_warp_sums).
+template <int HEAD_DIM, int NT>
+__device__ __forceinline__ void store_warp_state(const WarpAcc<HEAD_DIM, NT>& acc, float* mo, float* mm,
+                                                 float* ml, int mo_pitch, int lane) {
+  const int g = lane >> 2;
+  const int c4 = lane & 3;
+#pragma unroll
+  for (int dm = 0; dm < HEAD_DIM / 16; ++dm)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int head = nt * 8 + 2 * c4 + (i & 1);
+        const int d = dm * 16 + g + (i >> 1) * 8;
+        mo[head * mo_pitch + d] = acc.o[dm][nt][i];
+      }
+  if (g == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        mm[nt * 8 + 2 * c4 + j] = acc.m[nt][j];
+        ml[nt * 8 + 2 * c4 + j] = acc.l[nt][j];
+      }
+  }
+}
+
 // CLUSTER = false: CTA (kvh, part, s) covers partition `part` of
 //   partition_chunks chunks; a sequence with one partition writes `out`,
 //   otherwise the partition's (o, m, l) go to the split-K workspace.
@@ -153,8 +349,6 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int s = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = lane >> 2;   // fragment row group
-  const int c4 = lane & 3;   // fragment column pair
   const int G = p.group;
   const int H = p.num_heads;
 
@@ -180,21 +374,8 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int first = c0 + warp;
   const int nk_cap = first < cmax ? (cmax - first + WARPS - 1) / WARPS : 0;
 
-  // ---- query fragments (B operand of S = K Q^T): lane holds head nt*8+g,
-  //      dims ks*16 + {2c4, 2c4+1} and ks*16 + {2c4+8, 2c4+9}
   uint32_t qf[KSTEPS][NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int hq = nt * 8 + g;
-    const bool hv = hq < G;
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        p.q + (static_cast<size_t>(s) * H + kvh * G + (hv ? hq : 0)) * HEAD_DIM);
-#pragma unroll
-    for (int ks = 0; ks < KSTEPS; ++ks) {
-      qf[ks][nt][0] = hv ? __ldg(qrow + ks * 8 + c4) : 0u;
-      qf[ks][nt][1] = hv ? __ldg(qrow + ks * 8 + c4 + 4) : 0u;
-    }
-  }
+  load_q_frags<HEAD_DIM, NT>(qf, p.q, s, H, kvh, G, lane);
 
   // ---- block-table window: lane j holds the physical block of this warp's
   //      chunk (kbase + j); the next window is fetched 32 chunks ahead.  Only
@@ -270,17 +451,8 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll 1
   for (int i = 0; i < STAGES && i < nk; ++i) issue_next();
 
-  float m_run[NT][2], l_run[NT][2];
-  float oacc[KSTEPS][NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt][0] = m_run[nt][1] = -INFINITY;
-    l_run[nt][0] = l_run[nt][1] = 0.f;
-#pragma unroll
-    for (int dm = 0; dm < KSTEPS; ++dm)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) oacc[dm][nt][i] = 0.f;
-  }
+  WarpAcc<HEAD_DIM, NT> acc;
+  acc.reset();
   const float sl2 = p.scale_log2;
 
   int consumed = 0;
@@ -296,106 +468,8 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     }
     const int ch = first + k * WARPS;
     const int valid = min(CHUNK, ctx - ch * CHUNK);
-    const uint32_t kb = smem_addr(wring + slot * Cfg::STAGE_BYTES);
-    const uint32_t vb = kb + Cfg::HALF_BYTES;
-
-    // S[16 tokens][8*NT heads] = K Q^T, as two independent MMA chains (even
-    // and odd k-steps) that are added at the end
-    float sacc[NT][4], sacc2[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sacc[nt][i] = sacc2[nt][i] = 0.f;
-    // lane supplies row (lane & 15) at 16-byte unit 2*(ks%4) + lane/16 of box ks/4
-    const uint32_t ka = kb + (lane & 15) * 128;
-    const uint32_t kx = lane & 7;
-#pragma unroll
-    for (int ks = 0; ks < KSTEPS; ++ks) {
-      uint32_t a[4];
-      const uint32_t unit = ((ks & 3) * 2 + (lane >> 4)) ^ kx;
-      ldsm_x4(a, ka + (ks >> 2) * BOX_BYTES + unit * 16);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        mma_f16_16816((ks & 1) ? sacc2[nt] : sacc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sacc[nt][i] += sacc2[nt][i];
-
-    // online softmax (base 2); slots past the context are excluded by select
-    const bool v0 = g < valid;
-    const bool v1 = g + 8 < valid;
-    uint32_t pb[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const float x0 = v0 ? sacc[nt][0] * sl2 : -INFINITY;
-      const float x1 = v0 ? sacc[nt][1] * sl2 : -INFINITY;
-      const float x2 = v1 ? sacc[nt][2] * sl2 : -INFINITY;
-      const float x3 = v1 ? sacc[nt][3] * sl2 : -INFINITY;
-      float mx0 = fmaxf(x0, x2);
-      float mx1 = fmaxf(x1, x3);
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, off));
-      }
-      const float mn0 = fmaxf(m_run[nt][0], mx0);
-      const float mn1 = fmaxf(m_run[nt][1], mx1);
-      const float cr0 = ex2(m_run[nt][0] - mn0);
-      const float cr1 = ex2(m_run[nt][1] - mn1);
-      const bool grew = __any_sync(FULL_MASK, (mn0 != m_run[nt][0]) | (mn1 != m_run[nt][1]));
-      m_run[nt][0] = mn0;
-      m_run[nt][1] = mn1;
-      const uint32_t lo = pack_half2(ex2(x0 - mn0), ex2(x1 - mn1));  // token g
-      const uint32_t hi = pack_half2(ex2(x2 - mn0), ex2(x3 - mn1));  // token g + 8
-      const float2 flo = unpack_half2(lo);
-      const float2 fhi = unpack_half2(hi);
-      // the running sum adds the same rounded weights that multiply V
-      l_run[nt][0] = l_run[nt][0] * cr0 + (flo.x + fhi.x);
-      l_run[nt][1] = l_run[nt][1] * cr1 + (flo.y + fhi.y);
-      if (grew) {  // a running maximum moved: rescale the accumulators
-#pragma unroll
-        for (int dm = 0; dm < KSTEPS; ++dm) {
-          oacc[dm][nt][0] *= cr0;
-          oacc[dm][nt][1] *= cr1;
-          oacc[dm][nt][2] *= cr0;
-          oacc[dm][nt][3] *= cr1;
-        }
-      }
-      pb[nt][0] = movmatrix_trans(lo);  // P^T tokens 0-7 as the B fragment
-      pb[nt][1] = movmatrix_trans(hi);  // P^T tokens 8-15
-    }
-
-    // O^T[d][heads] += V^T P^T; V rows past the context are zeroed by select
-    const int t0 = 2 * c4;
-    const uint32_t mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-    const uint32_t mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
-    // lane supplies token row (lane & 7) + 8*(lane/16) at unit 2*(dm%4) + (lane/8)%2
-    const uint32_t va = vb + ((lane & 7) + ((lane >> 4) << 3)) * 128;
-    const uint32_t vsel = (lane >> 3) & 1;
-    const uint32_t vx = lane & 7;
-    if (valid == CHUNK) {
-#pragma unroll
-      for (int dm = 0; dm < KSTEPS; ++dm) {
-        uint32_t a[4];
-        ldsm_x4_trans(a, va + (dm >> 2) * BOX_BYTES + ((((dm & 3) * 2) + vsel) ^ vx) * 16);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(oacc[dm][nt], a, pb[nt][0], pb[nt][1]);
-      }
-    } else {  // the last chunk of the sequence
-#pragma unroll
-      for (int dm = 0; dm < KSTEPS; ++dm) {
-        uint32_t a[4];
-        ldsm_x4_trans(a, va + (dm >> 2) * BOX_BYTES + ((((dm & 3) * 2) + vsel) ^ vx) * 16);
-        a[0] &= mlo;
-        a[1] &= mlo;
-        a[2] &= mhi;
-        a[3] &= mhi;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(oacc[dm][nt], a, pb[nt][0], pb[nt][1]);
-      }
-    }
+    attend_chunk<HEAD_DIM, NT>(acc, qf, smem_addr(wring + slot * Cfg::STAGE_BYTES), Cfg::HALF_BYTES, valid,
+                               sl2, lane);
 
     fence_proxy_async_smem();  // this lane's reads of the slot precede the refill's writes
     __syncwarp();
@@ -409,38 +483,15 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
       (void)mbar_wait_bounded(&wbar[k % STAGES], (k / STAGES) & 1, WAIT_LIMIT_NS);
   }
 
-  // ---- per-warp running sums: reduce the per-lane partials over the 8 row groups
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) l_run[nt][j] += __shfl_xor_sync(FULL_MASK, l_run[nt][j], off);
+  reduce_warp_sums<HEAD_DIM, NT>(acc);
 
   __syncthreads();  // every warp is done with its ring: reuse it for the merge
   float* mo = reinterpret_cast<float*>(ring);
   float* mm = mo + WARPS * GMAX * Cfg::MO_PITCH;
   float* ml = mm + WARPS * GMAX;
   int* mbad = reinterpret_cast<int*>(ml + WARPS * GMAX);
-#pragma unroll
-  for (int dm = 0; dm < KSTEPS; ++dm)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int head = nt * 8 + 2 * c4 + (i & 1);
-        const int d = dm * 16 + g + (i >> 1) * 8;
-        mo[(warp * GMAX + head) * Cfg::MO_PITCH + d] = oacc[dm][nt][i];
-      }
-  if (g == 0) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        mm[warp * GMAX + nt * 8 + 2 * c4 + j] = m_run[nt][j];
-        ml[warp * GMAX + nt * 8 + 2 * c4 + j] = l_run[nt][j];
-      }
-  }
+  store_warp_state<HEAD_DIM, NT>(acc, mo + warp * GMAX * Cfg::MO_PITCH, mm + warp * GMAX, ml + warp * GMAX,
+                                 Cfg::MO_PITCH, lane);
   if (lane == 0) mbad[warp] = bad ? 1 : 0;
   __syncthreads();
 
@@ -765,19 +816,11 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
 #define PA_DECODE_STAGES 2
 #endif
 
-template <int HEAD_DIM, int NT, bool CLUSTER>
-cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
-  constexpr int WARPS = PA_DECODE_WARPS;
-  constexpr int STAGES = PA_DECODE_STAGES;
-  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
-  auto kern = paged_decode_kernel<HEAD_DIM, NT, WARPS, STAGES, CLUSTER>;
-  static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
-  if (e != cudaSuccess) return e;
-
-  DecodeParams p;
+template <int HEAD_DIM>
+cudaError_t fill_decode_params(const DecodeArgs& a, DecodeParams* pp) {
+  DecodeParams& p = *pp;
   const int64_t pool_rows = static_cast<int64_t>(a.num_blocks) * a.block_size;
-  e = make_pool_map(&p.tmap_k, a.k_cache, HEAD_DIM, a.num_kv_heads, pool_rows);
+  cudaError_t e = make_pool_map(&p.tmap_k, a.k_cache, HEAD_DIM, a.num_kv_heads, pool_rows);
   if (e != cudaSuccess) return e;
   e = make_pool_map(&p.tmap_v, a.v_cache, HEAD_DIM, a.num_kv_heads, pool_rows);
   if (e != cudaSuccess) return e;
@@ -799,7 +842,22 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   p.partition_chunks = a.partition_size / CHUNK;
   p.max_num_partitions = a.max_num_partitions;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  return cudaSuccess;
+}
 
+template <int HEAD_DIM, int NT, bool CLUSTER>
+cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int WARPS = PA_DECODE_WARPS;
+  constexpr int STAGES = PA_DECODE_STAGES;
+  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
+  auto kern = paged_decode_kernel<HEAD_DIM, NT, WARPS, STAGES, CLUSTER>;
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
+  if (e != cudaSuccess) return e;
+
+  DecodeParams p;
+  e = fill_decode_params<HEAD_DIM>(a, &p);
+  if (e != cudaSuccess) return e;
   dim3 grid(a.num_kv_heads, CLUSTER ? a.cluster_size : a.max_num_partitions, a.num_seqs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;

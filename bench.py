@@ -99,6 +99,22 @@ def load_traffic(workload: str, kernel: str):
     return rec.get("per_workload", {}).get(f"{workload}/{kernel}")
 
 
+# ----------------------------------------------------------- multi-rank
+def max_over_ranks(value: float, device) -> float:
+    """The largest value over all ranks of the default process group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(kv_bytes_per_rank_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Weak scaling: every rank decodes its own batch of the same shape, so the
+    job moves world * steps * kv_bytes in the slowest rank's time."""
+    return kv_bytes_per_rank_step * steps * world / (max_ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
@@ -316,9 +332,7 @@ def run_gpu(args, rank: int, world: int):
         clocks = ClockSampler(dev.index)
         ms, per, walls, mode, G = time_path(torch, dev, stream, paths[name], R, K, W, clocks, dist_g)
         if dist_g is not None:
-            tt = torch.tensor([ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms = float(tt.item())
+            ms = max_over_ranks(ms, dev)
         results[name] = dict(ms=ms, per=per, clocks=clocks.summary(*walls), mode=mode, G=G)
     best = min(results, key=lambda n: results[n]["ms"])
     r0 = results[best]
@@ -330,7 +344,7 @@ def run_gpu(args, rank: int, world: int):
 
     peak, peak_kind = load_peak()
     ms = r0["ms"]
-    value = kv_bytes * K * world / (ms * 1e-3) / 1e9
+    value = whole_job_gbs(kv_bytes, K, world, ms)
     step_ms = ms / K
     achieved = kv_bytes / (t_decode * 1e-3) / 1e9
     traffic = load_traffic(args.workload, decode_name)
@@ -376,7 +390,7 @@ def run_gpu(args, rank: int, world: int):
         "e2e": e2e,
         "clocks": r0["clocks"],
         "paths": {n: {"ms_per_step": round(v["ms"] / K, 5),
-                      "value": round(kv_bytes * K * world / (v["ms"] * 1e-3) / 1e9, 1),
+                      "value": round(whole_job_gbs(kv_bytes, K, world, v["ms"]), 1),
                       "kernel_ms": {kn: round(float(x), 5) for (kn, _), x in zip(paths[n], v["per"])}}
                   for n, v in results.items()},
     }

@@ -42,7 +42,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention KV-read GB/s (% of GB300 HBM peak) and decode tokens/s"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_173_gb300", "csrc", "pa_kernels.cu")
+DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_173_gb300", "csrc", "pa_decode.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.md")
 
 

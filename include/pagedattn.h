@@ -28,11 +28,13 @@
  *    and never read or write outside the buffers whose sizes the call states:
  *    the documented outcome of a bad device value is given with each call.
  *  - Tensor pointers must be 16-byte aligned and the tensors contiguous in
- *    the layouts given.  Element type: dtype = PA_FP16 (IEEE binary16).
- *    All arithmetic after the loads is float32.
- *  - Supported shapes: head_dim in {64, 128}; block_size in {16, 32, 64,
- *    128, 256};
- *    num_heads a multiple of num_kv_heads with num_heads / num_kv_heads <= 16;
+ *    the layouts given.  Element type (dtype): PA_FP16 or PA_BF16, the same
+ *    for q, the caches, the new tokens and out.  Scores, softmax and
+ *    accumulation are float32; the attention weights enter the P.V product
+ *    as fp16, or for bf16 as a rounded value plus its rounded residual.
+ *  - Supported shapes: head_dim in {64, 128, 256}; block_size in {16, 32,
+ *    64, 128, 256}; num_heads a multiple of num_kv_heads with
+ *    num_heads / num_kv_heads <= 16 (<= 8 for head_dim 256);
  *    num_seqs <= 65535.
  */
 #ifndef PAGEDATTN_H
@@ -52,7 +54,10 @@ typedef enum pa_status {
   PA_ERR_CUDA = -3         /* a CUDA runtime error; see pa_last_error()   */
 } pa_status;
 
-typedef enum pa_dtype { PA_FP16 = 0 } pa_dtype;
+typedef enum pa_dtype {
+  PA_FP16 = 0, /* IEEE binary16 */
+  PA_BF16 = 1  /* bfloat16 (the upper half of an IEEE binary32) */
+} pa_dtype;
 
 /*
  * pa_reshape_and_cache -- write each new token's key and value into its slot.

@@ -29,13 +29,15 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB)
         L.pa_oracle_half_to_double.argtypes = [ctypes.c_uint16]
         L.pa_oracle_half_to_double.restype = ctypes.c_double
+        L.pa_oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        L.pa_oracle_bf16_to_double.restype = ctypes.c_double
         L.pa_oracle_locate_kv.argtypes = [_I64, _P, _I, ctypes.POINTER(ctypes.c_int32),
                                           ctypes.POINTER(ctypes.c_int32)]
         L.pa_oracle_locate_kv.restype = _I
         L.pa_oracle_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I]
         L.pa_oracle_reshape_and_cache.restype = _I
         L.pa_oracle_decode.argtypes = [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I64,
-                                       ctypes.c_double, _I]
+                                       ctypes.c_double, _I, _I]
         L.pa_oracle_decode.restype = _I
         L.pa_oracle_max_threads.argtypes = []
         L.pa_oracle_max_threads.restype = _I
@@ -56,6 +58,13 @@ def half_to_double(bits: int) -> float:
     return lib().pa_oracle_half_to_double(int(bits) & 0xFFFF)
 
 
+def bf16_to_double(bits: int) -> float:
+    return lib().pa_oracle_bf16_to_double(int(bits) & 0xFFFF)
+
+
+DTYPES = {"fp16": 0, "bf16": 1}
+
+
 def locate_kv(logical_token_idx: int, block_table, block_size: int) -> Tuple[int, int]:
     bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
     phys = ctypes.c_int32()
@@ -71,7 +80,7 @@ def reshape_and_cache(key: np.ndarray, value: np.ndarray, k_cache: np.ndarray, v
                       slot_mapping: np.ndarray, inplace: bool = False) -> Tuple[np.ndarray, np.ndarray]:
     """Return the pools after the write: updated copies (inputs untouched), or
     the given pools themselves, written in place, with ``inplace=True``."""
-    assert key.dtype == np.float16 and value.dtype == np.float16
+    assert key.itemsize == 2 and value.itemsize == 2  # float16, or bfloat16 bit patterns
     if inplace:
         assert k_cache.flags["C_CONTIGUOUS"] and v_cache.flags["C_CONTIGUOUS"]
         kc, vc = k_cache, v_cache
@@ -90,9 +99,11 @@ def reshape_and_cache(key: np.ndarray, value: np.ndarray, k_cache: np.ndarray, v
 
 
 def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables: np.ndarray,
-           context_lens: np.ndarray, scale: float, num_threads: int = 0) -> np.ndarray:
-    """float64 attention output [S, H, d]."""
-    q = np.ascontiguousarray(q, dtype=np.float16)
+           context_lens: np.ndarray, scale: float, num_threads: int = 0, dtype: str = "fp16") -> np.ndarray:
+    """float64 attention output [S, H, d].  q and the caches are float16
+    arrays, or (dtype="bf16") uint16 arrays of bfloat16 bit patterns."""
+    assert q.itemsize == 2 and k_cache.itemsize == 2 and v_cache.itemsize == 2
+    q = np.ascontiguousarray(q)
     k_cache = np.ascontiguousarray(k_cache)
     v_cache = np.ascontiguousarray(v_cache)
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
@@ -103,7 +114,7 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables
     out = np.zeros((S, H, d), dtype=np.float64)
     rc = lib().pa_oracle_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt),
                                 int(bt.shape[1]), _ptr(cl), S, H, Hk, d, B, N, float(scale),
-                                int(num_threads))
+                                int(num_threads), DTYPES[dtype])
     if rc:
         raise OracleError(f"decode precondition failed ({rc})")
     return out

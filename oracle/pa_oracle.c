@@ -3,7 +3,7 @@
  *
  * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
  * CPU-baseline leg load this library.  It shares no code, header or constant
- * with the CUDA library: it has its own float16 decoding, its own address
+ * with the CUDA library: it has its own float16 / bfloat16 decoding, its own address
  * translation and its own attention, all written for clarity, not speed.
  *
  * What it computes (sources, by page title and section):
@@ -35,7 +35,8 @@
  *    groups; the pages do not fix the mapping).
  *
  *  The K and V pools have the layout [num_blocks, block_size, num_kv_heads,
- *  head_dim]; values are IEEE binary16 bit patterns.
+ *  head_dim]; values are IEEE binary16 or bfloat16 bit patterns, each
+ *  decoded by its own routine below.
  */
 #include <math.h>
 #include <stdint.h>
@@ -69,6 +70,31 @@ double pa_oracle_half_to_double(uint16_t bits) {
         v = ldexp((double)(1024 + frac), expo - 25);
     }
     return sign ? -v : v;
+}
+
+/* bfloat16 -> double, from the format's definition: 1 sign bit, 8 exponent
+ * bits (bias 127), 7 fraction bits.  Exponent 0 encodes zero and subnormals
+ * (fraction * 2^-133), exponent 255 encodes infinities and NaNs. */
+double pa_oracle_bf16_to_double(uint16_t bits) {
+    const int sign = (bits >> 15) & 1;
+    const int expo = (bits >> 7) & 0xff;
+    const int frac = bits & 0x7f;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -133);
+    } else if (expo == 255) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(128 + frac), expo - 134);
+    }
+    return sign ? -v : v;
+}
+
+#define ORACLE_FP16 0
+#define ORACLE_BF16 1
+
+static double decode_elem(uint16_t bits, int dtype) {
+    return dtype == ORACLE_BF16 ? pa_oracle_bf16_to_double(bits) : pa_oracle_half_to_double(bits);
 }
 
 /* Logical token position -> (physical block, slot in block). */
@@ -129,7 +155,7 @@ int pa_oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint
 static int decode_one(double* out, const uint16_t* q_row, const uint16_t* k_cache,
                       const uint16_t* v_cache, const int32_t* table, int max_blocks_per_seq,
                       int ctx, int num_kv_heads, int kv_head, int head_dim, int block_size,
-                      int64_t num_blocks, double scale) {
+                      int64_t num_blocks, double scale, int dtype) {
     if (ctx < 0 || (int64_t)ctx > (int64_t)max_blocks_per_seq * block_size) return ORACLE_BAD_CONTEXT;
     for (int j = 0; j < head_dim; ++j) out[j] = 0.0;
     if (ctx == 0) return ORACLE_OK; /* an empty sequence yields zeros */
@@ -153,12 +179,12 @@ static int decode_one(double* out, const uint16_t* q_row, const uint16_t* k_cach
         }
         const int64_t base = (((int64_t)phys * block_size + off) * num_kv_heads + kv_head) * head_dim;
         for (int j = 0; j < head_dim; ++j) {
-            K[(size_t)i * head_dim + j] = pa_oracle_half_to_double(k_cache[base + j]);
-            V[(size_t)i * head_dim + j] = pa_oracle_half_to_double(v_cache[base + j]);
+            K[(size_t)i * head_dim + j] = decode_elem(k_cache[base + j], dtype);
+            V[(size_t)i * head_dim + j] = decode_elem(v_cache[base + j], dtype);
         }
     }
     if (rc == ORACLE_OK) {
-        for (int j = 0; j < head_dim; ++j) qd[j] = pa_oracle_half_to_double(q_row[j]);
+        for (int j = 0; j < head_dim; ++j) qd[j] = decode_elem(q_row[j], dtype);
         /* pass 1: scores and their maximum */
         double m = -INFINITY;
         for (int i = 0; i < ctx; ++i) {
@@ -184,14 +210,16 @@ static int decode_one(double* out, const uint16_t* q_row, const uint16_t* k_cach
 
 /* Decode attention for every (sequence, query head).
  * out: [num_seqs, num_heads, head_dim] float64; q: [num_seqs, num_heads,
- * head_dim] binary16; block_tables: [num_seqs, max_blocks_per_seq].
+ * head_dim]; block_tables: [num_seqs, max_blocks_per_seq].  q and the caches
+ * hold bit patterns of dtype 0 (binary16) or 1 (bfloat16).
  * num_threads <= 0 uses every available thread. */
 int pa_oracle_decode(double* out, const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
                      int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                     int64_t num_blocks, double scale, int num_threads) {
+                     int64_t num_blocks, double scale, int num_threads, int dtype) {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-        num_blocks <= 0 || max_blocks_per_seq <= 0 || num_heads % num_kv_heads != 0)
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || num_heads % num_kv_heads != 0 ||
+        (dtype != ORACLE_FP16 && dtype != ORACLE_BF16))
         return ORACLE_BAD_ARG;
     const int group = num_heads / num_kv_heads;
     const int64_t work = (int64_t)num_seqs * num_heads;
@@ -206,7 +234,7 @@ int pa_oracle_decode(double* out, const uint16_t* q, const uint16_t* k_cache, co
         const int r = decode_one(out + w * head_dim, q + w * head_dim, k_cache, v_cache,
                                  block_tables + (int64_t)s * max_blocks_per_seq, max_blocks_per_seq,
                                  context_lens[s], num_kv_heads, h / group, head_dim, block_size,
-                                 num_blocks, scale);
+                                 num_blocks, scale, dtype);
         if (r != ORACLE_OK) {
 #ifdef _OPENMP
 #pragma omp critical

@@ -18,6 +18,7 @@ PA_ERR_INVALID_ARG = -1
 PA_ERR_UNSUPPORTED = -2
 PA_ERR_CUDA = -3
 PA_FP16 = 0
+PA_BF16 = 1
 
 # Every function the header declares, with its ctypes signature.
 _P = ctypes.c_void_p

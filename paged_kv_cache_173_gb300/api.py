@@ -12,7 +12,15 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import PA_FP16, PagedAttnError  # noqa: F401  (re-exported)
+from ._lib import PA_BF16, PA_FP16, PagedAttnError  # noqa: F401  (re-exported)
+
+_DTYPES = {torch.float16: PA_FP16, torch.bfloat16: PA_BF16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}: float16 or bfloat16")
+    return _DTYPES[t.dtype]
 
 
 def _stream_ptr(t: torch.Tensor, stream: Optional[torch.cuda.Stream]) -> int:
@@ -49,10 +57,11 @@ def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.
         raise ValueError("key/value must be [T, Hk, d] matching the pools [N, B, Hk, d]")
     if slot_mapping.shape != (T,):
         raise ValueError("slot_mapping must be [T]")
+    dt = k_cache.dtype
     st = _lib.lib().pa_reshape_and_cache(
-        _need(key, "key", torch.float16, dev), _need(value, "value", torch.float16, dev),
-        _need(k_cache, "k_cache", torch.float16, dev), _need(v_cache, "v_cache", torch.float16, dev),
-        _need(slot_mapping, "slot_mapping", torch.int64, dev), T, N, B, Hk, d, PA_FP16,
+        _need(key, "key", dt, dev), _need(value, "value", dt, dev),
+        _need(k_cache, "k_cache", dt, dev), _need(v_cache, "v_cache", dt, dev),
+        _need(slot_mapping, "slot_mapping", torch.int64, dev), T, N, B, Hk, d, _dtype_code(k_cache),
         _stream_ptr(k_cache, stream))
     _lib.check("pa_reshape_and_cache", st)
 
@@ -65,8 +74,10 @@ def _decode_common(out, q, k_cache, v_cache, block_tables, context_lens):
         raise ValueError("q/out [S, H, d] must match the pools [N, B, Hk, d]")
     if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
         raise ValueError("block_tables must be [S, M] and context_lens [S]")
-    ptrs = (_need(out, "out", torch.float16, dev), _need(q, "q", torch.float16, dev),
-            _need(k_cache, "k_cache", torch.float16, dev), _need(v_cache, "v_cache", torch.float16, dev),
+    dt = q.dtype
+    _dtype_code(q)
+    ptrs = (_need(out, "out", dt, dev), _need(q, "q", dt, dev),
+            _need(k_cache, "k_cache", dt, dev), _need(v_cache, "v_cache", dt, dev),
             _need(block_tables, "block_tables", torch.int32, dev))
     cl = _need(context_lens, "context_lens", torch.int32, dev)
     return dev, S, H, d, N, B, Hk, int(block_tables.shape[1]), ptrs, cl
@@ -78,7 +89,7 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
     """Single-pass paged decode: out[S, H, d] = attention of q over each sequence's paged KV."""
     dev, S, H, d, N, B, Hk, M, (po, pq, pk, pv, pbt), pcl = _decode_common(
         out, q, k_cache, v_cache, block_tables, context_lens)
-    st = _lib.lib().pa_decode(po, pq, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N, float(scale), PA_FP16,
+    st = _lib.lib().pa_decode(po, pq, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N, float(scale), _dtype_code(q),
                               _stream_ptr(q, stream))
     _lib.check("pa_decode", st)
 
@@ -103,7 +114,7 @@ def pa_decode_splitk(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, 
     P = max_num_partitions or max_num_partitions_for(M, B, partition_size)
     ws = _need(workspace, "workspace", workspace.dtype, dev)
     st = _lib.lib().pa_decode_splitk(po, pq, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N, float(scale),
-                                     PA_FP16, int(partition_size), int(P), ws,
+                                     _dtype_code(q), int(partition_size), int(P), ws,
                                      workspace.numel() * workspace.element_size(),
                                      _stream_ptr(q, stream))
     _lib.check("pa_decode_splitk", st)
@@ -118,9 +129,9 @@ def pa_splitk_reduce(out: torch.Tensor, workspace: torch.Tensor, context_lens: t
     S, H, d = out.shape
     P = max_num_partitions or max_num_partitions_for(max_blocks_per_seq, block_size, partition_size)
     st = _lib.lib().pa_splitk_reduce(
-        _need(out, "out", torch.float16, dev), _need(workspace, "workspace", workspace.dtype, dev),
+        _need(out, "out", out.dtype, dev), _need(workspace, "workspace", workspace.dtype, dev),
         workspace.numel() * workspace.element_size(), _need(context_lens, "context_lens", torch.int32, dev),
-        int(max_blocks_per_seq), int(block_size), S, H, d, int(partition_size), int(P), PA_FP16,
+        int(max_blocks_per_seq), int(block_size), S, H, d, int(partition_size), int(P), _dtype_code(out),
         _stream_ptr(out, stream))
     _lib.check("pa_splitk_reduce", st)
 
@@ -136,7 +147,7 @@ def pa_decode_splitk_static(out: torch.Tensor, q: torch.Tensor, k_cache: torch.T
     dev, S, H, d, N, B, Hk, M, (po, pq, pk, pv, pbt), pcl = _decode_common(
         out, q, k_cache, v_cache, block_tables, context_lens)
     st = _lib.lib().pa_decode_splitk_static(po, pq, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N,
-                                            float(scale), PA_FP16, int(partition_size),
+                                            float(scale), _dtype_code(q), int(partition_size),
                                             _stream_ptr(q, stream))
     _lib.check("pa_decode_splitk_static", st)
 

@@ -44,9 +44,10 @@ int check_decode(const void* out, const void* q, const void* k_cache, const void
                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
                  int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                  int num_blocks, float scale, int dtype) {
-  if (dtype != PA_FP16) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 only)", dtype);
-  if (head_dim != 64 && head_dim != 128)
-    return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (64 or 128)", head_dim);
+  if (dtype != PA_FP16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 or PA_BF16)", dtype);
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (64, 128 or 256)", head_dim);
   if (!block_size_supported(block_size))
     return fail(PA_ERR_UNSUPPORTED, "block_size %d is not supported (16, 32, 64, 128 or 256)",
                 block_size);
@@ -58,6 +59,9 @@ int check_decode(const void* out, const void* q, const void* k_cache, const void
                 num_kv_heads);
   if (num_heads / num_kv_heads > 16)
     return fail(PA_ERR_UNSUPPORTED, "query group size %d exceeds 16", num_heads / num_kv_heads);
+  if (head_dim == 256 && num_heads / num_kv_heads > 8)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 supports query groups of at most 8 (got %d)",
+                num_heads / num_kv_heads);
   if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs %d is negative", num_seqs);
   if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535", num_seqs);
   if (max_blocks_per_seq <= 0)
@@ -141,7 +145,8 @@ size_t pa_splitk_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
 int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                          const int64_t* slot_mapping, int num_tokens, int num_blocks,
                          int block_size, int num_kv_heads, int head_dim, int dtype, void* stream) {
-  if (dtype != PA_FP16) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 only)", dtype);
+  if (dtype != PA_FP16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 or PA_BF16)", dtype);
   if (head_dim <= 0 || head_dim % 8 != 0 || head_dim > 1024)
     return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (a multiple of 8, at most 1024)",
                 head_dim);
@@ -173,6 +178,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   if (st != PA_OK) return st;
   if (num_seqs == 0) return ok();
   pa::DecodeArgs a{};
+  a.dtype = dtype;
   a.out = out;
   a.q = q;
   a.k_cache = k_cache;
@@ -212,6 +218,7 @@ int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* 
   if (st != PA_OK) return st;
   if (num_seqs == 0) return ok();
   pa::DecodeArgs a{};
+  a.dtype = dtype;
   a.out = out;
   a.q = q;
   a.k_cache = k_cache;
@@ -238,9 +245,10 @@ int pa_splitk_reduce(void* out, const void* workspace, size_t workspace_bytes,
                      const int32_t* context_lens, int max_blocks_per_seq, int block_size,
                      int num_seqs, int num_heads, int head_dim, int partition_size,
                      int max_num_partitions, int dtype, void* stream) {
-  if (dtype != PA_FP16) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 only)", dtype);
-  if (head_dim != 64 && head_dim != 128)
-    return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (64 or 128)", head_dim);
+  if (dtype != PA_FP16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 or PA_BF16)", dtype);
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (64, 128 or 256)", head_dim);
   if (!block_size_supported(block_size))
     return fail(PA_ERR_UNSUPPORTED, "block_size %d is not supported", block_size);
   if (num_seqs < 0 || num_heads <= 0)
@@ -257,7 +265,7 @@ int pa_splitk_reduce(void* out, const void* workspace, size_t workspace_bytes,
   if (!out || !context_lens) return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
   if (!aligned(out, 16) || !aligned(context_lens, 4))
     return fail(PA_ERR_INVALID_ARG, "out must be 16-byte aligned, context_lens 4-byte aligned");
-  pa::ReduceArgs a{out, static_cast<const float*>(workspace), context_lens, max_blocks_per_seq,
+  pa::ReduceArgs a{dtype, out, static_cast<const float*>(workspace), context_lens, max_blocks_per_seq,
                    block_size, num_seqs, num_heads, head_dim, partition_size, max_num_partitions};
   return cuda_status(pa::launch_splitk_reduce(a, static_cast<cudaStream_t>(stream)),
                      "split-K reduce launch");

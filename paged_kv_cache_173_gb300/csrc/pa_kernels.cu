@@ -1,51 +1,20 @@
-// pa_kernels.cu -- the paged decode hot path for GB300 (sm_103a).
+// pa_kernels.cu -- the cache write (reshape_and_cache) and the dispatch of
+// the decode kernels by element type.
 //
 //  reshape_and_cache_kernel   scatter new tokens' K/V rows into their slots
-//  paged_decode_kernel        one CTA per (KV head, partition, sequence);
-//                             each warp streams 16-token chunks of its share
-//                             of the partition through a private ring of
-//                             shared-memory stages filled by bulk async copies,
-//                             scores the G query heads of the group against
-//                             K with m16n8k16 MMAs, runs the online softmax in
-//                             float32 and accumulates P.V with MMAs; the warps
-//                             are merged in shared memory at the end
-//  splitk_reduce_kernel       log-sum-exp merge of the partitions
-//
-//  The same decode kernel also runs as thread-block clusters (pa_decode): the
-//  C CTAs of a cluster split one (sequence, KV head) evenly and merge their
-//  partial results through distributed shared memory, with the log-sum-exp
-//  rule of the reduce, so a single launch needs no workspace.
-//
-// The method: "vLLM PagedAttention source walk-through", section 3.4 (block
-// walk, mask, online softmax with correction factor exp(old_max - new_max));
-// "PagedAttention: when the KV cache meets OS paging", sections 3.2 and 5.1
-// (the kernel translates logical to physical blocks itself; table entries are
-// prefetched so the lookups hide under memory latency); "Unveiling the NVIDIA
-// driver stack: GPU page tables and vLLM PagedAttention", sections 6 and 7.3
-// (address arithmetic from the physical block id; adjacent threads read
-// adjacent bytes).
-#include <cuda.h>
-#include <cuda_fp16.h>
+//                             ("vLLM PagedAttention source walk-through",
+//                             section 3.2: append_token writes the token's KV
+//                             at block_table[pos / B], offset pos % B)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <cooperative_groups.h>
-
-#include <atomic>
-#include <cmath>
-#include <algorithm>
-#include <type_traits>
-
 #include "pa_launch.h"
 #include "pa_ptx.cuh"
+#include "pagedattn.h"
 
 namespace pa {
 
 namespace {
-
-constexpr unsigned FULL_MASK = 0xffffffffu;
-constexpr int CHUNK = 16;                       // tokens per pipeline stage
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000;  // 2 s: a stage that takes longer is an error
 
 // ============================================================ reshape_and_cache
 struct ReshapeParams {
@@ -76,910 +45,6 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_con
   const uint4* src = (is_v ? p.value : p.key) + (static_cast<int64_t>(t) * p.num_kv_heads + h) * p.row_vecs;
   uint4* dst = (is_v ? p.v_cache : p.k_cache) + (slot * p.num_kv_heads + h) * p.row_vecs;
   for (int i = lane & 15; i < p.row_vecs; i += 16) dst[i] = __ldg(src + i);
-}
-
-// ================================================================ decode
-struct DecodeParams {
-  // Tensor maps over the K and V pools viewed as [N*B rows][Hk][d] (3-D,
-  // innermost first: d, Hk, rows) with a 64 x 1 x 16 box, 128-byte swizzle.
-  CUtensorMap tmap_k;
-  CUtensorMap tmap_v;
-  __half* out;
-  const __half* q;
-  const int32_t* block_tables;
-  const int32_t* context_lens;
-  float* ws_o;
-  float* ws_m;
-  float* ws_l;
-  int max_blocks_per_seq;
-  int num_heads;
-  int num_kv_heads;
-  int group;
-  int block_size;
-  int chunks_per_block_log2;  // block_size / 16 is a power of two
-  int num_blocks;
-  int partition_chunks;
-  int max_num_partitions;
-  float scale_log2;  // scale * log2(e): scores are kept in base-2 units
-};
-
-// Shared-memory stage of one 16-token chunk of one KV head: TMA boxes of 16
-// rows x 64 dims (128 bytes per row, 2 KB per box), 128-byte swizzled: the
-// 16-byte unit u of row r sits at unit u ^ (r % 8).  K boxes first (dims
-// 0-63, 64-127, ...), then V boxes.
-constexpr int BOX_DIMS = 64;
-constexpr int BOX_BYTES = CHUNK * BOX_DIMS * 2;
-
-template <int HEAD_DIM, int NT, int WARPS, int STAGES>
-struct DecodeCfg {
-  static constexpr int DBOX = HEAD_DIM / BOX_DIMS;  // boxes per row of K (or V)
-  static constexpr int HALF_BYTES = DBOX * BOX_BYTES;
-  static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
-  static constexpr int RING_BYTES = WARPS * STAGES * STAGE_BYTES;
-  static constexpr int GMAX = NT * 8;
-  static constexpr int MO_PITCH = HEAD_DIM + 4;  // floats; spreads the merge writes over banks
-  static constexpr int MERGE_BYTES = WARPS * GMAX * MO_PITCH * 4 + 2 * WARPS * GMAX * 4 + WARPS * 4;
-  // CTA result shared with the other CTAs of a cluster: o [GMAX][HEAD_DIM], m, l [GMAX]
-  static constexpr int CTA_OFFSET = (MERGE_BYTES + 15) / 16 * 16;
-  static constexpr int CTA_BYTES = GMAX * HEAD_DIM * 4 + 2 * GMAX * 4;
-  static constexpr int TAIL_BYTES = CTA_OFFSET + CTA_BYTES;
-  static constexpr int BAR_BYTES = 1024;  // the ring that follows is 1024-byte aligned
-  static_assert(WARPS * STAGES * 8 <= BAR_BYTES, "barrier area");
-  // + 1024 so that the ring can be aligned whatever the base alignment is
-  static constexpr int SMEM_BYTES = 1024 + BAR_BYTES + (RING_BYTES > TAIL_BYTES ? RING_BYTES : TAIL_BYTES);
-};
-
-// ------------------------------------------------- per-warp attention state
-// One warp's running softmax state for the 8*NT query heads of a KV head:
-// maxima m and sums l (base 2) per head, and the unnormalised output O^T as
-// m16n8k16 accumulator fragments (rows = dims, columns = heads).
-template <int HEAD_DIM, int NT>
-struct WarpAcc {
-  static constexpr int KSTEPS = HEAD_DIM / 16;
-  float m[NT][2];
-  float l[NT][2];
-  float o[KSTEPS][NT][4];
-
-  __device__ __forceinline__ void reset() {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      m[nt][0] = m[nt][1] = -INFINITY;
-      l[nt][0] = l[nt][1] = 0.f;
-#pragma unroll
-      for (int dm = 0; dm < KSTEPS; ++dm)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[dm][nt][i] = 0.f;
-    }
-  }
-};
-
-// Query fragments (B operand of S = K Q^T): lane holds head nt*8 + lane/4,
-// dims ks*16 + {2c, 2c+1} and ks*16 + {2c+8, 2c+9} with c = lane % 4;
-// heads past the group are zero.
-template <int HEAD_DIM, int NT>
-__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HEAD_DIM / 16][NT][2], const __half* q,
-                                             int s, int H, int kvh, int G, int lane) {
-  const int g = lane >> 2;
-  const int c4 = lane & 3;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int hq = nt * 8 + g;
-    const bool hv = hq < G;
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        q + (static_cast<size_t>(s) * H + kvh * G + (hv ? hq : 0)) * HEAD_DIM);
-#pragma unroll
-    for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
-      qf[ks][nt][0] = hv ? __ldg(qrow + ks * 8 + c4) : 0u;
-      qf[ks][nt][1] = hv ? __ldg(qrow + ks * 8 + c4 + 4) : 0u;
-    }
-  }
-}
-
-// Attend one 16-token chunk held in shared memory at `kb` (K boxes, then V
-// boxes at kb + half_bytes; 128-byte swizzle), of which the first `valid`
-// tokens belong to the sequence.  Updates the warp's running state.
-template <int HEAD_DIM, int NT>
-__device__ __forceinline__ void attend_chunk(WarpAcc<HEAD_DIM, NT>& acc,
-                                             const uint32_t (&qf)[HEAD_DIM / 16][NT][2], uint32_t kb,
-                                             uint32_t half_bytes, int valid, float sl2, int lane) {
-  constexpr int KSTEPS = HEAD_DIM / 16;
-  const int g = lane >> 2;
-  const int c4 = lane & 3;
-  const uint32_t vb = kb + half_bytes;
-
-  // S[16 tokens][8*NT heads] = K Q^T, as two independent MMA chains (even
-  // and odd k-steps) that are added at the end
-  float sacc[NT][4], sacc2[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sacc[nt][i] = sacc2[nt][i] = 0.f;
-  // lane supplies row (lane & 15) at 16-byte unit 2*(ks%4) + lane/16 of box ks/4
-  const uint32_t ka = kb + (lane & 15) * 128;
-  const uint32_t kx = lane & 7;
-#pragma unroll
-  for (int ks = 0; ks < KSTEPS; ++ks) {
-    uint32_t a[4];
-    const uint32_t unit = ((ks & 3) * 2 + (lane >> 4)) ^ kx;
-    ldsm_x4(a, ka + (ks >> 2) * BOX_BYTES + unit * 16);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      mma_f16_16816((ks & 1) ? sacc2[nt] : sacc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
-  }
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sacc[nt][i] += sacc2[nt][i];
-
-  // online softmax (base 2); slots past the context are excluded by select
-  const bool v0 = g < valid;
-  const bool v1 = g + 8 < valid;
-  uint32_t pb[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const float x0 = v0 ? sacc[nt][0] * sl2 : -INFINITY;
-    const float x1 = v0 ? sacc[nt][1] * sl2 : -INFINITY;
-    const float x2 = v1 ? sacc[nt][2] * sl2 : -INFINITY;
-    const float x3 = v1 ? sacc[nt][3] * sl2 : -INFINITY;
-    float mx0 = fmaxf(x0, x2);
-    float mx1 = fmaxf(x1, x3);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, off));
-    }
-    const float mn0 = fmaxf(acc.m[nt][0], mx0);
-    const float mn1 = fmaxf(acc.m[nt][1], mx1);
-    const float cr0 = ex2(acc.m[nt][0] - mn0);
-    const float cr1 = ex2(acc.m[nt][1] - mn1);
-    const bool grew = __any_sync(FULL_MASK, (mn0 != acc.m[nt][0]) | (mn1 != acc.m[nt][1]));
-    acc.m[nt][0] = mn0;
-    acc.m[nt][1] = mn1;
-    const uint32_t lo = pack_half2(ex2(x0 - mn0), ex2(x1 - mn1));  // token g
-    const uint32_t hi = pack_half2(ex2(x2 - mn0), ex2(x3 - mn1));  // token g + 8
-    const float2 flo = unpack_half2(lo);
-    const float2 fhi = unpack_half2(hi);
-    // the running sum adds the same rounded weights that multiply V
-    acc.l[nt][0] = acc.l[nt][0] * cr0 + (flo.x + fhi.x);
-    acc.l[nt][1] = acc.l[nt][1] * cr1 + (flo.y + fhi.y);
-    if (grew) {  // a running maximum moved: rescale the accumulators
-#pragma unroll
-      for (int dm = 0; dm < KSTEPS; ++dm) {
-        acc.o[dm][nt][0] *= cr0;
-        acc.o[dm][nt][1] *= cr1;
-        acc.o[dm][nt][2] *= cr0;
-        acc.o[dm][nt][3] *= cr1;
-      }
-    }
-    pb[nt][0] = movmatrix_trans(lo);  // P^T tokens 0-7 as the B fragment
-    pb[nt][1] = movmatrix_trans(hi);  // P^T tokens 8-15
-  }
-
-  // O^T[d][heads] += V^T P^T; V rows past the context are zeroed by select
-  const int t0 = 2 * c4;
-  const uint32_t mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-  const uint32_t mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
-  // lane supplies token row (lane & 7) + 8*(lane/16) at unit 2*(dm%4) + (lane/8)%2
-  const uint32_t va = vb + ((lane & 7) + ((lane >> 4) << 3)) * 128;
-  const uint32_t vsel = (lane >> 3) & 1;
-  const uint32_t vx = lane & 7;
-  if (valid == CHUNK) {
-#pragma unroll
-    for (int dm = 0; dm < KSTEPS; ++dm) {
-      uint32_t a[4];
-      ldsm_x4_trans(a, va + (dm >> 2) * BOX_BYTES + ((((dm & 3) * 2) + vsel) ^ vx) * 16);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(acc.o[dm][nt], a, pb[nt][0], pb[nt][1]);
-    }
-  } else {  // the last chunk of the sequence
-#pragma unroll
-    for (int dm = 0; dm < KSTEPS; ++dm) {
-      uint32_t a[4];
-      ldsm_x4_trans(a, va + (dm >> 2) * BOX_BYTES + ((((dm & 3) * 2) + vsel) ^ vx) * 16);
-      a[0] &= mlo;
-      a[1] &= mlo;
-      a[2] &= mhi;
-      a[3] &= mhi;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(acc.o[dm][nt], a, pb[nt][0], pb[nt][1]);
-    }
-  }
-}
-
-// Sum the per-lane partial running sums over the 8 row groups of the warp.
-template <int HEAD_DIM, int NT>
-__device__ __forceinline__ void reduce_warp_sums(WarpAcc<HEAD_DIM, NT>& acc) {
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) acc.l[nt][j] += __shfl_xor_sync(FULL_MASK, acc.l[nt][j], off);
-}
-
-// Store one warp's state in the merge area: o [GMAX][mo_pitch] floats, m and
-// l [GMAX] (call after reduce_warp_sums).
-template <int HEAD_DIM, int NT>
-__device__ __forceinline__ void store_warp_state(const WarpAcc<HEAD_DIM, NT>& acc, float* mo, float* mm,
-                                                 float* ml, int mo_pitch, int lane) {
-  const int g = lane >> 2;
-  const int c4 = lane & 3;
-#pragma unroll
-  for (int dm = 0; dm < HEAD_DIM / 16; ++dm)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int head = nt * 8 + 2 * c4 + (i & 1);
-        const int d = dm * 16 + g + (i >> 1) * 8;
-        mo[head * mo_pitch + d] = acc.o[dm][nt][i];
-      }
-  if (g == 0) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        mm[nt * 8 + 2 * c4 + j] = acc.m[nt][j];
-        ml[nt * 8 + 2 * c4 + j] = acc.l[nt][j];
-      }
-  }
-}
-
-// CLUSTER = false: CTA (kvh, part, s) covers partition `part` of
-//   partition_chunks chunks; a sequence with one partition writes `out`,
-//   otherwise the partition's (o, m, l) go to the split-K workspace.
-// CLUSTER = true: gridDim.y CTAs form a cluster per (kvh, s); CTA `part`
-//   takes chunks [part * n / C, (part + 1) * n / C) of the sequence's n chunks
-//   and the cluster merges the C results into `out`.
-template <int HEAD_DIM, int NT, int WARPS, int STAGES, bool CLUSTER>
-__global__ void __launch_bounds__(WARPS * 32)
-paged_decode_kernel(const __grid_constant__ DecodeParams p) {
-  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
-  constexpr int KSTEPS = HEAD_DIM / 16;
-  constexpr int GMAX = Cfg::GMAX;
-
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // swizzled TMA destinations must be 1024-byte aligned
-  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint8_t* ring = smem + Cfg::BAR_BYTES;
-
-  const int kvh = blockIdx.x;
-  const int part = blockIdx.y;
-  const int s = blockIdx.z;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int G = p.group;
-  const int H = p.num_heads;
-
-  // The previous kernel on the stream (typically the cache write) may still
-  // be running: everything up to here overlapped with its tail.
-  grid_dependency_wait();
-
-  // Loads that do not depend on the context length go out first, so that
-  // their latencies overlap with the one of context_lens[s].
-  const int ctx = __ldg(p.context_lens + s);
-  const int cpb_log2 = p.chunks_per_block_log2;
-  const int table_chunks = p.max_blocks_per_seq << cpb_log2;
-  const int cap = p.max_blocks_per_seq * p.block_size;
-  const bool ctx_bad = ctx < 0 || ctx > cap;
-  const int nchunks = ctx_bad ? 0 : (ctx + CHUNK - 1) / CHUNK;
-  const int nclu = CLUSTER ? static_cast<int>(gridDim.y) : 1;
-  // The split-K chunk range is known before the context length arrives; the
-  // cluster split depends on it.
-  const int c0 = CLUSTER ? static_cast<int>((static_cast<int64_t>(part) * nchunks) / nclu)
-                         : part * p.partition_chunks;
-  const int cmax = CLUSTER ? static_cast<int>((static_cast<int64_t>(part + 1) * nchunks) / nclu)
-                           : min(c0 + p.partition_chunks, table_chunks);  // chunks the table can hold
-  const int first = c0 + warp;
-  const int nk_cap = first < cmax ? (cmax - first + WARPS - 1) / WARPS : 0;
-
-  uint32_t qf[KSTEPS][NT][2];
-  load_q_frags<HEAD_DIM, NT>(qf, p.q, s, H, kvh, G, lane);
-
-  // ---- block-table window: lane j holds the physical block of this warp's
-  //      chunk (kbase + j); the next window is fetched 32 chunks ahead.  Only
-  //      entries inside the table row are read; those past the context are
-  //      fetched but never used.
-  const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
-  auto win_load = [&](int kbase) -> int {
-    const int k = kbase + lane;
-    if (k >= nk_cap) return 0;
-    return __ldg(bt + ((first + k * WARPS) >> cpb_log2));
-  };
-  int win_cur = win_load(0);
-  int win_nxt = win_load(32);
-
-  uint64_t* wbar = bars + warp * STAGES;
-  uint8_t* wring = ring + warp * STAGES * Cfg::STAGE_BYTES;
-  if (lane == 0) {
-    for (int i = 0; i < STAGES; ++i) mbar_init(&wbar[i], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
-  const int nparts = CLUSTER ? nclu : (nchunks + p.partition_chunks - 1) / p.partition_chunks;
-
-  if (nchunks == 0) {
-    // Empty sequence -> zeros; impossible context length -> NaN.  Written once.
-    if (part == 0) {
-      const __half v = ctx_bad ? __float2half(NAN) : __float2half(0.f);
-      __half* o = p.out + (static_cast<size_t>(s) * H + kvh * G) * HEAD_DIM;
-      for (int i = threadIdx.x; i < G * HEAD_DIM; i += WARPS * 32) o[i] = v;
-    }
-    allow_dependent_launch();
-    return;  // in a cluster every CTA takes this exit together
-  }
-  if (!CLUSTER && part >= nparts) {
-    allow_dependent_launch();
-    return;
-  }
-  const bool single = !CLUSTER && nparts == 1;
-  const int c1 = CLUSTER ? cmax : min(c0 + p.partition_chunks, nchunks);
-  const int nk = first < c1 ? (c1 - first + WARPS - 1) / WARPS : 0;  // <= nk_cap
-
-  int issued = 0;
-  bool bad = false;
-
-  auto issue_next = [&]() {
-    const int k = issued;
-    if (k > 0 && (k & 31) == 0) {
-      win_cur = win_nxt;
-      win_nxt = win_load(k + 32);
-    }
-    int phys = __shfl_sync(FULL_MASK, win_cur, k & 31);
-    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
-      bad = true;  // never read outside the pool; the result becomes NaN
-      phys = 0;
-    }
-    const int ch = first + k * WARPS;
-    const int row0 = (ch & ((1 << cpb_log2) - 1)) * CHUNK;
-    const int slot = k % STAGES;
-    if (lane == 0) {
-      uint8_t* dst = wring + slot * Cfg::STAGE_BYTES;
-      const int y = phys * p.block_size + row0;  // pool row of the chunk's first token
-      mbar_arrive_expect_tx(&wbar[slot], Cfg::STAGE_BYTES);
-#pragma unroll
-      for (int b = 0; b < Cfg::DBOX; ++b) {
-        tma_load_3d(dst + b * BOX_BYTES, &p.tmap_k, b * BOX_DIMS, kvh, y, &wbar[slot]);
-        tma_load_3d(dst + Cfg::HALF_BYTES + b * BOX_BYTES, &p.tmap_v, b * BOX_DIMS, kvh, y, &wbar[slot]);
-      }
-    }
-    ++issued;
-  };
-
-#pragma unroll 1
-  for (int i = 0; i < STAGES && i < nk; ++i) issue_next();
-
-  WarpAcc<HEAD_DIM, NT> acc;
-  acc.reset();
-  const float sl2 = p.scale_log2;
-
-  int consumed = 0;
-  bool timed_out = false;
-#pragma unroll 1
-  for (; consumed < nk; ++consumed) {
-    const int k = consumed;
-    const int slot = k % STAGES;
-    const bool ok = mbar_wait_bounded(&wbar[slot], (k / STAGES) & 1, WAIT_LIMIT_NS);
-    if (!__all_sync(FULL_MASK, ok)) {  // a warp-uniform decision
-      timed_out = true;
-      break;
-    }
-    const int ch = first + k * WARPS;
-    const int valid = min(CHUNK, ctx - ch * CHUNK);
-    attend_chunk<HEAD_DIM, NT>(acc, qf, smem_addr(wring + slot * Cfg::STAGE_BYTES), Cfg::HALF_BYTES, valid,
-                               sl2, lane);
-
-    fence_proxy_async_smem();  // this lane's reads of the slot precede the refill's writes
-    __syncwarp();
-    if (issued < nk) issue_next();
-  }
-
-  if (timed_out) {
-    bad = true;
-    // let the copies still in flight land before the shared memory is reused
-    for (int k = consumed; k < issued; ++k)
-      (void)mbar_wait_bounded(&wbar[k % STAGES], (k / STAGES) & 1, WAIT_LIMIT_NS);
-  }
-
-  reduce_warp_sums<HEAD_DIM, NT>(acc);
-
-  __syncthreads();  // every warp is done with its ring: reuse it for the merge
-  float* mo = reinterpret_cast<float*>(ring);
-  float* mm = mo + WARPS * GMAX * Cfg::MO_PITCH;
-  float* ml = mm + WARPS * GMAX;
-  int* mbad = reinterpret_cast<int*>(ml + WARPS * GMAX);
-  store_warp_state<HEAD_DIM, NT>(acc, mo + warp * GMAX * Cfg::MO_PITCH, mm + warp * GMAX, ml + warp * GMAX,
-                                 Cfg::MO_PITCH, lane);
-  if (lane == 0) mbad[warp] = bad ? 1 : 0;
-  __syncthreads();
-
-  bool any_bad = false;
-#pragma unroll
-  for (int w = 0; w < WARPS; ++w) any_bad |= mbad[w] != 0;
-
-  for (int idx = threadIdx.x; idx < G * HEAD_DIM; idx += WARPS * 32) {
-    const int head = idx / HEAD_DIM;
-    const int d = idx - head * HEAD_DIM;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, mm[w * GMAX + head]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {  // only a cluster CTA can have no chunk at all
-#pragma unroll
-      for (int w = 0; w < WARPS; ++w) {
-        const float f = ex2(mm[w * GMAX + head] - M);  // warps without chunks: 2^-inf = 0
-        L += ml[w * GMAX + head] * f;
-        O += mo[(w * GMAX + head) * Cfg::MO_PITCH + d] * f;
-      }
-    }
-    const float r = any_bad ? NAN : (L > 0.f ? O / L : 0.f);
-    const size_t qrow = static_cast<size_t>(s) * H + kvh * G + head;
-    if (CLUSTER) {
-      // an empty CTA publishes m = -inf, l = 0: weight 0 in the cluster merge
-      float* cta = reinterpret_cast<float*>(ring + Cfg::CTA_OFFSET);
-      cta[head * HEAD_DIM + d] = r;
-      if (d == 0) {
-        cta[GMAX * HEAD_DIM + head] = any_bad ? 0.f : M;
-        cta[GMAX * HEAD_DIM + GMAX + head] = any_bad ? 1.f : L;
-      }
-    } else if (single) {
-      p.out[qrow * HEAD_DIM + d] = __float2half_rn(r);
-    } else {
-      const size_t row = qrow * p.max_num_partitions + part;
-      p.ws_o[row * HEAD_DIM + d] = r;
-      if (d == 0) {
-        p.ws_m[row] = any_bad ? 0.f : M;
-        p.ws_l[row] = any_bad ? 1.f : L;
-      }
-    }
-  }
-
-  if constexpr (CLUSTER) {
-    // Merge the cluster's CTA results (o_r, m_r, l_r) read from each CTA's
-    // shared memory: M = max m_r, w_r = l_r 2^(m_r - M), out = sum w_r o_r / sum w_r.
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();  // every CTA's result is in its shared memory
-    float* cta = reinterpret_cast<float*>(ring + Cfg::CTA_OFFSET);
-    const int rank = static_cast<int>(cluster.block_rank());
-    for (int idx = rank * (WARPS * 32) + threadIdx.x; idx < G * HEAD_DIM; idx += nclu * WARPS * 32) {
-      const int head = idx / HEAD_DIM;
-      const int d = idx - head * HEAD_DIM;
-      float M = -INFINITY;
-      for (int r = 0; r < nclu; ++r) {
-        const float* peer = cluster.map_shared_rank(cta, r);
-        M = fmaxf(M, peer[GMAX * HEAD_DIM + head]);
-      }
-      float L = 0.f, O = 0.f;
-      for (int r = 0; r < nclu; ++r) {
-        const float* peer = cluster.map_shared_rank(cta, r);
-        const float w = peer[GMAX * HEAD_DIM + GMAX + head] * ex2(peer[GMAX * HEAD_DIM + head] - M);
-        L += w;
-        O += w * peer[head * HEAD_DIM + d];
-      }
-      p.out[(static_cast<size_t>(s) * H + kvh * G + head) * HEAD_DIM + d] = __float2half_rn(O / L);
-    }
-    cluster.sync();  // no CTA leaves while the others still read its shared memory
-  }
-  allow_dependent_launch();
-}
-
-// ================================================================ reduce
-struct ReduceParams {
-  __half* out;
-  const float* ws_o;
-  const float* ws_m;
-  const float* ws_l;
-  const int32_t* context_lens;
-  int cap;  // max_blocks_per_seq * block_size
-  int num_heads;
-  int partition_size;
-  int max_num_partitions;
-};
-
-// At most PMAX partitions: one warp per (sequence, head), 8 per CTA.  Every
-// load is issued at once -- the context length, lane q's (m_q, l_q) and each
-// lane's HEAD_DIM / 32 dims of all PMAX partition outputs -- so the kernel
-// waits for memory once.  Rows past the sequence's partitions hold stale data
-// and are dropped by select, never multiplied by a zero weight.
-template <int HEAD_DIM, int PMAX>
-__global__ void __launch_bounds__(256) splitk_reduce_small_kernel(const __grid_constant__ ReduceParams p) {
-  constexpr int VEC = HEAD_DIM / 32;
-  using VecT = typename std::conditional<VEC == 4, float4, float2>::type;
-  grid_dependency_wait();  // the partitions come from the decode kernel just before
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int h = blockIdx.x * 8 + warp;
-  const int s = blockIdx.y;
-  if (h >= p.num_heads) return;
-  const size_t row0 = (static_cast<size_t>(s) * p.num_heads + h) * p.max_num_partitions;
-  const int ctx = __ldg(p.context_lens + s);
-  VecT o[PMAX];
-#pragma unroll
-  for (int q = 0; q < PMAX; ++q)
-    o[q] = q < p.max_num_partitions ? __ldg(reinterpret_cast<const VecT*>(p.ws_o + (row0 + q) * HEAD_DIM) + lane)
-                                   : VecT{};
-  const bool mine = lane < p.max_num_partitions;
-  const float m = mine ? __ldg(p.ws_m + row0 + lane) : -INFINITY;
-  const float l = mine ? __ldg(p.ws_l + row0 + lane) : 0.f;
-  const int nparts = (ctx <= 0 || ctx > p.cap) ? 0 : (ctx + p.partition_size - 1) / p.partition_size;
-  if (nparts <= 1) return;  // finished by the decode kernel
-  const float mv = lane < nparts ? m : -INFINITY;
-  float M = mv;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  const float w = lane < nparts ? l * ex2(m - M) : 0.f;
-  float L = w;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  float acc[VEC];
-#pragma unroll
-  for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-#pragma unroll
-  for (int q = 0; q < PMAX; ++q) {
-    const float wq = __shfl_sync(0xffffffffu, w, q);
-    if (q < nparts) {
-      acc[0] += wq * o[q].x;
-      acc[1] += wq * o[q].y;
-      if constexpr (VEC == 4) {
-        acc[2] += wq * o[q].z;
-        acc[3] += wq * o[q].w;
-      }
-    }
-  }
-  __half* dst = p.out + (static_cast<size_t>(s) * p.num_heads + h) * HEAD_DIM + lane * VEC;
-  const float inv = 1.f / L;
-  if constexpr (VEC == 4) {
-    __half2 a = __floats2half2_rn(acc[0] * inv, acc[1] * inv);
-    __half2 b = __floats2half2_rn(acc[2] * inv, acc[3] * inv);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(dst) = u;
-  } else {
-    *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(acc[0] * inv, acc[1] * inv);
-  }
-}
-
-// Warps per (sequence, head): WPH warps split the partitions (q = sub, sub +
-// WPH, ...); each lane owns HEAD_DIM / 32 consecutive output dims and reads
-// them as one vector per partition.  A CTA has 8 warps = 8 / WPH heads.
-template <int HEAD_DIM, int WPH>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
-  constexpr int VEC = HEAD_DIM / 32;
-  constexpr int HPC = 8 / WPH;
-  using VecT = typename std::conditional<VEC == 4, float4, float2>::type;
-  __shared__ float sm_m[8], sm_l[8];
-  __shared__ VecT sm_o[8][32];
-  grid_dependency_wait();  // the partitions come from the decode kernel just before
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int h = blockIdx.x * HPC + warp / WPH;
-  const int sub = warp % WPH;
-  const int s = blockIdx.y;
-  const int ctx = __ldg(p.context_lens + s);
-  const int nparts = (ctx <= 0 || ctx > p.cap) ? 0 : (ctx + p.partition_size - 1) / p.partition_size;
-  const bool active = h < p.num_heads && nparts > 1;  // one partition: finished by the decode kernel
-  const size_t row0 = (static_cast<size_t>(s) * p.num_heads + (active ? h : 0)) * p.max_num_partitions;
-  const int cnt = active ? (nparts - sub + WPH - 1) / WPH : 0;  // this warp's partitions
-
-  // maximum over this warp's partitions
-  float Mw = -INFINITY;
-  for (int i = lane; i < cnt; i += 32) Mw = fmaxf(Mw, __ldg(p.ws_m + row0 + sub + i * WPH));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
-
-  // weights w_q = l_q 2^(m_q - Mw), broadcast 32 at a time; weighted sum of o_q
-  float Lw = 0.f;
-  float acc[VEC];
-#pragma unroll
-  for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-  for (int base = 0; base < cnt; base += 32) {
-    const int i = base + lane;
-    float w = 0.f;
-    if (i < cnt) {
-      const size_t r = row0 + sub + static_cast<size_t>(i) * WPH;
-      w = __ldg(p.ws_l + r) * ex2(__ldg(p.ws_m + r) - Mw);
-    }
-    Lw += w;
-    const int n = min(32, cnt - base);
-#pragma unroll 8
-    for (int j = 0; j < n; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
-      const size_t r = row0 + sub + static_cast<size_t>(base + j) * WPH;
-      const VecT o = __ldg(reinterpret_cast<const VecT*>(p.ws_o + r * HEAD_DIM) + lane);
-      acc[0] += wj * o.x;
-      acc[1] += wj * o.y;
-      if constexpr (VEC == 4) {
-        acc[2] += wj * o.z;
-        acc[3] += wj * o.w;
-      }
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) Lw += __shfl_xor_sync(0xffffffffu, Lw, off);
-
-  if constexpr (WPH > 1) {
-    // combine the WPH warps of each head
-    if (lane == 0) {
-      sm_m[warp] = Mw;
-      sm_l[warp] = Lw;
-    }
-    VecT o;
-    o.x = acc[0];
-    o.y = acc[1];
-    if constexpr (VEC == 4) {
-      o.z = acc[2];
-      o.w = acc[3];
-    }
-    sm_o[warp][lane] = o;
-    __syncthreads();
-    if (sub != 0 || !active) return;
-    const int w0 = warp;
-    float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < WPH; ++k) M = fmaxf(M, sm_m[w0 + k]);
-    float L = 0.f;
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-#pragma unroll
-    for (int k = 0; k < WPH; ++k) {
-      const float f = ex2(sm_m[w0 + k] - M);  // a warp without partitions: 2^-inf = 0
-      L += sm_l[w0 + k] * f;
-      const VecT ok = sm_o[w0 + k][lane];
-      acc[0] += f * ok.x;
-      acc[1] += f * ok.y;
-      if constexpr (VEC == 4) {
-        acc[2] += f * ok.z;
-        acc[3] += f * ok.w;
-      }
-    }
-    Lw = L;
-  } else {
-    if (!active) return;
-  }
-  __half* dst = p.out + (static_cast<size_t>(s) * p.num_heads + h) * HEAD_DIM + lane * VEC;
-  const float inv = 1.f / Lw;
-  if constexpr (VEC == 4) {
-    __half2 a = __floats2half2_rn(acc[0] * inv, acc[1] * inv);
-    __half2 b = __floats2half2_rn(acc[2] * inv, acc[3] * inv);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(dst) = u;
-  } else {
-    *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(acc[0] * inv, acc[1] * inv);
-  }
-}
-
-// ================================================================ launchers
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled, resolved through the runtime once (the library does
-// not link the driver library directly).
-cudaError_t encode_fn(EncodeTiledFn* out) {
-  static std::atomic<EncodeTiledFn> cached{nullptr};
-  EncodeTiledFn f = cached.load(std::memory_order_acquire);
-  if (f == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess) return e;
-    if (q != cudaDriverEntryPointSuccess || ptr == nullptr) return cudaErrorNotSupported;
-    f = reinterpret_cast<EncodeTiledFn>(ptr);
-    cached.store(f, std::memory_order_release);
-  }
-  *out = f;
-  return cudaSuccess;
-}
-
-// A KV pool [N][B][Hk][d] seen as rows x heads x dims, boxes of 16 rows x 1
-// head x 64 dims, 128-byte swizzled.
-cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int head_dim, int num_kv_heads,
-                          int64_t rows) {
-  EncodeTiledFn enc = nullptr;
-  cudaError_t e = encode_fn(&enc);
-  if (e != cudaSuccess) return e;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
-                              static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
-                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
-  const cuuint32_t box[3] = {BOX_DIMS, 1, CHUNK};
-  const cuuint32_t estride[3] = {1, 1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(pool), dims, strides, box,
-                         estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-template <typename Kernel>
-cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
-  if (bit && (done_mask.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && bit) done_mask.fetch_or(bit, std::memory_order_acq_rel);
-  return e;
-}
-
-#ifndef PA_DECODE_WARPS
-#define PA_DECODE_WARPS 4
-#endif
-#ifndef PA_DECODE_STAGES
-#define PA_DECODE_STAGES 2
-#endif
-
-template <int HEAD_DIM>
-cudaError_t fill_decode_params(const DecodeArgs& a, DecodeParams* pp) {
-  DecodeParams& p = *pp;
-  const int64_t pool_rows = static_cast<int64_t>(a.num_blocks) * a.block_size;
-  cudaError_t e = make_pool_map(&p.tmap_k, a.k_cache, HEAD_DIM, a.num_kv_heads, pool_rows);
-  if (e != cudaSuccess) return e;
-  e = make_pool_map(&p.tmap_v, a.v_cache, HEAD_DIM, a.num_kv_heads, pool_rows);
-  if (e != cudaSuccess) return e;
-  p.out = static_cast<__half*>(a.out);
-  p.q = static_cast<const __half*>(a.q);
-  p.block_tables = a.block_tables;
-  p.context_lens = a.context_lens;
-  const size_t rows = ws_rows(a.num_seqs, a.num_heads, a.max_num_partitions);
-  p.ws_o = a.ws;
-  p.ws_m = a.ws ? a.ws + rows * HEAD_DIM : nullptr;
-  p.ws_l = a.ws ? a.ws + rows * HEAD_DIM + rows : nullptr;
-  p.max_blocks_per_seq = a.max_blocks_per_seq;
-  p.num_heads = a.num_heads;
-  p.num_kv_heads = a.num_kv_heads;
-  p.group = a.num_heads / a.num_kv_heads;
-  p.block_size = a.block_size;
-  p.chunks_per_block_log2 = __builtin_ctz(static_cast<unsigned>(a.block_size / CHUNK));
-  p.num_blocks = a.num_blocks;
-  p.partition_chunks = a.partition_size / CHUNK;
-  p.max_num_partitions = a.max_num_partitions;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
-  return cudaSuccess;
-}
-
-template <int HEAD_DIM, int NT, bool CLUSTER>
-cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
-  constexpr int WARPS = PA_DECODE_WARPS;
-  constexpr int STAGES = PA_DECODE_STAGES;
-  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
-  auto kern = paged_decode_kernel<HEAD_DIM, NT, WARPS, STAGES, CLUSTER>;
-  static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
-  if (e != cudaSuccess) return e;
-
-  DecodeParams p;
-  e = fill_decode_params<HEAD_DIM>(a, &p);
-  if (e != cudaSuccess) return e;
-  dim3 grid(a.num_kv_heads, CLUSTER ? a.cluster_size : a.max_num_partitions, a.num_seqs);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(WARPS * 32);
-  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if constexpr (CLUSTER) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = a.cluster_size;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
-  }
-  e = cudaLaunchKernelEx(&cfg, kern, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-// Resident decode CTAs the device holds at once (SMs x CTAs per SM), cached
-// per device.
-template <int HEAD_DIM, int NT>
-cudaError_t decode_slots(int* slots) {
-  constexpr int WARPS = PA_DECODE_WARPS;
-  constexpr int STAGES = PA_DECODE_STAGES;
-  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
-  static std::atomic<int> cache[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 64) {
-    const int c = cache[dev].load(std::memory_order_acquire);
-    if (c > 0) {
-      *slots = c;
-      return cudaSuccess;
-    }
-  }
-  auto kern = paged_decode_kernel<HEAD_DIM, NT, WARPS, STAGES, false>;
-  static std::atomic<uint64_t> smem_set{0};
-  e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
-  if (e != cudaSuccess) return e;
-  int sms = 0, per_sm = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, WARPS * 32, Cfg::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  const int v = sms * (per_sm > 0 ? per_sm : 1);
-  if (dev < 64) cache[dev].store(v, std::memory_order_release);
-  *slots = v;
-  return cudaSuccess;
-}
-
-// Cluster size for single-launch decode: one CTA per (sequence, KV head) when
-// those fill the resident slots; otherwise up to 8 CTAs per pair, each with
-// at least 512 tokens of capacity.
-template <int HEAD_DIM, int NT>
-cudaError_t auto_cluster_size(const DecodeArgs& a, int* c) {
-  int slots = 0;
-  cudaError_t e = decode_slots<HEAD_DIM, NT>(&slots);
-  if (e != cudaSuccess) return e;
-  const int64_t pairs = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-  int64_t k = pairs > 0 ? slots / pairs : 1;
-  const int64_t cap = static_cast<int64_t>(a.max_blocks_per_seq) * a.block_size;
-  k = std::min<int64_t>(k, (cap + 511) / 512);
-  *c = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(8, k)));
-  return cudaSuccess;
-}
-
-template <int HEAD_DIM, int NT>
-cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.cluster_size >= 0) {
-    return a.cluster_size > 0 ? launch_decode_t<HEAD_DIM, NT, true>(a, stream)
-                              : launch_decode_t<HEAD_DIM, NT, false>(a, stream);
-  }
-  DecodeArgs b = a;
-  cudaError_t e = auto_cluster_size<HEAD_DIM, NT>(a, &b.cluster_size);
-  if (e != cudaSuccess) return e;
-  if (b.cluster_size == 1) {  // a plain single pass: one CTA per (sequence, KV head)
-    b.cluster_size = 0;
-    return launch_decode_t<HEAD_DIM, NT, false>(b, stream);
-  }
-  return launch_decode_t<HEAD_DIM, NT, true>(b, stream);
-}
-
-template <int HEAD_DIM>
-cudaError_t launch_reduce_t(const ReduceArgs& a, cudaStream_t stream) {
-  ReduceParams p;
-  const size_t rows = ws_rows(a.num_seqs, a.num_heads, a.max_num_partitions);
-  p.out = static_cast<__half*>(a.out);
-  p.ws_o = a.ws;
-  p.ws_m = a.ws + rows * HEAD_DIM;
-  p.ws_l = a.ws + rows * HEAD_DIM + rows;
-  p.context_lens = a.context_lens;
-  p.cap = a.max_blocks_per_seq * a.block_size;
-  p.num_heads = a.num_heads;
-  p.partition_size = a.partition_size;
-  p.max_num_partitions = a.max_num_partitions;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e;
-  if (a.max_num_partitions <= 8) {  // one warp per (sequence, head), one memory round trip
-    cfg.gridDim = dim3((a.num_heads + 7) / 8, a.num_seqs);
-    e = cudaLaunchKernelEx(&cfg, splitk_reduce_small_kernel<HEAD_DIM, 8>, p);
-  } else if (a.max_num_partitions <= 32) {  // one warp per (sequence, head)
-    cfg.gridDim = dim3((a.num_heads + 7) / 8, a.num_seqs);
-    e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<HEAD_DIM, 1>, p);
-  } else {  // four warps per (sequence, head)
-    cfg.gridDim = dim3((a.num_heads + 1) / 2, a.num_seqs);
-    e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<HEAD_DIM, 4>, p);
-  }
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -1013,23 +78,11 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) 
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.num_seqs == 0) return cudaSuccess;
-  const int G = a.num_heads / a.num_kv_heads;
-  const bool two = G > 8;
-  switch (a.head_dim) {
-    case 64: return two ? launch_decode_auto<64, 2>(a, stream) : launch_decode_auto<64, 1>(a, stream);
-    case 128: return two ? launch_decode_auto<128, 2>(a, stream) : launch_decode_auto<128, 1>(a, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return a.dtype == PA_BF16 ? launch_decode_bf16(a, stream) : launch_decode_f16(a, stream);
 }
 
 cudaError_t launch_splitk_reduce(const ReduceArgs& a, cudaStream_t stream) {
-  if (a.num_seqs == 0) return cudaSuccess;
-  switch (a.head_dim) {
-    case 64: return launch_reduce_t<64>(a, stream);
-    case 128: return launch_reduce_t<128>(a, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return a.dtype == PA_BF16 ? launch_splitk_reduce_bf16(a, stream) : launch_splitk_reduce_f16(a, stream);
 }
 
 }  // namespace pa

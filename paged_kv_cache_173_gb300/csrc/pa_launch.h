@@ -22,6 +22,7 @@ struct ReshapeArgs {
 };
 
 struct DecodeArgs {
+  int dtype;  // PA_FP16 or PA_BF16
   void* out;
   const void* q;
   const void* k_cache;
@@ -44,6 +45,7 @@ struct DecodeArgs {
 };
 
 struct ReduceArgs {
+  int dtype;  // PA_FP16 or PA_BF16
   void* out;
   const float* ws;
   const int32_t* context_lens;
@@ -62,6 +64,12 @@ int set_last_error(int status, const char* fmt, ...);
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceArgs& a, cudaStream_t stream);
+
+// per element type (pa_decode_f16.cu, pa_decode_bf16.cu)
+cudaError_t launch_decode_f16(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_splitk_reduce_f16(const ReduceArgs& a, cudaStream_t stream);
+cudaError_t launch_splitk_reduce_bf16(const ReduceArgs& a, cudaStream_t stream);
 
 // Workspace geometry shared by the partition kernel and the reduce kernel:
 // o [S][H][P][d], then m [S][H][P], then l [S][H][P], float32.

@@ -4,8 +4,11 @@
 // completion, ldmatrix / movmatrix fragment moves and the m16n8k16 f16 MMA.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 namespace pa {
 
@@ -138,6 +141,26 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The m16n8k16 MMA for element type T (__half or __nv_bfloat16); A and B
+// always share the type.
+template <typename T>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (std::is_same<T, __half>::value) {
+    mma_f16_16816(d, a, b0, b1);
+  } else {
+    mma_bf16_16816(d, a, b0, b1);
+  }
+}
+
 // ------------------------------------------------ programmatic dependent launch --
 // Block until the grids this one depends on have completed and their memory
 // is visible (returns at once when the launch had no such dependency).
@@ -164,6 +187,44 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 
 __device__ __forceinline__ float2 unpack_half2(uint32_t v) {
   return __half22float2(*reinterpret_cast<__half2*>(&v));
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack_bf162(uint32_t v) {
+  return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v));
+}
+
+// Two floats rounded (nearest even) to a packed pair of T.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (std::is_same<T, __half>::value) {
+    return pack_half2(lo, hi);
+  } else {
+    return pack_bf162(lo, hi);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+  if constexpr (std::is_same<T, __half>::value) {
+    return unpack_half2(v);
+  } else {
+    return unpack_bf162(v);
+  }
+}
+
+// One float rounded (nearest even) to T.
+template <typename T>
+__device__ __forceinline__ T to_elem(float x) {
+  if constexpr (std::is_same<T, __half>::value) {
+    return __float2half_rn(x);
+  } else {
+    return __float2bfloat16_rn(x);
+  }
 }
 
 }  // namespace pa

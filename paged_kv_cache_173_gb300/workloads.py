@@ -10,7 +10,9 @@ Recipe (every batch):
 * ``rng = numpy.random.default_rng(seed)`` (PCG64); draws happen in a fixed
   order: context lengths, the physical-id permutation, ``q``, the K pool, the
   V pool, the new tokens' K and V.
-* values are standard normal drawn as float32 and rounded to float16 (RNE).
+* values are standard normal drawn as float32 and rounded (to nearest even)
+  to float16, or to bfloat16 with ``dtype="bf16"``; bfloat16 arrays are kept
+  as uint16 bit patterns, since numpy has no bfloat16 type.
 * the KV pools have the layout ``[num_blocks, block_size, num_kv_heads,
   head_dim]``, one pool for K and one for V.
 * a sequence of ``ctx`` tokens owns ``ceil(ctx / block_size)`` blocks.  The
@@ -39,6 +41,15 @@ from typing import List, Optional, Sequence
 import numpy as np
 
 FP16_NAN_BITS = np.uint16(0x7E00)
+BF16_NAN_BITS = np.uint16(0x7FC0)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round finite float32 values to the nearest bfloat16 (ties to even) and
+    return the 16-bit patterns: the upper half of the float32 after adding
+    0x7FFF plus the lowest kept bit."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
 
 
 @dataclasses.dataclass
@@ -64,6 +75,7 @@ class PagedBatch:
     slot_mapping: np.ndarray  # [T] int64, flat slot id, -1 = skip
     partition_size: int  # split-K partition length (tokens) for this workload
     unique_blocks: int  # distinct physical blocks referenced by the tables
+    dtype: str = "fp16"  # "fp16": float16 arrays; "bf16": uint16 bfloat16 bit patterns
 
     @property
     def group_size(self) -> int:
@@ -74,14 +86,16 @@ class PagedBatch:
         return int(self.key.shape[0])
 
 
-def _normal_f16(rng: np.random.Generator, shape, chunk_elems: int = 1 << 26) -> np.ndarray:
-    """Standard normal float32 draws rounded to float16, drawn in chunks."""
-    out = np.empty(int(np.prod(shape)), dtype=np.float16)
+def _normal_f16(rng: np.random.Generator, shape, chunk_elems: int = 1 << 26, dtype: str = "fp16") -> np.ndarray:
+    """Standard normal float32 draws rounded to float16 (or bfloat16 bit
+    patterns), drawn in chunks."""
+    out = np.empty(int(np.prod(shape)), dtype=np.float16 if dtype == "fp16" else np.uint16)
     pos = 0
     total = out.size
     while pos < total:
         n = min(chunk_elems, total - pos)
-        out[pos:pos + n] = rng.standard_normal(n, dtype=np.float32).astype(np.float16)
+        x = rng.standard_normal(n, dtype=np.float32)
+        out[pos:pos + n] = x.astype(np.float16) if dtype == "fp16" else f32_to_bf16_bits(x)
         pos += n
     return out.reshape(shape)
 
@@ -105,6 +119,7 @@ def build_batch(
     partition_size: int = 512,
     rng: Optional[np.random.Generator] = None,
     q_scale: float = 1.0,
+    dtype: str = "fp16",
 ) -> PagedBatch:
     """Build one batch.
 
@@ -163,15 +178,17 @@ def build_batch(
             nxt += nblk[s]
     unique_blocks = nxt
 
-    q = _normal_f16(rng, (S, H, d))
+    assert dtype in ("fp16", "bf16")
+    assert q_scale == 1.0 or dtype == "fp16"
+    q = _normal_f16(rng, (S, H, d), dtype=dtype)
     if q_scale != 1.0:
         q = (q.astype(np.float32) * np.float32(q_scale)).astype(np.float16)
-    k_cache = _normal_f16(rng, (N, B, Hk, d))
-    v_cache = _normal_f16(rng, (N, B, Hk, d))
+    k_cache = _normal_f16(rng, (N, B, Hk, d), dtype=dtype)
+    v_cache = _normal_f16(rng, (N, B, Hk, d), dtype=dtype)
 
     T = S if new_token else 0
-    key = _normal_f16(rng, (T, Hk, d))
-    value = _normal_f16(rng, (T, Hk, d))
+    key = _normal_f16(rng, (T, Hk, d), dtype=dtype)
+    value = _normal_f16(rng, (T, Hk, d), dtype=dtype)
     slot_mapping = np.full((T,), -1, dtype=np.int64)
     if new_token:
         for s in range(S):
@@ -191,15 +208,16 @@ def build_batch(
                 valid[sl // B, sl % B] = False
         kb = k_cache.view(np.uint16)
         vb = v_cache.view(np.uint16)
-        kb[~valid] = FP16_NAN_BITS
-        vb[~valid] = FP16_NAN_BITS
+        nan = FP16_NAN_BITS if dtype == "fp16" else BF16_NAN_BITS
+        kb[~valid] = nan
+        vb[~valid] = nan
 
     return PagedBatch(
         name=name, num_seqs=S, num_heads=H, num_kv_heads=Hk, head_dim=d, block_size=B,
         num_blocks=N, max_blocks_per_seq=M, scale=float(np.float32(1.0 / math.sqrt(d))),
         q=q, k_cache=k_cache, v_cache=v_cache, block_tables=tables,
         context_lens=ctx.astype(np.int32), key=key, value=value, slot_mapping=slot_mapping,
-        partition_size=int(partition_size), unique_blocks=int(unique_blocks),
+        partition_size=int(partition_size), unique_blocks=int(unique_blocks), dtype=dtype,
     )
 
 
@@ -219,7 +237,8 @@ def tiny(seed: int = 0, poison: bool = True) -> PagedBatch:
 
 
 def llama3_8b(seed: int = 0, num_seqs: int = 64, poison: bool = True,
-              min_ctx: int = 128, max_ctx: int = 2048, partition_size: int = 512) -> PagedBatch:
+              min_ctx: int = 128, max_ctx: int = 2048, partition_size: int = 512,
+              dtype: str = "fp16") -> PagedBatch:
     """Llama-3-8B-shaped decode layer: 32 q heads, 8 KV heads (GQA 4), d = 128,
     B = 16; contexts uniform in [min_ctx, max_ctx]; 1.25x pool, shuffled ids."""
     rng = np.random.default_rng(seed)
@@ -227,30 +246,31 @@ def llama3_8b(seed: int = 0, num_seqs: int = 64, poison: bool = True,
     return build_batch(name="llama3-8b", seed=seed, rng=rng, context_lens=ctx, num_heads=32,
                        num_kv_heads=8, head_dim=128, block_size=16,
                        max_blocks_per_seq=(max_ctx + 15) // 16, poison=poison,
-                       partition_size=partition_size)
+                       partition_size=partition_size, dtype=dtype)
 
 
 def llama2_70b(seed: int = 0, block_size: int = 16, num_seqs: int = 32, ctx: int = 8192,
-               poison: bool = True, partition_size: int = 512) -> PagedBatch:
+               poison: bool = True, partition_size: int = 512, dtype: str = "fp16") -> PagedBatch:
     """Llama-2-70B-shaped GQA decode: 64 q heads, 8 KV heads (GQA 8), d = 128;
     every context ``ctx`` tokens; one new token per sequence at position
     ctx - 1; 1.25x pool, shuffled ids."""
     return build_batch(name=f"llama2-70b-b{block_size}", seed=seed, context_lens=[ctx] * num_seqs,
                        num_heads=64, num_kv_heads=8, head_dim=128, block_size=block_size,
-                       poison=poison, partition_size=partition_size)
+                       poison=poison, partition_size=partition_size, dtype=dtype)
 
 
 def long_context(seed: int = 0, ctxs: Sequence[int] = (32768, 65536, 98304, 131072),
-                 poison: bool = True, partition_size: int = 512) -> PagedBatch:
+                 poison: bool = True, partition_size: int = 512, dtype: str = "fp16") -> PagedBatch:
     """Long-context split-K decode: 32 q heads, 8 KV heads, d = 128, B = 16;
     4 sequences of 32K..128K tokens; 512-token partitions."""
     return build_batch(name="long-context", seed=seed, context_lens=list(ctxs), num_heads=32,
                        num_kv_heads=8, head_dim=128, block_size=16, poison=poison,
-                       partition_size=partition_size)
+                       partition_size=partition_size, dtype=dtype)
 
 
 def shared_prefix(seed: int = 0, num_prompts: int = 16, samples: int = 8, prompt_len: int = 1024,
-                  max_suffix: int = 512, poison: bool = True, partition_size: int = 512) -> PagedBatch:
+                  max_suffix: int = 512, poison: bool = True, partition_size: int = 512,
+                  dtype: str = "fp16") -> PagedBatch:
     """Parallel sampling: ``num_prompts`` prompts of ``prompt_len`` tokens, each
     sampled ``samples`` times.  The samples' tables point at the same prompt
     blocks (reference count ``samples``) and then diverge with suffixes
@@ -265,7 +285,7 @@ def shared_prefix(seed: int = 0, num_prompts: int = 16, samples: int = 8, prompt
     return build_batch(name="shared-prefix", seed=seed, rng=rng, context_lens=ctx, num_heads=40,
                        num_kv_heads=40, head_dim=128, block_size=16, max_blocks_per_seq=M,
                        share_groups=groups, shared_prefix_len=prompt_len, poison=poison,
-                       partition_size=partition_size)
+                       partition_size=partition_size, dtype=dtype)
 
 
 WORKLOADS = {

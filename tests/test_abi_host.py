@@ -67,7 +67,8 @@ def _decode(L, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(d=96), _lib.PA_ERR_UNSUPPORTED),
-    (dict(dtype=1), _lib.PA_ERR_UNSUPPORTED),
+    (dict(dtype=2), _lib.PA_ERR_UNSUPPORTED),
+    (dict(d=256, H=32, Hk=2), _lib.PA_ERR_UNSUPPORTED),  # head_dim 256: query groups up to 8
     (dict(H=6, Hk=4), _lib.PA_ERR_UNSUPPORTED),
     (dict(H=64, Hk=2), _lib.PA_ERR_UNSUPPORTED),
     (dict(B=8), _lib.PA_ERR_UNSUPPORTED),

@@ -434,3 +434,48 @@ def test_pins_catch_planted_mistakes(monkeypatch, mutant):
             return out[:, perm]
     assert orig_locate(37, [7, 42, 9, 103], 16) == (9, 5)
     assert _run_pins(decode) != []
+
+
+# --------------------------------------------------------------------------
+# bfloat16 inputs
+# --------------------------------------------------------------------------
+
+def _bf16_to_f64(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).view(
+        torch.bfloat16).double().numpy()
+
+
+def test_bf16_decoding_matches_torch_for_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = _bf16_to_f64(bits)
+    got = np.array([c_oracle.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_generator_bf16_rounding_matches_torch():
+    x = np.random.default_rng(0).standard_normal(200_000, dtype=np.float32) * np.float32(3.0)
+    x[:4] = [1.00390625, 1.01171875, -2.0078125, 0.0]  # exact ties round to even
+    ours = workloads.f32_to_bf16_bits(x)
+    theirs = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, theirs)
+
+
+def test_bf16_batch_equals_library_attention():
+    b = workloads.build_batch(name="bf16", seed=21, context_lens=[1, 17, 40], num_heads=8, num_kv_heads=2,
+                              head_dim=64, block_size=16, dtype="bf16")
+    kc, vc = c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
+    got = c_oracle.decode(b.q, kc, vc, b.block_tables, b.context_lens, b.scale, dtype="bf16")
+    assert np.isfinite(got).all()
+    kf, vf, qf = _bf16_to_f64(kc), _bf16_to_f64(vc), _bf16_to_f64(b.q)
+    for s in range(b.num_seqs):
+        c = int(b.context_lens[s])
+        ks = np.stack([kf[b.block_tables[s, t // 16], t % 16] for t in range(c)])
+        vs = np.stack([vf[b.block_tables[s, t // 16], t % 16] for t in range(c)])
+        ref = _sdpa_contiguous(qf[s], ks, vs, b.scale, b.group_size)
+        np.testing.assert_allclose(got[s], ref, rtol=0, atol=1e-12)
+    # ctx = 1: the output is that token's V, exactly
+    blk = b.block_tables[0, 0]
+    for h in range(b.num_heads):
+        assert np.array_equal(got[0, h], vf[blk, 0, h // b.group_size])

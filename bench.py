@@ -47,25 +47,43 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.md")
 
 
 # ----------------------------------------------------------------- workload
-def make_workload(name: str, seed: int, partition_size: int):
+def make_workload(name: str, seed: int, partition_size: int, dtype: str = "fp16"):
     from paged_kv_cache_173_gb300 import workloads
+    kw = dict(seed=seed, poison=False, partition_size=partition_size, dtype=dtype)
     if name == "llama3-8b":
-        b = workloads.llama3_8b(seed=seed, poison=False, partition_size=partition_size)
+        b = workloads.llama3_8b(**kw)
         desc = ("llama3-8b decode layer: S=64, H=32, Hk=8, d=128, B=16, ctx~U[128,2048], "
                 "1.25x pool, shuffled ids, 1 new token/seq")
     elif name in ("llama2-70b-b16", "llama2-70b-b32"):
         bs = int(name[-2:])
-        b = workloads.llama2_70b(seed=seed, block_size=bs, poison=False, partition_size=partition_size)
+        b = workloads.llama2_70b(block_size=bs, **kw)
         desc = f"llama2-70b GQA decode: S=32, H=64, Hk=8, d=128, B={bs}, ctx=8192, 1.25x pool, shuffled"
     elif name == "long-context":
-        b = workloads.long_context(seed=seed, poison=False, partition_size=partition_size)
+        b = workloads.long_context(**kw)
         desc = "long-context decode: S=4, ctx {32K,64K,96K,128K}, H=32, Hk=8, d=128, B=16"
     elif name == "shared-prefix":
-        b = workloads.shared_prefix(seed=seed, poison=False, partition_size=partition_size)
+        b = workloads.shared_prefix(**kw)
         desc = "shared-prefix sampling: 16 prompts x 8 samples, prompt 1024, suffix U[0,512], MHA 40, d=128"
+    elif name == "head-dim-256":
+        rng = np.random.default_rng(seed)
+        b = workloads.build_batch(name=name, rng=rng, context_lens=rng.integers(128, 4097, size=32),
+                                  num_heads=16, num_kv_heads=4, head_dim=256, block_size=16,
+                                  max_blocks_per_seq=256, **kw)
+        desc = "head_dim 256 GQA decode: S=32, H=16, Hk=4, d=256, B=16, ctx~U[128,4096], 1.25x pool"
     else:
         raise SystemExit(f"unknown workload {name}")
+    if dtype != "fp16":
+        desc += f", {dtype}"
     return b, desc
+
+
+def to_device(a: np.ndarray, dtype: str, dev):
+    """A workload array on the device; bfloat16 bit patterns become bf16 tensors."""
+    import torch
+    a = np.ascontiguousarray(a)
+    if dtype == "bf16" and a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(a).to(dev)
 
 
 def load_peak():
@@ -283,12 +301,12 @@ def run_gpu(args, rank: int, world: int):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    b, desc = make_workload(args.workload, args.seed + rank, args.partition_size)
+    b, desc = make_workload(args.workload, args.seed + rank, args.partition_size, args.dtype)
     kv_bytes = workloads.algorithmic_kv_bytes(b)
     ps = b.partition_size
     P = api.max_num_partitions_for(b.max_blocks_per_seq, b.block_size, ps)
 
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    t = lambda a: to_device(a, b.dtype, dev)  # noqa: E731
     pool_bytes = 2 * b.k_cache.nbytes
     l2_bytes = 129 * 2 ** 20
     R = max(2, min(8, math.ceil(4 * l2_bytes / max(1, kv_bytes)) + 1))
@@ -359,7 +377,7 @@ def run_gpu(args, rank: int, world: int):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16",
+        "dtype": "bf16" if b.dtype == "bf16" else "f16",
         "data": "synthetic",
         "config": {
             "workload": desc,
@@ -404,7 +422,7 @@ def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, path):
     import torch
     from paged_kv_cache_173_gb300 import api
 
-    host = {k: torch.from_numpy(np.ascontiguousarray(getattr(b, k))).pin_memory()
+    host = {k: to_device(getattr(b, k), b.dtype, "cpu").pin_memory()
             for k in ("q", "key", "value", "slot_mapping", "block_tables", "context_lens")}
     devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
     out = torch.empty_like(devb["q"])
@@ -468,7 +486,7 @@ def oracle_step_runner(b):
     def run(n, off):
         idx = (np.arange(n) + off) % S
         c_oracle.reshape_and_cache(b.key[idx], b.value[idx], kc, vc, b.slot_mapping[idx], inplace=True)
-        c_oracle.decode(b.q[idx], kc, vc, b.block_tables[idx], b.context_lens[idx], b.scale)
+        c_oracle.decode(b.q[idx], kc, vc, b.block_tables[idx], b.context_lens[idx], b.scale, dtype=b.dtype)
         return int(np.sum(b.context_lens[idx].astype(np.int64))) * per_tok
 
     return run, cores
@@ -494,7 +512,7 @@ def cpu_baseline(b, kv_bytes, budget_s: float):
 def run_reference(args, rank: int):
     if rank != 0:
         return None
-    b, desc = make_workload(args.workload, args.seed, args.partition_size)
+    b, desc = make_workload(args.workload, args.seed, args.partition_size, args.dtype)
     run, cores = oracle_step_runner(b)
     t0 = time.perf_counter()
     run(1, 0)
@@ -534,6 +552,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="llama3-8b")
     p.add_argument("--partition-size", type=int, default=512)
+    p.add_argument("--dtype", choices=["fp16", "bf16"], default="fp16")
     p.add_argument("--path", choices=["auto", "decode", "splitk"], default="auto",
                    help="decode: reshape + pa_decode; splitk: reshape + pa_decode_splitk + reduce; "
                         "auto: time both, report the faster")

@@ -462,6 +462,47 @@ def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, path):
             "ms_per_step": round(ms / n, 5)}
 
 
+# ------------------------------------------------------------ copy_blocks
+def run_copy_blocks(args):
+    """Time pa_copy_blocks: K steps, each copying `--copy-pairs` whole blocks of
+    the workload's pool (src and dst drawn from distinct halves of the pool,
+    rotating over sets larger than L2).  Bytes = read + write of K and V."""
+    import torch
+    from paged_kv_cache_173_gb300 import api
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    b, desc = make_workload(args.workload, args.seed, args.partition_size, args.dtype)
+    kc = to_device(b.k_cache, b.dtype, dev)
+    vc = to_device(b.v_cache, b.dtype, dev)
+    N = b.num_blocks
+    half = N // 2
+    n = min(args.copy_pairs, half)
+    block_bytes = kc[0].numel() * kc.element_size()
+    rng = np.random.default_rng(args.seed)
+    sets = []
+    for _ in range(max(2, math.ceil(4 * 129 * 2 ** 20 / max(1, 4 * n * block_bytes)) + 1)):
+        src = rng.choice(half, size=n, replace=False)
+        dst = half + rng.choice(N - half, size=n, replace=False)
+        sets.append(torch.from_numpy(np.stack([src, dst], axis=1).astype(np.int64)).to(dev))
+    stream = torch.cuda.Stream(dev)
+    kernels = [("copy_blocks", lambda r: api.pa_copy_blocks(kc, vc, sets[r % len(sets)]))]
+    clocks = ClockSampler(dev.index)
+    ms, per, walls, mode, G = time_path(torch, dev, stream, kernels, len(sets), args.steps, args.warmup, clocks)
+    moved = 2 * 2 * n * block_bytes  # K and V, read and written
+    peak, kind = load_peak()
+    value = moved * args.steps / (ms * 1e-3) / 1e9
+    return {"metric": "pa_copy_blocks GB/s (bytes read + written)", "value": round(value, 1), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
+            "higher_is_better": True, "dtype": "bf16" if b.dtype == "bf16" else "f16", "data": "synthetic",
+            "config": {"workload": desc, "pairs_per_step": n, "block_bytes": block_bytes,
+                       "kernel_timing": mode},
+            "roofline": {"kernel": "copy_blocks", "bound": "hbm", "achieved": round(value, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,
+                         "peak_kind": f"{kind} (copy GB/s)"},
+            "gpu_launches": args.steps, "clocks": clocks.summary(*walls)}
+
+
 # ------------------------------------------------------------ CPU oracle
 def _cpu_model() -> str:
     try:
@@ -553,6 +594,9 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="llama3-8b")
     p.add_argument("--partition-size", type=int, default=512)
     p.add_argument("--dtype", choices=["fp16", "bf16"], default="fp16")
+    p.add_argument("--op", choices=["step", "copy-blocks"], default="step",
+                   help="step: the decode step (the headline); copy-blocks: time pa_copy_blocks")
+    p.add_argument("--copy-pairs", type=int, default=1024)
     p.add_argument("--path", choices=["auto", "decode", "splitk"], default="auto",
                    help="decode: reshape + pa_decode; splitk: reshape + pa_decode_splitk + reduce; "
                         "auto: time both, report the faster")
@@ -582,6 +626,9 @@ def main(argv=None):
         dist.init_process_group("nccl")
     import __graft_entry__
     __graft_entry__.build()
+    if args.op == "copy-blocks":
+        print(json.dumps(run_copy_blocks(args)), flush=True)
+        return 0
     res = run_gpu(args, rank, world)
     if rank == 0:
         print(json.dumps(res), flush=True)

@@ -92,6 +92,38 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
                          void* stream);
 
 /*
+ * pa_copy_blocks -- copy whole KV blocks, the copy step of copy-on-write.
+ *
+ * Sequences may share physical blocks (parallel sampling from one prompt:
+ * their block tables point at the same ids, with a reference count); before
+ * one of them writes into a shared block, its runtime copies the block to a
+ * free one and repoints that sequence's table entry.  ("Unveiling the NVIDIA
+ * driver stack: GPU page tables and vLLM PagedAttention", section 4:
+ * reference counts and copy-on-write protect writes to shared blocks;
+ * "PagedAttention: when the KV cache meets OS paging", section 4.3;
+ * "Efficient Memory Management for LLM Serving with PagedAttention --
+ * in-depth reading", section 2.4.)
+ *
+ * For every pair i < num_pairs with src = block_mapping[2i] and
+ * dst = block_mapping[2i + 1]:
+ *     k_cache[dst][:][:][:] = k_cache[src][:][:][:], likewise v_cache,
+ * a bit-exact copy of block_size * num_kv_heads * head_dim elements.
+ *
+ *   k_cache, v_cache  [num_blocks][block_size][num_kv_heads][head_dim]
+ *   block_mapping     [num_pairs][2] int64 (src, dst)
+ *   dtype             PA_FP16 or PA_BF16 (the copy moves bytes; only the
+ *                     element size matters)
+ *
+ * Device-value outcomes: a pair with an id outside [0, num_blocks), or with
+ * src == dst, is skipped.  Destinations must be distinct and no destination
+ * may be the source of another pair in the same call (otherwise the result
+ * depends on the order of the copies).
+ */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int num_pairs,
+                   int num_blocks, int block_size, int num_kv_heads, int head_dim, int dtype,
+                   void* stream);
+
+/*
  * pa_decode -- single-pass paged decode attention, one query token per
  * sequence.
  *

@@ -39,6 +39,8 @@ def lib() -> ctypes.CDLL:
         L.pa_oracle_decode.argtypes = [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I64,
                                        ctypes.c_double, _I, _I]
         L.pa_oracle_decode.restype = _I
+        L.pa_oracle_copy_blocks.argtypes = [_P, _P, _P, _I64, _I64, _I, _I, _I]
+        L.pa_oracle_copy_blocks.restype = _I
         L.pa_oracle_max_threads.argtypes = []
         L.pa_oracle_max_threads.restype = _I
         _lib = L
@@ -95,6 +97,18 @@ def reshape_and_cache(key: np.ndarray, value: np.ndarray, k_cache: np.ndarray, v
                                            int(sm.size), N, B, Hk, d)
     if rc:
         raise OracleError(f"reshape_and_cache precondition failed ({rc})")
+    return kc, vc
+
+
+def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, block_mapping) -> Tuple[np.ndarray, np.ndarray]:
+    """Return copies of the pools after copying the (src, dst) blocks."""
+    kc = np.ascontiguousarray(k_cache).copy()
+    vc = np.ascontiguousarray(v_cache).copy()
+    N, B, Hk, d = kc.shape
+    bm = np.ascontiguousarray(np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2))
+    rc = lib().pa_oracle_copy_blocks(_ptr(kc), _ptr(vc), _ptr(bm), int(bm.shape[0]), N, B, Hk, d)
+    if rc:
+        raise OracleError(f"copy_blocks precondition failed ({rc})")
     return kc, vc
 
 

@@ -65,3 +65,13 @@ def decode_bruteforce(q, k_cache, v_cache, block_tables, context_lens, scale) ->
                 acc += (w[t] / z) * v_cache[blk, off, kvh].astype(np.float64)
             out[s, h] = acc
     return out
+
+
+def copy_blocks(k_cache, v_cache, block_mapping):
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    for src, dst in np.asarray(block_mapping).reshape(-1, 2).tolist():
+        if 0 <= src < kc.shape[0] and 0 <= dst < kc.shape[0] and src != dst:
+            kc[dst] = kc[src]
+            vc[dst] = vc[src]
+    return kc, vc

@@ -151,6 +151,42 @@ int pa_oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint
     return ORACLE_OK;
 }
 
+/* Copy whole blocks, the copy step of copy-on-write ("Unveiling the NVIDIA
+ * driver stack", section 4; "in-depth reading", section 2.4): for each pair
+ * (src, dst) the dst block of both pools becomes a copy of the src block.
+ * Pairs with an id outside the pool or src == dst are skipped; destinations
+ * must be distinct and must not be the source of another pair. */
+int pa_oracle_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int64_t* block_mapping,
+                          int64_t num_pairs, int64_t num_blocks, int block_size, int num_kv_heads,
+                          int head_dim) {
+    if (num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return ORACLE_BAD_ARG;
+#define COPIES(k) (block_mapping[2 * (k)] >= 0 && block_mapping[2 * (k) + 1] >= 0 && \
+                   block_mapping[2 * (k)] < num_blocks && block_mapping[2 * (k) + 1] < num_blocks && \
+                   block_mapping[2 * (k)] != block_mapping[2 * (k) + 1])
+    /* precondition, over the pairs that copy (the others write nothing) */
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        if (!COPIES(i)) continue;
+        for (int64_t j = 0; j < num_pairs; ++j) {
+            if (i == j || !COPIES(j)) continue;
+            const int64_t dst_i = block_mapping[2 * i + 1];
+            if (dst_i == block_mapping[2 * j + 1] || dst_i == block_mapping[2 * j]) return ORACLE_BAD_ARG;
+        }
+    }
+    const int64_t elems = (int64_t)block_size * num_kv_heads * head_dim;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        const int64_t src = block_mapping[2 * i];
+        const int64_t dst = block_mapping[2 * i + 1];
+        if (!COPIES(i)) continue;
+        for (int64_t e = 0; e < elems; ++e) {
+            k_cache[dst * elems + e] = k_cache[src * elems + e];
+            v_cache[dst * elems + e] = v_cache[src * elems + e];
+        }
+    }
+#undef COPIES
+    return ORACLE_OK;
+}
+
 /* One (sequence, query head): gather, score, softmax, weighted sum. */
 static int decode_one(double* out, const uint16_t* q_row, const uint16_t* k_cache,
                       const uint16_t* v_cache, const int32_t* table, int max_blocks_per_seq,

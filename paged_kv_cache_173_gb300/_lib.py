@@ -27,6 +27,7 @@ _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 SIGNATURES = {
     "pa_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pa_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pa_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "pa_splitk_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "pa_decode_splitk": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I,

@@ -66,6 +66,24 @@ def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.
     _lib.check("pa_reshape_and_cache", st)
 
 
+def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: torch.Tensor,
+                   stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy whole blocks: for each row (src, dst) of block_mapping [n, 2] (int64),
+    k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src]."""
+    dev = _cuda_device(k_cache)
+    N, B, Hk, d = k_cache.shape
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must have the same shape")
+    if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be [n, 2]")
+    dt = k_cache.dtype
+    st = _lib.lib().pa_copy_blocks(
+        _need(k_cache, "k_cache", dt, dev), _need(v_cache, "v_cache", dt, dev),
+        _need(block_mapping, "block_mapping", torch.int64, dev), int(block_mapping.shape[0]), N, B, Hk, d,
+        _dtype_code(k_cache), _stream_ptr(k_cache, stream))
+    _lib.check("pa_copy_blocks", st)
+
+
 def _decode_common(out, q, k_cache, v_cache, block_tables, context_lens):
     dev = _cuda_device(q)
     S, H, d = q.shape

@@ -168,6 +168,26 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
                      "reshape_and_cache launch");
 }
 
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int num_pairs,
+                   int num_blocks, int block_size, int num_kv_heads, int head_dim, int dtype,
+                   void* stream) {
+  if (dtype != PA_FP16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 or PA_BF16)", dtype);
+  if (num_pairs < 0) return fail(PA_ERR_INVALID_ARG, "num_pairs %d is negative", num_pairs);
+  if (num_pairs > INT32_MAX / 2) return fail(PA_ERR_UNSUPPORTED, "num_pairs %d is too large", num_pairs);
+  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_blocks, block_size, num_kv_heads and head_dim must be positive");
+  const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * 2;
+  if (block_bytes % 16 != 0)
+    return fail(PA_ERR_UNSUPPORTED, "block bytes %lld are not a multiple of 16", (long long)block_bytes);
+  if (num_pairs == 0) return ok();
+  if (!k_cache || !v_cache || !block_mapping) return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_mapping, 8))
+    return fail(PA_ERR_INVALID_ARG, "the caches must be 16-byte aligned, block_mapping 8-byte aligned");
+  pa::CopyBlocksArgs a{k_cache, v_cache, block_mapping, num_pairs, num_blocks, block_bytes};
+  return cuda_status(pa::launch_copy_blocks(a, static_cast<cudaStream_t>(stream)), "copy_blocks launch");
+}
+
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,

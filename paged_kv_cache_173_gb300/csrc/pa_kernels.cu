@@ -47,7 +47,56 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_con
   for (int i = lane & 15; i < p.row_vecs; i += 16) dst[i] = __ldg(src + i);
 }
 
+// ================================================================ copy_blocks
+struct CopyBlocksParams {
+  uint4* k_cache;
+  uint4* v_cache;
+  const int64_t* block_mapping;
+  int num_blocks;
+  int64_t block_vecs;  // 16-byte vectors per block
+  int64_t slice_vecs;  // vectors per CTA slice of a block
+};
+
+// grid (pair, K or V, slice of the block): each CTA copies one slice of one
+// block with 16-byte loads and stores.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const __grid_constant__ CopyBlocksParams p) {
+  grid_dependency_wait();
+  const int64_t src = __ldg(p.block_mapping + 2 * static_cast<int64_t>(blockIdx.x));
+  const int64_t dst = __ldg(p.block_mapping + 2 * static_cast<int64_t>(blockIdx.x) + 1);
+  if (src < 0 || dst < 0 || src >= p.num_blocks || dst >= p.num_blocks || src == dst) return;
+  uint4* pool = blockIdx.y == 0 ? p.k_cache : p.v_cache;
+  const int64_t begin = static_cast<int64_t>(blockIdx.z) * p.slice_vecs;
+  const int64_t end = begin + p.slice_vecs < p.block_vecs ? begin + p.slice_vecs : p.block_vecs;
+  const uint4* from = pool + src * p.block_vecs;
+  uint4* to = pool + dst * p.block_vecs;
+  for (int64_t i = begin + threadIdx.x; i < end; i += blockDim.x) to[i] = __ldg(from + i);
+}
+
 }  // namespace
+
+cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream) {
+  if (a.num_pairs == 0) return cudaSuccess;
+  CopyBlocksParams p;
+  p.k_cache = static_cast<uint4*>(a.k_cache);
+  p.v_cache = static_cast<uint4*>(a.v_cache);
+  p.block_mapping = a.block_mapping;
+  p.num_blocks = a.num_blocks;
+  p.block_vecs = a.block_bytes / 16;
+  p.slice_vecs = 2048;  // 32 KB per CTA
+  const int64_t slices = (p.block_vecs + p.slice_vecs - 1) / p.slice_vecs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_pairs, 2, static_cast<unsigned>(slices));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, copy_blocks_kernel, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;

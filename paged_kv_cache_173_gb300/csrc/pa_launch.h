@@ -21,6 +21,15 @@ struct ReshapeArgs {
   int head_dim;
 };
 
+struct CopyBlocksArgs {
+  void* k_cache;
+  void* v_cache;
+  const int64_t* block_mapping;
+  int num_pairs;
+  int num_blocks;
+  int64_t block_bytes;  // block_size * num_kv_heads * head_dim * element size
+};
+
 struct DecodeArgs {
   int dtype;  // PA_FP16 or PA_BF16
   void* out;
@@ -62,6 +71,7 @@ struct ReduceArgs {
 int set_last_error(int status, const char* fmt, ...);
 
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceArgs& a, cudaStream_t stream);
 

@@ -479,3 +479,68 @@ def test_bf16_batch_equals_library_attention():
     blk = b.block_tables[0, 0]
     for h in range(b.num_heads):
         assert np.array_equal(got[0, h], vf[blk, 0, h // b.group_size])
+
+
+# --------------------------------------------------------------------------
+# copy-on-write block copy
+# --------------------------------------------------------------------------
+
+def _cow_fork(b, kc, vc, s_fork, free_block):
+    """Sequence s_fork shares its last, partial block with sequence 0; copy
+    that block to free_block and point s_fork's table there."""
+    B = b.block_size
+    last = (int(b.context_lens[s_fork]) - 1) // B
+    bt = b.block_tables.copy()
+    src = int(bt[s_fork, last])
+    kc2, vc2 = c_oracle.copy_blocks(kc, vc, [[src, free_block]])
+    bt[s_fork, last] = free_block
+    return kc2, vc2, bt, src
+
+
+def test_copy_blocks_c_and_numpy_agree_and_skip_invalid_pairs():
+    b = workloads.llama3_8b(num_seqs=4, max_ctx=120, min_ctx=40, poison=False)
+    pairs = [[3, 7], [5, 5], [2, b.num_blocks + 1], [-1, 9], [11, 1]]
+    ck, cv = c_oracle.copy_blocks(b.k_cache, b.v_cache, pairs)
+    nk, nv = numpy_oracle.copy_blocks(b.k_cache, b.v_cache, pairs)
+    assert np.array_equal(ck.view(np.uint16), nk.view(np.uint16))
+    assert np.array_equal(cv.view(np.uint16), nv.view(np.uint16))
+    changed = np.any(ck.view(np.uint16) != b.k_cache.view(np.uint16), axis=(1, 2, 3))
+    assert set(np.nonzero(changed)[0]) <= {7, 1}
+    assert np.array_equal(ck[7].view(np.uint16), b.k_cache[3].view(np.uint16))
+    with pytest.raises(c_oracle.OracleError):
+        c_oracle.copy_blocks(b.k_cache, b.v_cache, [[1, 2], [2, 3]])  # a destination is also a source
+
+
+def test_copy_on_write_keeps_the_original_and_forks_the_copy():
+    # two sequences share every block (a sample forked from a 37-token prompt)
+    rng = np.random.default_rng(4)
+    B, Hk, H, d, n = 16, 2, 4, 64, 37
+    K = rng.standard_normal((n, Hk, d), dtype=np.float32).astype(np.float16)
+    V = rng.standard_normal((n, Hk, d), dtype=np.float32).astype(np.float16)
+    q = rng.standard_normal((2, H, d), dtype=np.float32).astype(np.float16)
+    N = 8
+    ids = np.array([5, 2, 6], np.int32)
+    kc = np.full((N, B, Hk, d), np.float16(np.nan), np.float16)
+    vc = np.full_like(kc, np.float16(np.nan))
+    for t in range(n):
+        kc[ids[t // B], t % B] = K[t]
+        vc[ids[t // B], t % B] = V[t]
+    batch = workloads.PagedBatch(name="cow", num_seqs=2, num_heads=H, num_kv_heads=Hk, head_dim=d, block_size=B,
+                                 num_blocks=N, max_blocks_per_seq=3, scale=0.125, q=q, k_cache=kc, v_cache=vc,
+                                 block_tables=np.stack([ids, ids]), context_lens=np.array([n, n], np.int32),
+                                 key=K[:0], value=V[:0], slot_mapping=np.zeros(0, np.int64),
+                                 partition_size=16, unique_blocks=3)
+    kc2, vc2, bt, src = _cow_fork(batch, kc, vc, 1, free_block=0)
+    # sequence 1 now writes its 38th token into the private copy (slot 5 of block 0)
+    newk = rng.standard_normal((1, Hk, d), dtype=np.float32).astype(np.float16)
+    newv = rng.standard_normal((1, Hk, d), dtype=np.float32).astype(np.float16)
+    kc3, vc3 = c_oracle.reshape_and_cache(newk, newv, kc2, vc2, np.array([0 * B + n % B]))
+    cl = np.array([n, n + 1], np.int32)
+    out = c_oracle.decode(q, kc3, vc3, bt, cl, 0.125)
+    before = c_oracle.decode(q, kc, vc, np.stack([ids, ids]), np.array([n, n], np.int32), 0.125)
+    assert np.array_equal(out[0], before[0])           # the original sequence is untouched
+    assert np.array_equal(kc3[src].view(np.uint16), kc[src].view(np.uint16))  # and so is its block
+    ks = np.concatenate([K, newk]).astype(np.float64)
+    vs = np.concatenate([V, newv]).astype(np.float64)
+    ref = _sdpa_contiguous(q[1], ks, vs, 0.125, H // Hk)
+    np.testing.assert_allclose(out[1], ref, rtol=0, atol=1e-12)

@@ -291,3 +291,55 @@ def test_full_size_workloads_on_sampled_sequences(name):
     ref_k, ref_v = c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
     assert np.array_equal(d.k_cache.cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
     assert np.array_equal(d.v_cache.cpu().numpy().view(np.uint16), ref_v.view(np.uint16))
+
+
+# ------------------------------------------------------------ copy-on-write
+@pytest.mark.parametrize("shape", [(16, 8, 128), (256, 8, 128), (32, 4, 64)])
+def test_copy_blocks_is_bit_exact(shape):
+    B, Hk, d = shape
+    b = workloads.build_batch(name="cp", seed=12, context_lens=[B * 3 + 1, B * 2], num_heads=Hk,
+                              num_kv_heads=Hk, head_dim=d, block_size=B, num_blocks=20, poison=True)
+    srcs = [int(b.block_tables[0, 0]), int(b.block_tables[0, 3]), int(b.block_tables[1, 1])]
+    free = [i for i in range(b.num_blocks) if i not in set(b.block_tables[b.block_tables >= 0].tolist())]
+    pairs = np.array([[srcs[0], free[0]], [srcs[1], free[1]], [4, 4],
+                      [2, b.num_blocks + 3], [srcs[2], free[2]]], np.int64)
+    kc, vc = T(b.k_cache), T(b.v_cache)
+    api.pa_copy_blocks(kc, vc, T(pairs))
+    ref_k, ref_v = c_oracle.copy_blocks(b.k_cache, b.v_cache, pairs)
+    torch.cuda.synchronize()
+    assert np.array_equal(kc.cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
+    assert np.array_equal(vc.cpu().numpy().view(np.uint16), ref_v.view(np.uint16))
+
+
+def test_copy_on_write_fork_then_decode():
+    # 8 samples share a 2-block prompt whose last block is partial (20 tokens);
+    # sample 3 forks: its shared last block is copied, repointed, then written
+    B, S = 16, 8
+    b = workloads.build_batch(name="fork", seed=13, context_lens=[20], num_heads=8, num_kv_heads=2,
+                              head_dim=128, block_size=B, new_token=False, poison=True, num_blocks=12)
+    q = np.random.default_rng(3).standard_normal((S, 8, 128), dtype=np.float32).astype(np.float16)
+    bt = np.repeat(b.block_tables, S, axis=0)
+    kc_h, vc_h = b.k_cache.copy(), b.v_cache.copy()
+    # the shared prompt: every sample reads blocks bt[0]
+    free = [i for i in range(b.num_blocks) if i not in set(bt[0].tolist())][0]
+    shared_last = int(bt[0, 1])
+    newk = np.random.default_rng(1).standard_normal((1, 2, 128), dtype=np.float32).astype(np.float16)
+    newv = np.random.default_rng(2).standard_normal((1, 2, 128), dtype=np.float32).astype(np.float16)
+    slot = np.array([free * B + 20 % B], np.int64)
+    bt2 = bt.copy()
+    bt2[3, 1] = free
+    cl = np.full(S, 20, np.int32)
+    cl[3] = 21
+    # oracle: copy, write, decode
+    ok, ov = c_oracle.copy_blocks(kc_h, vc_h, [[shared_last, free]])
+    ok, ov = c_oracle.reshape_and_cache(newk, newv, ok, ov, slot)
+    ref = c_oracle.decode(q, ok, ov, bt2, cl, b.scale)
+    # GPU: the same three calls
+    kc, vc = T(kc_h), T(vc_h)
+    api.pa_copy_blocks(kc, vc, T(np.array([[shared_last, free]], np.int64)))
+    api.pa_reshape_and_cache(T(newk), T(newv), kc, vc, T(slot))
+    out = torch.empty_like(T(q))
+    api.pa_decode(out, T(q), kc, vc, T(bt2), T(cl), b.scale)
+    assert max_err(out, ref) <= TOL
+    # the other samples still read the shared block, unchanged
+    assert np.array_equal(kc.cpu().numpy()[shared_last].view(np.uint16), kc_h[shared_last].view(np.uint16))

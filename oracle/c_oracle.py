@@ -37,7 +37,14 @@ def lib() -> ctypes.CDLL:
         L.pa_oracle_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I]
         L.pa_oracle_reshape_and_cache.restype = _I
         L.pa_oracle_decode.argtypes = [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I64,
-                                       ctypes.c_double, _I, _I]
+                                       ctypes.c_double, _I, _I, _I, ctypes.c_double, ctypes.c_double]
+        L.pa_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.pa_oracle_e4m3_to_double.restype = ctypes.c_double
+        L.pa_oracle_quantize_e4m3.argtypes = [ctypes.c_float, ctypes.c_float]
+        L.pa_oracle_quantize_e4m3.restype = ctypes.c_uint8
+        L.pa_oracle_reshape_and_cache_fp8.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I,
+                                                      ctypes.c_float, ctypes.c_float]
+        L.pa_oracle_reshape_and_cache_fp8.restype = _I
         L.pa_oracle_decode.restype = _I
         L.pa_oracle_copy_blocks.argtypes = [_P, _P, _P, _I64, _I64, _I, _I, _I]
         L.pa_oracle_copy_blocks.restype = _I
@@ -64,7 +71,35 @@ def bf16_to_double(bits: int) -> float:
     return lib().pa_oracle_bf16_to_double(int(bits) & 0xFFFF)
 
 
-DTYPES = {"fp16": 0, "bf16": 1}
+DTYPES = {"fp16": 0, "bf16": 1, "fp8": 2}
+
+
+def e4m3_to_double(bits: int) -> float:
+    return lib().pa_oracle_e4m3_to_double(int(bits) & 0xFF)
+
+
+def quantize_e4m3(x: float, scale: float) -> int:
+    return int(lib().pa_oracle_quantize_e4m3(float(x), float(scale)))
+
+
+def reshape_and_cache_fp8(key: np.ndarray, value: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                          slot_mapping: np.ndarray, k_scale: float, v_scale: float,
+                          dtype: str = "fp16") -> Tuple[np.ndarray, np.ndarray]:
+    """Return copies of the E4M3 pools (uint8) after quantising and writing
+    the new tokens (key/value: float16, or bfloat16 bit patterns)."""
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    kc = np.ascontiguousarray(k_cache).copy()
+    vc = np.ascontiguousarray(v_cache).copy()
+    N, B, Hk, d = kc.shape
+    key = np.ascontiguousarray(key)
+    value = np.ascontiguousarray(value)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    rc = lib().pa_oracle_reshape_and_cache_fp8(_ptr(key), _ptr(value), _ptr(kc), _ptr(vc), _ptr(sm),
+                                               int(sm.size), N, B, Hk, d, DTYPES[dtype], float(k_scale),
+                                               float(v_scale))
+    if rc:
+        raise OracleError(f"reshape_and_cache_fp8 precondition failed ({rc})")
+    return kc, vc
 
 
 def locate_kv(logical_token_idx: int, block_table, block_size: int) -> Tuple[int, int]:
@@ -113,10 +148,13 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, block_mapping) -> Tupl
 
 
 def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables: np.ndarray,
-           context_lens: np.ndarray, scale: float, num_threads: int = 0, dtype: str = "fp16") -> np.ndarray:
+           context_lens: np.ndarray, scale: float, num_threads: int = 0, dtype: str = "fp16",
+           k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
     """float64 attention output [S, H, d].  q and the caches are float16
-    arrays, or (dtype="bf16") uint16 arrays of bfloat16 bit patterns."""
-    assert q.itemsize == 2 and k_cache.itemsize == 2 and v_cache.itemsize == 2
+    arrays, or (dtype="bf16") uint16 arrays of bfloat16 bit patterns; uint8
+    caches are E4M3 codes whose values are multiplied by k_scale / v_scale."""
+    cache_dtype = "fp8" if k_cache.dtype == np.uint8 else dtype
+    assert q.itemsize == 2 and k_cache.dtype == v_cache.dtype
     q = np.ascontiguousarray(q)
     k_cache = np.ascontiguousarray(k_cache)
     v_cache = np.ascontiguousarray(v_cache)
@@ -128,7 +166,8 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables
     out = np.zeros((S, H, d), dtype=np.float64)
     rc = lib().pa_oracle_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt),
                                 int(bt.shape[1]), _ptr(cl), S, H, Hk, d, B, N, float(scale),
-                                int(num_threads), DTYPES[dtype])
+                                int(num_threads), DTYPES[dtype], DTYPES[cache_dtype], float(k_scale),
+                                float(v_scale))
     if rc:
         raise OracleError(f"decode precondition failed ({rc})")
     return out

@@ -34,9 +34,16 @@
  *    h / (num_heads / num_kv_heads) (grouped-query attention with consecutive
  *    groups; the pages do not fix the mapping).
  *
+ *  - FP8 caches: the block's contents are compressed and the attention
+ *    kernel dequantises them ("PagedAttention: when the KV cache meets OS
+ *    paging", section 6, the layer diagram).  The page names FP8 and nothing
+ *    more; the oracle reads it as OCP E4M3 ("e4m3fn") codes with one float
+ *    scale for the K pool and one for the V pool: the write stores the code
+ *    nearest to x / scale, the read uses code value * scale.
+ *
  *  The K and V pools have the layout [num_blocks, block_size, num_kv_heads,
- *  head_dim]; values are IEEE binary16 or bfloat16 bit patterns, each
- *  decoded by its own routine below.
+ *  head_dim]; values are IEEE binary16 or bfloat16 bit patterns, or E4M3
+ *  bytes, each decoded by its own routine below.
  */
 #include <math.h>
 #include <stdint.h>
@@ -88,6 +95,62 @@ double pa_oracle_bf16_to_double(uint16_t bits) {
         v = ldexp((double)(128 + frac), expo - 134);
     }
     return sign ? -v : v;
+}
+
+/* FP8 E4M3 (OCP "e4m3fn") -> double, from the format's definition: 1 sign
+ * bit, 4 exponent bits (bias 7), 3 fraction bits; exponent 0 encodes zero
+ * and subnormals (fraction * 2^-9); no infinities; exponent 15 with fraction
+ * 7 is NaN, so the largest finite value is 1.75 * 2^8 = 448. */
+double pa_oracle_e4m3_to_double(uint8_t bits) {
+    const int sign = (bits >> 7) & 1;
+    const int expo = (bits >> 3) & 0xf;
+    const int frac = bits & 0x7;
+    double v;
+    if (expo == 15 && frac == 7) {
+        v = NAN;
+    } else if (expo == 0) {
+        v = ldexp((double)frac, -9);
+    } else {
+        v = ldexp((double)(8 + frac), expo - 10);
+    }
+    return sign ? -v : v;
+}
+
+/* Round half to even of a non-negative double to an integer-valued double. */
+static double round_half_even(double a) {
+    const double f = floor(a);
+    const double r = a - f;
+    if (r > 0.5) return f + 1.0;
+    if (r < 0.5) return f;
+    return fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+}
+
+/* The E4M3 code of x / scale: the quotient is taken in float32 (correctly
+ * rounded), then rounded to the nearest E4M3 value, ties to even; finite
+ * values beyond 448 saturate to +-448 and so do infinities; NaN gives NaN. */
+uint8_t pa_oracle_quantize_e4m3(float x, float scale) {
+    const float v = x / scale;
+    if (isnan(v)) return 0x7f;
+    const int sign = signbit(v) ? 1 : 0;
+    double a = fabs((double)v);
+    int code;
+    if (a >= 448.0) {
+        code = 0x7e;
+    } else if (a < ldexp(1.0, -6)) {             /* subnormal quanta of 2^-9 */
+        code = (int)round_half_even(a / ldexp(1.0, -9)); /* 8 becomes the smallest normal */
+    } else {
+        int e = (int)floor(log2(a));
+        if (ldexp(1.0, e) > a) --e;                /* guard log2 rounding */
+        if (ldexp(1.0, e + 1) <= a) ++e;
+        double m = round_half_even(a / ldexp(1.0, e - 3)); /* 8 .. 16 */
+        if (m == 16.0) {
+            m = 8.0;
+            ++e;
+        }
+        code = ((e + 7) << 3) | ((int)m - 8);
+        if (code > 0x7e) code = 0x7e;
+    }
+    return (uint8_t)((sign << 7) | code);
 }
 
 #define ORACLE_FP16 0
@@ -151,6 +214,32 @@ int pa_oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint
     return ORACLE_OK;
 }
 
+/* The cache write into an FP8 E4M3 cache ("when the KV cache meets OS
+ * paging", section 6: compress inside the block): each element of the new token's K
+ * (V) row, decoded from key (value) of dtype 0 (binary16) or 1 (bfloat16), is
+ * stored as pa_oracle_quantize_e4m3(x, k_scale) (v_scale).  Slots as in
+ * pa_oracle_reshape_and_cache. */
+int pa_oracle_reshape_and_cache_fp8(const uint16_t* key, const uint16_t* value, uint8_t* k_cache,
+                                    uint8_t* v_cache, const int64_t* slot_mapping, int64_t num_tokens,
+                                    int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                                    int dtype, float k_scale, float v_scale) {
+    if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return ORACLE_BAD_ARG;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * block_size) return ORACLE_BAD_SLOT;
+        for (int64_t e = 0; e < row; ++e) {
+            const float kx = (float)decode_elem(key[t * row + e], dtype);
+            const float vx = (float)decode_elem(value[t * row + e], dtype);
+            k_cache[slot * row + e] = pa_oracle_quantize_e4m3(kx, k_scale);
+            v_cache[slot * row + e] = pa_oracle_quantize_e4m3(vx, v_scale);
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* Copy whole blocks, the copy step of copy-on-write ("Unveiling the NVIDIA
  * driver stack", section 4; "in-depth reading", section 2.4): for each pair
  * (src, dst) the dst block of both pools becomes a copy of the src block.
@@ -187,11 +276,19 @@ int pa_oracle_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int64_t* b
     return ORACLE_OK;
 }
 
+/* Element `idx` of a cache of cache_dtype 0/1 (16-bit) or 2 (E4M3 bytes,
+ * multiplied by its scale). */
+static double cache_elem(const void* cache, int64_t idx, int cache_dtype, double cache_scale) {
+    if (cache_dtype == 2) return pa_oracle_e4m3_to_double(((const uint8_t*)cache)[idx]) * cache_scale;
+    return decode_elem(((const uint16_t*)cache)[idx], cache_dtype);
+}
+
 /* One (sequence, query head): gather, score, softmax, weighted sum. */
-static int decode_one(double* out, const uint16_t* q_row, const uint16_t* k_cache,
-                      const uint16_t* v_cache, const int32_t* table, int max_blocks_per_seq,
+static int decode_one(double* out, const uint16_t* q_row, const void* k_cache,
+                      const void* v_cache, const int32_t* table, int max_blocks_per_seq,
                       int ctx, int num_kv_heads, int kv_head, int head_dim, int block_size,
-                      int64_t num_blocks, double scale, int dtype) {
+                      int64_t num_blocks, double scale, int dtype, int cache_dtype, double k_scale,
+                      double v_scale) {
     if (ctx < 0 || (int64_t)ctx > (int64_t)max_blocks_per_seq * block_size) return ORACLE_BAD_CONTEXT;
     for (int j = 0; j < head_dim; ++j) out[j] = 0.0;
     if (ctx == 0) return ORACLE_OK; /* an empty sequence yields zeros */
@@ -215,8 +312,8 @@ static int decode_one(double* out, const uint16_t* q_row, const uint16_t* k_cach
         }
         const int64_t base = (((int64_t)phys * block_size + off) * num_kv_heads + kv_head) * head_dim;
         for (int j = 0; j < head_dim; ++j) {
-            K[(size_t)i * head_dim + j] = decode_elem(k_cache[base + j], dtype);
-            V[(size_t)i * head_dim + j] = decode_elem(v_cache[base + j], dtype);
+            K[(size_t)i * head_dim + j] = cache_elem(k_cache, base + j, cache_dtype, k_scale);
+            V[(size_t)i * head_dim + j] = cache_elem(v_cache, base + j, cache_dtype, v_scale);
         }
     }
     if (rc == ORACLE_OK) {
@@ -246,16 +343,19 @@ static int decode_one(double* out, const uint16_t* q_row, const uint16_t* k_cach
 
 /* Decode attention for every (sequence, query head).
  * out: [num_seqs, num_heads, head_dim] float64; q: [num_seqs, num_heads,
- * head_dim]; block_tables: [num_seqs, max_blocks_per_seq].  q and the caches
- * hold bit patterns of dtype 0 (binary16) or 1 (bfloat16).
- * num_threads <= 0 uses every available thread. */
-int pa_oracle_decode(double* out, const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+ * head_dim]; block_tables: [num_seqs, max_blocks_per_seq].  q holds bit
+ * patterns of dtype 0 (binary16) or 1 (bfloat16); the caches hold bit
+ * patterns of cache_dtype 0 or 1, or (2) E4M3 bytes whose values are
+ * multiplied by k_scale (v_scale).  num_threads <= 0 uses every available
+ * thread. */
+int pa_oracle_decode(double* out, const uint16_t* q, const void* k_cache, const void* v_cache,
                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
                      int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                     int64_t num_blocks, double scale, int num_threads, int dtype) {
+                     int64_t num_blocks, double scale, int num_threads, int dtype, int cache_dtype,
+                     double k_scale, double v_scale) {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks <= 0 || max_blocks_per_seq <= 0 || num_heads % num_kv_heads != 0 ||
-        (dtype != ORACLE_FP16 && dtype != ORACLE_BF16))
+        (dtype != ORACLE_FP16 && dtype != ORACLE_BF16) || cache_dtype < 0 || cache_dtype > 2)
         return ORACLE_BAD_ARG;
     const int group = num_heads / num_kv_heads;
     const int64_t work = (int64_t)num_seqs * num_heads;
@@ -270,7 +370,7 @@ int pa_oracle_decode(double* out, const uint16_t* q, const uint16_t* k_cache, co
         const int r = decode_one(out + w * head_dim, q + w * head_dim, k_cache, v_cache,
                                  block_tables + (int64_t)s * max_blocks_per_seq, max_blocks_per_seq,
                                  context_lens[s], num_kv_heads, h / group, head_dim, block_size,
-                                 num_blocks, scale, dtype);
+                                 num_blocks, scale, dtype, cache_dtype, k_scale, v_scale);
         if (r != ORACLE_OK) {
 #ifdef _OPENMP
 #pragma omp critical

@@ -42,6 +42,15 @@ import numpy as np
 
 FP16_NAN_BITS = np.uint16(0x7E00)
 BF16_NAN_BITS = np.uint16(0x7FC0)
+E4M3_NAN_BITS = np.uint8(0x7F)
+FP8_SCALE = 2.0 ** -5  # FP8 pools hold N(0,1) / FP8_SCALE as E4M3 codes (an exact power of two)
+
+
+def f32_to_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """E4M3 codes of float32 values, through torch's float8 conversion."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -76,6 +85,9 @@ class PagedBatch:
     partition_size: int  # split-K partition length (tokens) for this workload
     unique_blocks: int  # distinct physical blocks referenced by the tables
     dtype: str = "fp16"  # "fp16": float16 arrays; "bf16": uint16 bfloat16 bit patterns
+    kv_dtype: str = ""  # "": the caches have `dtype`; "fp8": uint8 E4M3 codes scaled by k/v_scale
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def group_size(self) -> int:
@@ -120,6 +132,7 @@ def build_batch(
     rng: Optional[np.random.Generator] = None,
     q_scale: float = 1.0,
     dtype: str = "fp16",
+    kv_dtype: str = "",
 ) -> PagedBatch:
     """Build one batch.
 
@@ -183,8 +196,14 @@ def build_batch(
     q = _normal_f16(rng, (S, H, d), dtype=dtype)
     if q_scale != 1.0:
         q = (q.astype(np.float32) * np.float32(q_scale)).astype(np.float16)
-    k_cache = _normal_f16(rng, (N, B, Hk, d), dtype=dtype)
-    v_cache = _normal_f16(rng, (N, B, Hk, d), dtype=dtype)
+    if kv_dtype == "fp8":
+        assert dtype == "fp16", "FP8 caches take float16 queries and new tokens"
+        k_cache = f32_to_e4m3_codes(_normal_f16(rng, (N, B, Hk, d)).astype(np.float32) / np.float32(FP8_SCALE))
+        v_cache = f32_to_e4m3_codes(_normal_f16(rng, (N, B, Hk, d)).astype(np.float32) / np.float32(FP8_SCALE))
+    else:
+        assert kv_dtype == ""
+        k_cache = _normal_f16(rng, (N, B, Hk, d), dtype=dtype)
+        v_cache = _normal_f16(rng, (N, B, Hk, d), dtype=dtype)
 
     T = S if new_token else 0
     key = _normal_f16(rng, (T, Hk, d), dtype=dtype)
@@ -206,9 +225,12 @@ def build_batch(
             for s in range(S):
                 sl = int(slot_mapping[s])
                 valid[sl // B, sl % B] = False
-        kb = k_cache.view(np.uint16)
-        vb = v_cache.view(np.uint16)
-        nan = FP16_NAN_BITS if dtype == "fp16" else BF16_NAN_BITS
+        if kv_dtype == "fp8":
+            kb, vb, nan = k_cache, v_cache, E4M3_NAN_BITS
+        else:
+            kb = k_cache.view(np.uint16)
+            vb = v_cache.view(np.uint16)
+            nan = FP16_NAN_BITS if dtype == "fp16" else BF16_NAN_BITS
         kb[~valid] = nan
         vb[~valid] = nan
 
@@ -218,6 +240,8 @@ def build_batch(
         q=q, k_cache=k_cache, v_cache=v_cache, block_tables=tables,
         context_lens=ctx.astype(np.int32), key=key, value=value, slot_mapping=slot_mapping,
         partition_size=int(partition_size), unique_blocks=int(unique_blocks), dtype=dtype,
+        kv_dtype=kv_dtype, k_scale=FP8_SCALE if kv_dtype == "fp8" else 1.0,
+        v_scale=FP8_SCALE if kv_dtype == "fp8" else 1.0,
     )
 
 
@@ -238,7 +262,7 @@ def tiny(seed: int = 0, poison: bool = True) -> PagedBatch:
 
 def llama3_8b(seed: int = 0, num_seqs: int = 64, poison: bool = True,
               min_ctx: int = 128, max_ctx: int = 2048, partition_size: int = 512,
-              dtype: str = "fp16") -> PagedBatch:
+              dtype: str = "fp16", kv_dtype: str = "") -> PagedBatch:
     """Llama-3-8B-shaped decode layer: 32 q heads, 8 KV heads (GQA 4), d = 128,
     B = 16; contexts uniform in [min_ctx, max_ctx]; 1.25x pool, shuffled ids."""
     rng = np.random.default_rng(seed)
@@ -246,31 +270,31 @@ def llama3_8b(seed: int = 0, num_seqs: int = 64, poison: bool = True,
     return build_batch(name="llama3-8b", seed=seed, rng=rng, context_lens=ctx, num_heads=32,
                        num_kv_heads=8, head_dim=128, block_size=16,
                        max_blocks_per_seq=(max_ctx + 15) // 16, poison=poison,
-                       partition_size=partition_size, dtype=dtype)
+                       partition_size=partition_size, dtype=dtype, kv_dtype=kv_dtype)
 
 
 def llama2_70b(seed: int = 0, block_size: int = 16, num_seqs: int = 32, ctx: int = 8192,
-               poison: bool = True, partition_size: int = 512, dtype: str = "fp16") -> PagedBatch:
+               poison: bool = True, partition_size: int = 512, dtype: str = "fp16", kv_dtype: str = "") -> PagedBatch:
     """Llama-2-70B-shaped GQA decode: 64 q heads, 8 KV heads (GQA 8), d = 128;
     every context ``ctx`` tokens; one new token per sequence at position
     ctx - 1; 1.25x pool, shuffled ids."""
     return build_batch(name=f"llama2-70b-b{block_size}", seed=seed, context_lens=[ctx] * num_seqs,
                        num_heads=64, num_kv_heads=8, head_dim=128, block_size=block_size,
-                       poison=poison, partition_size=partition_size, dtype=dtype)
+                       poison=poison, partition_size=partition_size, dtype=dtype, kv_dtype=kv_dtype)
 
 
 def long_context(seed: int = 0, ctxs: Sequence[int] = (32768, 65536, 98304, 131072),
-                 poison: bool = True, partition_size: int = 512, dtype: str = "fp16") -> PagedBatch:
+                 poison: bool = True, partition_size: int = 512, dtype: str = "fp16", kv_dtype: str = "") -> PagedBatch:
     """Long-context split-K decode: 32 q heads, 8 KV heads, d = 128, B = 16;
     4 sequences of 32K..128K tokens; 512-token partitions."""
     return build_batch(name="long-context", seed=seed, context_lens=list(ctxs), num_heads=32,
                        num_kv_heads=8, head_dim=128, block_size=16, poison=poison,
-                       partition_size=partition_size, dtype=dtype)
+                       partition_size=partition_size, dtype=dtype, kv_dtype=kv_dtype)
 
 
 def shared_prefix(seed: int = 0, num_prompts: int = 16, samples: int = 8, prompt_len: int = 1024,
                   max_suffix: int = 512, poison: bool = True, partition_size: int = 512,
-                  dtype: str = "fp16") -> PagedBatch:
+                  dtype: str = "fp16", kv_dtype: str = "") -> PagedBatch:
     """Parallel sampling: ``num_prompts`` prompts of ``prompt_len`` tokens, each
     sampled ``samples`` times.  The samples' tables point at the same prompt
     blocks (reference count ``samples``) and then diverge with suffixes
@@ -285,7 +309,7 @@ def shared_prefix(seed: int = 0, num_prompts: int = 16, samples: int = 8, prompt
     return build_batch(name="shared-prefix", seed=seed, rng=rng, context_lens=ctx, num_heads=40,
                        num_kv_heads=40, head_dim=128, block_size=16, max_blocks_per_seq=M,
                        share_groups=groups, shared_prefix_len=prompt_len, poison=poison,
-                       partition_size=partition_size, dtype=dtype)
+                       partition_size=partition_size, dtype=dtype, kv_dtype=kv_dtype)
 
 
 WORKLOADS = {
@@ -301,19 +325,24 @@ WORKLOADS = {
 # Byte accounting for the measurement (what one decode must read at least).
 # ---------------------------------------------------------------------------
 
+def kv_elem_bytes(batch: PagedBatch) -> int:
+    """Bytes of one cache element: 1 for E4M3 caches, else 2."""
+    return 1 if batch.kv_dtype == "fp8" else 2
+
+
 def kv_bytes_per_token(num_kv_heads: int, head_dim: int, elem_bytes: int = 2) -> int:
     """K plus V bytes of one token of one layer."""
     return 2 * num_kv_heads * head_dim * elem_bytes
 
 
-def algorithmic_kv_bytes(batch: PagedBatch, elem_bytes: int = 2) -> int:
+def algorithmic_kv_bytes(batch: PagedBatch, elem_bytes: int = 0) -> int:
     """Sum over sequences of ctx * (K + V bytes per token): the valid slots
     only, counted once per sequence that reads them (logical bytes)."""
     return int(np.sum(batch.context_lens.astype(np.int64))) * kv_bytes_per_token(
-        batch.num_kv_heads, batch.head_dim, elem_bytes)
+        batch.num_kv_heads, batch.head_dim, elem_bytes or kv_elem_bytes(batch))
 
 
-def unique_kv_bytes(batch: PagedBatch, elem_bytes: int = 2) -> int:
+def unique_kv_bytes(batch: PagedBatch, elem_bytes: int = 0) -> int:
     """Bytes of the distinct valid slots (shared prefix blocks counted once)."""
     seen = set()
     B = batch.block_size
@@ -327,4 +356,5 @@ def unique_kv_bytes(batch: PagedBatch, elem_bytes: int = 2) -> int:
                 continue
             seen.add(blk)
             total_slots += valid
-    return total_slots * kv_bytes_per_token(batch.num_kv_heads, batch.head_dim, elem_bytes)
+    return total_slots * kv_bytes_per_token(batch.num_kv_heads, batch.head_dim,
+                                            elem_bytes or kv_elem_bytes(batch))

@@ -544,3 +544,67 @@ def test_copy_on_write_keeps_the_original_and_forks_the_copy():
     vs = np.concatenate([V, newv]).astype(np.float64)
     ref = _sdpa_contiguous(q[1], ks, vs, 0.125, H // Hk)
     np.testing.assert_allclose(out[1], ref, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) caches
+# --------------------------------------------------------------------------
+
+def test_e4m3_decoding_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([c_oracle.e4m3_to_double(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_e4m3_quantiser_matches_torch_within_range():
+    rng = np.random.default_rng(7)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(40.0),
+        rng.standard_normal(5000).astype(np.float32) * np.float32(0.004),   # subnormal range
+        np.array([1.0625, 1.1875, -3.25, 0.0, -0.0, 2.0 ** -10, 3 * 2.0 ** -10, 464.0, -464.0, 447.9],
+                 np.float32),                                              # ties and edges
+    ])
+    x = x[np.abs(x) <= 464.0]
+    ours = np.array([c_oracle.quantize_e4m3(float(v), 1.0) for v in x], np.uint8)
+    theirs = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, theirs)
+
+
+def test_e4m3_quantiser_saturates_and_divides_by_the_scale():
+    assert c_oracle.quantize_e4m3(1000.0, 1.0) == 0x7E
+    assert c_oracle.quantize_e4m3(-1e30, 1.0) == 0xFE
+    assert c_oracle.quantize_e4m3(float("inf"), 1.0) == 0x7E
+    assert c_oracle.quantize_e4m3(float("nan"), 1.0) == 0x7F
+    # x / scale: 1.5 / 0.25 = 6 exactly
+    assert c_oracle.e4m3_to_double(c_oracle.quantize_e4m3(1.5, 0.25)) == 6.0
+    # relative error of a normal value is at most half a 3-bit ulp, 2^-4
+    rng = np.random.default_rng(8)
+    for v in rng.uniform(0.02, 400.0, 2000):
+        back = c_oracle.e4m3_to_double(c_oracle.quantize_e4m3(float(v), 1.0))
+        assert abs(back - np.float32(v)) <= 2.0 ** -4 * abs(np.float32(v))
+
+
+def test_fp8_cache_write_and_decode_equal_library_attention_on_dequantised_values():
+    b = workloads.build_batch(name="fp8", seed=31, context_lens=[1, 20, 45], num_heads=8, num_kv_heads=2,
+                              head_dim=128, block_size=16, kv_dtype="fp8")
+    kc, vc = c_oracle.reshape_and_cache_fp8(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping,
+                                            b.k_scale, b.v_scale)
+    # the new token's row holds the quantised key
+    s, pos = 1, 19
+    blk = b.block_tables[s, pos // 16]
+    want = [c_oracle.quantize_e4m3(float(x), b.k_scale) for x in b.key[s].reshape(-1)]
+    assert np.array_equal(kc[blk, pos % 16].reshape(-1), np.array(want, np.uint8))
+    got = c_oracle.decode(b.q, kc, vc, b.block_tables, b.context_lens, b.scale, k_scale=b.k_scale,
+                          v_scale=b.v_scale)
+    assert np.isfinite(got).all()
+    deq = np.vectorize(c_oracle.e4m3_to_double)
+    for s in range(b.num_seqs):
+        c = int(b.context_lens[s])
+        ks = np.stack([deq(kc[b.block_tables[s, t // 16], t % 16]) for t in range(c)]) * b.k_scale
+        vs = np.stack([deq(vc[b.block_tables[s, t // 16], t % 16]) for t in range(c)]) * b.v_scale
+        ref = _sdpa_contiguous(b.q[s], ks, vs, b.scale, b.group_size)
+        np.testing.assert_allclose(got[s], ref, rtol=0, atol=1e-12)

@@ -55,8 +55,10 @@ typedef enum pa_status {
 } pa_status;
 
 typedef enum pa_dtype {
-  PA_FP16 = 0, /* IEEE binary16 */
-  PA_BF16 = 1  /* bfloat16 (the upper half of an IEEE binary32) */
+  PA_FP16 = 0,    /* IEEE binary16 */
+  PA_BF16 = 1,    /* bfloat16 (the upper half of an IEEE binary32) */
+  PA_FP8_E4M3 = 2 /* a cache of OCP E4M3 codes (pa_*_fp8 entry points and
+                     pa_copy_blocks only) */
 } pa_dtype;
 
 /*
@@ -111,8 +113,8 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
  *
  *   k_cache, v_cache  [num_blocks][block_size][num_kv_heads][head_dim]
  *   block_mapping     [num_pairs][2] int64 (src, dst)
- *   dtype             PA_FP16 or PA_BF16 (the copy moves bytes; only the
- *                     element size matters)
+ *   dtype             PA_FP16, PA_BF16 or PA_FP8_E4M3 (the copy moves
+ *                     bytes; only the element size matters)
  *
  * Device-value outcomes: a pair with an id outside [0, num_blocks), or with
  * src == dst, is skipped.  Destinations must be distinct and no destination
@@ -262,6 +264,70 @@ int pa_decode_splitk_static(void* out, const void* q, const void* k_cache, const
                             const int32_t* context_lens, int num_seqs, int num_heads,
                             int num_kv_heads, int head_dim, int block_size, int num_blocks,
                             float scale, int dtype, int partition_size, void* stream);
+
+/*
+ * FP8 caches.  "PagedAttention: when the KV cache meets OS paging", section
+ * 6, stacks FP8 quantisation of the KV cache on the block abstraction: the
+ * data are compressed inside each block and the attention kernel
+ * dequantises them.  The page fixes no format or scale; these entry points
+ * use OCP E4M3 ("e4m3fn": 1 sign, 4 exponent bits with bias 7, 3 fraction
+ * bits, no infinities, 0x7F/0xFF NaN, largest finite 448) and one float
+ * scale per pool: the element stored for x is
+ *
+ *     code = E4M3_satfinite( fp32(x) / k_scale )   (v_scale for V),
+ *
+ * the IEEE float32 quotient rounded to the nearest code, ties to even,
+ * finite values beyond 448 saturating to +-448; the element read back is
+ * value(code) * k_scale (v_scale).  The pools have the layout of the 16-bit
+ * caches with one byte per element.  Queries, new tokens and outputs stay
+ * 16-bit.  Scales must be finite and positive (else PA_ERR_INVALID_ARG).
+ */
+
+/*
+ * pa_reshape_and_cache_fp8 -- pa_reshape_and_cache into E4M3 pools.
+ *
+ *   key, value        [num_tokens][num_kv_heads][head_dim] of dtype
+ *                     (PA_FP16 or PA_BF16)
+ *   k_cache, v_cache  [num_blocks][block_size][num_kv_heads][head_dim]
+ *                     uint8 E4M3 codes; head_dim a multiple of 16
+ *
+ * Slots and device-value outcomes as pa_reshape_and_cache.
+ */
+int pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                             int block_size, int num_kv_heads, int head_dim, int dtype,
+                             float k_scale, float v_scale, void* stream);
+
+/*
+ * pa_decode_fp8 -- pa_decode over E4M3 pools: the same attention with
+ * K_i = value(k code) * k_scale and V_i = value(v code) * v_scale.  The
+ * codes are widened exactly to fp16 inside the kernel; k_scale multiplies
+ * the scores and v_scale the output, both in float32.
+ *
+ *   q, out   [num_seqs][num_heads][head_dim], dtype PA_FP16 (PA_BF16 is
+ *            PA_ERR_UNSUPPORTED)
+ *
+ * Other arguments, supported shapes and device-value outcomes as pa_decode
+ * (a NaN code in a valid slot gives NaN in the affected output).
+ */
+int pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                  int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                  int num_blocks, float scale, int dtype, float k_scale, float v_scale,
+                  void* stream);
+
+/*
+ * pa_decode_splitk_fp8 -- pa_decode_splitk over E4M3 pools.  The workspace
+ * holds the scaled float32 partials, so pa_splitk_reduce (dtype PA_FP16)
+ * finishes the call unchanged.
+ */
+int pa_decode_splitk_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int num_seqs, int num_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         float scale, int dtype, float k_scale, float v_scale, int partition_size,
+                         int max_num_partitions, void* workspace, size_t workspace_bytes,
+                         void* stream);
 
 /* Fixed text naming a status code. */
 const char* pa_status_string(int status);

@@ -136,10 +136,15 @@ def reshape_and_cache(key: np.ndarray, value: np.ndarray, k_cache: np.ndarray, v
 
 
 def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, block_mapping) -> Tuple[np.ndarray, np.ndarray]:
-    """Return copies of the pools after copying the (src, dst) blocks."""
+    """Return copies of the pools after copying the (src, dst) blocks.  The
+    copy moves whole blocks of bytes, so one-byte (E4M3) pools go through as
+    16-bit elements, two codes to an element."""
     kc = np.ascontiguousarray(k_cache).copy()
     vc = np.ascontiguousarray(v_cache).copy()
     N, B, Hk, d = kc.shape
+    if kc.itemsize == 1:
+        assert d % 2 == 0
+        d //= 2
     bm = np.ascontiguousarray(np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2))
     rc = lib().pa_oracle_copy_blocks(_ptr(kc), _ptr(vc), _ptr(bm), int(bm.shape[0]), N, B, Hk, d)
     if rc:

@@ -19,6 +19,7 @@ PA_ERR_UNSUPPORTED = -2
 PA_ERR_CUDA = -3
 PA_FP16 = 0
 PA_BF16 = 1
+PA_FP8_E4M3 = 2
 
 # Every function the header declares, with its ctypes signature.
 _P = ctypes.c_void_p
@@ -35,6 +36,10 @@ SIGNATURES = {
     "pa_splitk_reduce": (_I, [_P, _P, _SZ, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "pa_decode_splitk_static": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                      _P]),
+    "pa_reshape_and_cache_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _P]),
+    "pa_decode_fp8": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _F, _F, _P]),
+    "pa_decode_splitk_fp8": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _F, _F, _I,
+                                  _I, _P, _SZ, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
     "pa_last_error": (ctypes.c_char_p, []),
 }

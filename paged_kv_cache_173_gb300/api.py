@@ -12,9 +12,11 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import PA_BF16, PA_FP16, PagedAttnError  # noqa: F401  (re-exported)
+from ._lib import PA_BF16, PA_FP16, PA_FP8_E4M3, PagedAttnError  # noqa: F401  (re-exported)
 
 _DTYPES = {torch.float16: PA_FP16, torch.bfloat16: PA_BF16}
+# E4M3 pools: uint8 codes, or torch's float8_e4m3fn (the same bytes)
+_CODE_DTYPES = (torch.uint8, torch.float8_e4m3fn)
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -38,6 +40,13 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device) 
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return int(t.data_ptr())
+
+
+def _need_codes(t: torch.Tensor, name: str, device: torch.device) -> int:
+    """Pointer of an E4M3 pool (uint8 or float8_e4m3fn, contiguous, on `device`)."""
+    if not isinstance(t, torch.Tensor) or t.dtype not in _CODE_DTYPES:
+        raise TypeError(f"{name} must be a uint8 or float8_e4m3fn tensor of E4M3 codes")
+    return _need(t, name, t.dtype, device)
 
 
 def _cuda_device(t: torch.Tensor) -> torch.device:
@@ -77,14 +86,15 @@ def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: 
     if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
         raise ValueError("block_mapping must be [n, 2]")
     dt = k_cache.dtype
+    code = PA_FP8_E4M3 if dt in _CODE_DTYPES else _dtype_code(k_cache)
     st = _lib.lib().pa_copy_blocks(
         _need(k_cache, "k_cache", dt, dev), _need(v_cache, "v_cache", dt, dev),
         _need(block_mapping, "block_mapping", torch.int64, dev), int(block_mapping.shape[0]), N, B, Hk, d,
-        _dtype_code(k_cache), _stream_ptr(k_cache, stream))
+        code, _stream_ptr(k_cache, stream))
     _lib.check("pa_copy_blocks", st)
 
 
-def _decode_common(out, q, k_cache, v_cache, block_tables, context_lens):
+def _decode_common(out, q, k_cache, v_cache, block_tables, context_lens, codes: bool = False):
     dev = _cuda_device(q)
     S, H, d = q.shape
     N, B, Hk, d2 = k_cache.shape
@@ -94,8 +104,11 @@ def _decode_common(out, q, k_cache, v_cache, block_tables, context_lens):
         raise ValueError("block_tables must be [S, M] and context_lens [S]")
     dt = q.dtype
     _dtype_code(q)
-    ptrs = (_need(out, "out", dt, dev), _need(q, "q", dt, dev),
-            _need(k_cache, "k_cache", dt, dev), _need(v_cache, "v_cache", dt, dev),
+    if codes:
+        pk, pv = _need_codes(k_cache, "k_cache", dev), _need_codes(v_cache, "v_cache", dev)
+    else:
+        pk, pv = _need(k_cache, "k_cache", dt, dev), _need(v_cache, "v_cache", dt, dev)
+    ptrs = (_need(out, "out", dt, dev), _need(q, "q", dt, dev), pk, pv,
             _need(block_tables, "block_tables", torch.int32, dev))
     cl = _need(context_lens, "context_lens", torch.int32, dev)
     return dev, S, H, d, N, B, Hk, int(block_tables.shape[1]), ptrs, cl
@@ -168,6 +181,55 @@ def pa_decode_splitk_static(out: torch.Tensor, q: torch.Tensor, k_cache: torch.T
                                             float(scale), _dtype_code(q), int(partition_size),
                                             _stream_ptr(q, stream))
     _lib.check("pa_decode_splitk_static", st)
+
+
+def pa_reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                             v_cache: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,
+                             v_scale: float, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Quantise key/value [T, Hk, d] (float16 or bfloat16) into the E4M3 pools
+    [N, B, Hk, d] (uint8 codes) at slot_mapping [T]: code = E4M3(x / scale)."""
+    dev = _cuda_device(k_cache)
+    N, B, Hk, d = k_cache.shape
+    T = key.shape[0]
+    if key.shape != (T, Hk, d) or value.shape != (T, Hk, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("key/value must be [T, Hk, d] matching the pools [N, B, Hk, d]")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [T]")
+    dt = key.dtype
+    st = _lib.lib().pa_reshape_and_cache_fp8(
+        _need(key, "key", dt, dev), _need(value, "value", dt, dev),
+        _need_codes(k_cache, "k_cache", dev), _need_codes(v_cache, "v_cache", dev),
+        _need(slot_mapping, "slot_mapping", torch.int64, dev), T, N, B, Hk, d, _dtype_code(key),
+        float(k_scale), float(v_scale), _stream_ptr(k_cache, stream))
+    _lib.check("pa_reshape_and_cache_fp8", st)
+
+
+def pa_decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                  block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, k_scale: float,
+                  v_scale: float, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """pa_decode over E4M3 pools whose values are code * k_scale (K) and code * v_scale (V)."""
+    dev, S, H, d, N, B, Hk, M, (po, pq, pk, pv, pbt), pcl = _decode_common(
+        out, q, k_cache, v_cache, block_tables, context_lens, codes=True)
+    st = _lib.lib().pa_decode_fp8(po, pq, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N, float(scale),
+                                  _dtype_code(q), float(k_scale), float(v_scale), _stream_ptr(q, stream))
+    _lib.check("pa_decode_fp8", st)
+
+
+def pa_decode_splitk_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                         k_scale: float, v_scale: float, partition_size: int, workspace: torch.Tensor,
+                         max_num_partitions: Optional[int] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Split-K decode over E4M3 pools; follow with pa_splitk_reduce on the same stream."""
+    dev, S, H, d, N, B, Hk, M, (po, pq, pk, pv, pbt), pcl = _decode_common(
+        out, q, k_cache, v_cache, block_tables, context_lens, codes=True)
+    P = max_num_partitions or max_num_partitions_for(M, B, partition_size)
+    ws = _need(workspace, "workspace", workspace.dtype, dev)
+    st = _lib.lib().pa_decode_splitk_fp8(po, pq, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N, float(scale),
+                                         _dtype_code(q), float(k_scale), float(v_scale), int(partition_size),
+                                         int(P), ws, workspace.numel() * workspace.element_size(),
+                                         _stream_ptr(q, stream))
+    _lib.check("pa_decode_splitk_fp8", st)
 
 
 def pa_status_string(status: int) -> str:

@@ -108,6 +108,120 @@ int check_splitk(int max_blocks_per_seq, int block_size, int partition_size, int
   return PA_OK;
 }
 
+int check_kv_scales(float k_scale, float v_scale) {
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+    return fail(PA_ERR_INVALID_ARG, "k_scale (%g) and v_scale (%g) must be finite and positive",
+                static_cast<double>(k_scale), static_cast<double>(v_scale));
+  return PA_OK;
+}
+
+// The cache type of an E4M3 decode and the query types it takes.
+int check_fp8_decode(int dtype, float k_scale, float v_scale) {
+  if (dtype != PA_FP16)
+    return fail(PA_ERR_UNSUPPORTED, "E4M3 caches take PA_FP16 queries (got dtype %d)", dtype);
+  return check_kv_scales(k_scale, v_scale);
+}
+
+pa::DecodeArgs decode_args(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                           int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, float scale, int dtype, int kv_dtype, float k_scale,
+                           float v_scale) {
+  pa::DecodeArgs a{};
+  a.dtype = dtype;
+  a.kv_dtype = kv_dtype;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.ws = nullptr;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  return a;
+}
+
+// pa_decode / pa_decode_fp8 after their own dtype checks.
+int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                int num_blocks, float scale, int dtype, int kv_dtype, float k_scale, float v_scale,
+                void* stream) {
+  int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                        dtype);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0) return ok();
+  pa::DecodeArgs a = decode_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                 num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                 dtype, kv_dtype, k_scale, v_scale);
+  // One CTA per (sequence, KV head) when the pairs fill the GPU; otherwise a
+  // cluster of up to 8 CTAs per pair that split the sequence and merge
+  // through distributed shared memory (chosen by the launcher).
+  a.cluster_size = -1;
+  a.partition_size = max_blocks_per_seq * block_size;
+  a.max_num_partitions = 1;
+  return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)), "decode launch");
+}
+
+// pa_decode_splitk / pa_decode_splitk_fp8 after their own dtype checks.
+int splitk_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                int num_blocks, float scale, int dtype, int kv_dtype, float k_scale, float v_scale,
+                int partition_size, int max_num_partitions, void* workspace, size_t workspace_bytes,
+                void* stream) {
+  int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                        dtype);
+  if (st != PA_OK) return st;
+  st = check_splitk(max_blocks_per_seq, block_size, partition_size, max_num_partitions, workspace,
+                    workspace_bytes, num_seqs, num_heads, head_dim);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0) return ok();
+  pa::DecodeArgs a = decode_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                 num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                 dtype, kv_dtype, k_scale, v_scale);
+  a.ws = static_cast<float*>(workspace);
+  a.partition_size = partition_size;
+  a.max_num_partitions = max_num_partitions;
+  a.cluster_size = 0;
+  return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)), "split-K decode launch");
+}
+
+// The checks shared by both cache writes.
+int check_reshape(const void* key, const void* value, const void* k_cache, const void* v_cache,
+                  const int64_t* slot_mapping, int num_tokens, int num_blocks, int block_size,
+                  int num_kv_heads, int head_dim, int dtype) {
+  if (dtype != PA_FP16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 or PA_BF16)", dtype);
+  if (head_dim <= 0 || head_dim % 8 != 0 || head_dim > 1024)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (a multiple of 8, at most 1024)",
+                head_dim);
+  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens %d is negative", num_tokens);
+  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_blocks, block_size and num_kv_heads must be positive");
+  if (static_cast<int64_t>(num_tokens) * num_kv_heads > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "num_tokens * num_kv_heads exceeds 2^31 - 1");
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return fail(PA_ERR_INVALID_ARG, "key, value and the caches must be 16-byte aligned, "
+                "slot_mapping 8-byte aligned");
+  return PA_OK;
+}
+
 }  // namespace
 
 namespace pa {
@@ -145,39 +259,46 @@ size_t pa_splitk_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
 int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                          const int64_t* slot_mapping, int num_tokens, int num_blocks,
                          int block_size, int num_kv_heads, int head_dim, int dtype, void* stream) {
-  if (dtype != PA_FP16 && dtype != PA_BF16)
-    return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 or PA_BF16)", dtype);
-  if (head_dim <= 0 || head_dim % 8 != 0 || head_dim > 1024)
-    return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported (a multiple of 8, at most 1024)",
-                head_dim);
-  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens %d is negative", num_tokens);
-  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0)
-    return fail(PA_ERR_INVALID_ARG, "num_blocks, block_size and num_kv_heads must be positive");
-  if (static_cast<int64_t>(num_tokens) * num_kv_heads > INT32_MAX)
-    return fail(PA_ERR_UNSUPPORTED, "num_tokens * num_kv_heads exceeds 2^31 - 1");
+  const int st = check_reshape(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
+                               block_size, num_kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
   if (num_tokens == 0) return ok();
-  if (!key || !value || !k_cache || !v_cache || !slot_mapping)
-    return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(slot_mapping, 8))
-    return fail(PA_ERR_INVALID_ARG, "key, value and the caches must be 16-byte aligned, "
-                "slot_mapping 8-byte aligned");
-  pa::ReshapeArgs a{key, value, k_cache, v_cache, slot_mapping, num_tokens,
-                    num_blocks, block_size, num_kv_heads, head_dim};
+  pa::ReshapeArgs a{key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks, block_size,
+                    num_kv_heads, head_dim, dtype, dtype, 1.f, 1.f};
   return cuda_status(pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream)),
                      "reshape_and_cache launch");
+}
+
+int pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                             int block_size, int num_kv_heads, int head_dim, int dtype,
+                             float k_scale, float v_scale, void* stream) {
+  int st = check_reshape(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks, block_size,
+                         num_kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (head_dim % 16 != 0)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not supported for E4M3 caches (a multiple of 16)",
+                head_dim);
+  st = check_kv_scales(k_scale, v_scale);
+  if (st != PA_OK) return st;
+  if (num_tokens == 0) return ok();
+  pa::ReshapeArgs a{key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks, block_size,
+                    num_kv_heads, head_dim, dtype, PA_FP8_E4M3, k_scale, v_scale};
+  return cuda_status(pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream)),
+                     "reshape_and_cache_fp8 launch");
 }
 
 int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int num_pairs,
                    int num_blocks, int block_size, int num_kv_heads, int head_dim, int dtype,
                    void* stream) {
-  if (dtype != PA_FP16 && dtype != PA_BF16)
-    return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16 or PA_BF16)", dtype);
+  if (dtype != PA_FP16 && dtype != PA_BF16 && dtype != PA_FP8_E4M3)
+    return fail(PA_ERR_UNSUPPORTED, "dtype %d is not supported (PA_FP16, PA_BF16 or PA_FP8_E4M3)", dtype);
   if (num_pairs < 0) return fail(PA_ERR_INVALID_ARG, "num_pairs %d is negative", num_pairs);
   if (num_pairs > INT32_MAX / 2) return fail(PA_ERR_UNSUPPORTED, "num_pairs %d is too large", num_pairs);
   if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
     return fail(PA_ERR_INVALID_ARG, "num_blocks, block_size, num_kv_heads and head_dim must be positive");
-  const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * 2;
+  const int64_t block_bytes =
+      static_cast<int64_t>(block_size) * num_kv_heads * head_dim * (dtype == PA_FP8_E4M3 ? 1 : 2);
   if (block_bytes % 16 != 0)
     return fail(PA_ERR_UNSUPPORTED, "block bytes %lld are not a multiple of 16", (long long)block_bytes);
   if (num_pairs == 0) return ok();
@@ -192,35 +313,21 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
               int num_blocks, float scale, int dtype, void* stream) {
-  int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                        dtype);
+  return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, dtype, 1.f,
+                     1.f, stream);
+}
+
+int pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                  int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                  int num_blocks, float scale, int dtype, float k_scale, float v_scale,
+                  void* stream) {
+  const int st = check_fp8_decode(dtype, k_scale, v_scale);
   if (st != PA_OK) return st;
-  if (num_seqs == 0) return ok();
-  pa::DecodeArgs a{};
-  a.dtype = dtype;
-  a.out = out;
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.block_tables = block_tables;
-  a.context_lens = context_lens;
-  a.ws = nullptr;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.num_seqs = num_seqs;
-  a.num_heads = num_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.head_dim = head_dim;
-  a.block_size = block_size;
-  a.num_blocks = num_blocks;
-  a.scale = scale;
-  // One CTA per (sequence, KV head) when the pairs fill the GPU; otherwise a
-  // cluster of up to 8 CTAs per pair that split the sequence and merge
-  // through distributed shared memory (chosen by the launcher).
-  a.cluster_size = -1;
-  a.partition_size = max_blocks_per_seq * block_size;
-  a.max_num_partitions = 1;
-  return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)), "decode launch");
+  return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, PA_FP8_E4M3,
+                     k_scale, v_scale, stream);
 }
 
 int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -229,36 +336,24 @@ int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* 
                      int head_dim, int block_size, int num_blocks, float scale, int dtype,
                      int partition_size, int max_num_partitions, void* workspace,
                      size_t workspace_bytes, void* stream) {
-  int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                        dtype);
+  return splitk_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, dtype, 1.f,
+                     1.f, partition_size, max_num_partitions, workspace, workspace_bytes, stream);
+}
+
+int pa_decode_splitk_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int num_seqs, int num_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         float scale, int dtype, float k_scale, float v_scale, int partition_size,
+                         int max_num_partitions, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  const int st = check_fp8_decode(dtype, k_scale, v_scale);
   if (st != PA_OK) return st;
-  st = check_splitk(max_blocks_per_seq, block_size, partition_size, max_num_partitions, workspace,
-                    workspace_bytes, num_seqs, num_heads, head_dim);
-  if (st != PA_OK) return st;
-  if (num_seqs == 0) return ok();
-  pa::DecodeArgs a{};
-  a.dtype = dtype;
-  a.out = out;
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.block_tables = block_tables;
-  a.context_lens = context_lens;
-  a.ws = static_cast<float*>(workspace);
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.num_seqs = num_seqs;
-  a.num_heads = num_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.head_dim = head_dim;
-  a.block_size = block_size;
-  a.num_blocks = num_blocks;
-  a.scale = scale;
-  a.partition_size = partition_size;
-  a.max_num_partitions = max_num_partitions;
-  a.cluster_size = 0;
-  return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)),
-                     "split-K decode launch");
+  return splitk_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, PA_FP8_E4M3,
+                     k_scale, v_scale, partition_size, max_num_partitions, workspace, workspace_bytes,
+                     stream);
 }
 
 int pa_splitk_reduce(void* out, const void* workspace, size_t workspace_bytes,

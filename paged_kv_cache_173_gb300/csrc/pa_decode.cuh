@@ -53,10 +53,11 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000;  // 2 s: a stage that takes longe
 // ================================================================ decode
 struct DecodeParams {
   // Tensor maps over the K and V pools viewed as [N*B rows][Hk][d] (3-D,
-  // innermost first: d, Hk, rows) with a 64 x 1 x 16 box, 128-byte swizzle.
+  // innermost first: d, Hk, rows) with a box of one 128-byte row segment (64
+  // bytes for 64 one-byte dims) x 1 head x 16 rows, swizzled over its width.
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
-    void* out;        // [S][H][d] of T
+  void* out;        // [S][H][d] of T
   const void* q;    // [S][H][d] of T
   const int32_t* block_tables;
   const int32_t* context_lens;
@@ -72,20 +73,34 @@ struct DecodeParams {
   int num_blocks;
   int partition_chunks;
   int max_num_partitions;
-  float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+  float scale_log2;  // scale * k_scale * log2(e): scores are kept in base-2 units
+  float out_scale;   // v_scale of an E4M3 V pool (1 otherwise)
 };
 
 // Shared-memory stage of one 16-token chunk of one KV head: TMA boxes of 16
 // rows x 64 dims (128 bytes per row, 2 KB per box), 128-byte swizzled: the
 // 16-byte unit u of row r sits at unit u ^ (r % 8).  K boxes first (dims
 // 0-63, 64-127, ...), then V boxes.
+// E4M3 caches use the same 128-byte box rows (128 dims; 64-byte rows of 64
+// dims with a 64-byte swizzle: unit u of row r at u ^ ((r / 2) % 4)).
 constexpr int BOX_DIMS = 64;
 constexpr int BOX_BYTES = CHUNK * BOX_DIMS * 2;
 
-template <int HEAD_DIM, int NT, int WARPS, int STAGES>
+// Cache element tag for E4M3 codes: one byte per element, one float scale
+// per pool.  A 16-bit cache uses the query type T itself.
+struct E4M3 {};
+template <typename KV>
+constexpr bool kIsFp8 = std::is_same<KV, E4M3>::value;
+template <typename KV>
+constexpr int kElemBytes = kIsFp8<KV> ? 1 : 2;
+
+template <int HEAD_DIM, int NT, int WARPS, int STAGES, int ELEM = 2>
 struct DecodeCfg {
-  static constexpr int DBOX = HEAD_DIM / BOX_DIMS;  // boxes per row of K (or V)
-  static constexpr int HALF_BYTES = DBOX * BOX_BYTES;
+  static constexpr int ROW_BYTES = HEAD_DIM * ELEM < 128 ? HEAD_DIM * ELEM : 128;  // bytes per box row
+  static constexpr int BOX_ELEMS = ROW_BYTES / ELEM;
+  static constexpr int BOX_B = CHUNK * ROW_BYTES;
+  static constexpr int DBOX = HEAD_DIM / BOX_ELEMS;  // boxes per row of K (or V)
+  static constexpr int HALF_BYTES = DBOX * BOX_B;
   static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
   static constexpr int RING_BYTES = WARPS * STAGES * STAGE_BYTES;
   static constexpr int GMAX = NT * 8;
@@ -137,7 +152,7 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HEAD_DIM / 16][NT][2
   for (int nt = 0; nt < NT; ++nt) {
     const int hq = nt * 8 + g;
     const bool hv = hq < G;
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
         static_cast<const uint16_t*>(q) + (static_cast<size_t>(s) * H + kvh * G + (hv ? hq : 0)) * HEAD_DIM);
 #pragma unroll
     for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
@@ -147,47 +162,46 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HEAD_DIM / 16][NT][2
   }
 }
 
-// Attend one 16-token chunk held in shared memory at `kb` (K boxes, then V
-// boxes at kb + half_bytes; 128-byte swizzle), of which the first `valid`
-// tokens belong to the sequence.  Updates the warp's running state.
-template <typename T, int HEAD_DIM, int NT>
-__device__ __forceinline__ void attend_chunk(WarpAcc<HEAD_DIM, NT>& acc,
-                                             const uint32_t (&qf)[HEAD_DIM / 16][NT][2], uint32_t kb,
-                                             uint32_t half_bytes, int valid, float sl2, int lane) {
-  constexpr int KSTEPS = HEAD_DIM / 16;
+// Query fragments for E4M3 keys: k-step ks pairs the MMA's k indices
+// {2c, 2c+1, 2c+8, 2c+9} with dims ks*16 + 4c .. 4c+3, the order in which
+// the key fragments arrive (attend_chunk_e4m3), so each lane loads four
+// consecutive dims at once.
+template <int HEAD_DIM, int NT>
+__device__ __forceinline__ void load_q_frags_e4m3(uint32_t (&qf)[HEAD_DIM / 16][NT][2], const void* q, int s,
+                                                  int H, int kvh, int G, int lane) {
   const int g = lane >> 2;
   const int c4 = lane & 3;
-  const uint32_t vb = kb + half_bytes;
-
-  // S[16 tokens][8*NT heads] = K Q^T, as two independent MMA chains (even
-  // and odd k-steps) that are added at the end
-  float sacc[NT][4], sacc2[NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hq = nt * 8 + g;
+    const bool hv = hq < G;
+    const uint2* qrow = reinterpret_cast<const uint2*>(
+        static_cast<const uint16_t*>(q) + (static_cast<size_t>(s) * H + kvh * G + (hv ? hq : 0)) * HEAD_DIM);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) sacc[nt][i] = sacc2[nt][i] = 0.f;
-  // lane supplies row (lane & 15) at 16-byte unit 2*(ks%4) + lane/16 of box ks/4
-  const uint32_t ka = kb + (lane & 15) * 128;
-  const uint32_t kx = lane & 7;
-#pragma unroll
-  for (int ks = 0; ks < KSTEPS; ++ks) {
-    uint32_t a[4];
-    const uint32_t unit = ((ks & 3) * 2 + (lane >> 4)) ^ kx;
-    ldsm_x4(a, ka + (ks >> 2) * BOX_BYTES + unit * 16);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      mma_16816<T>((ks & 1) ? sacc2[nt] : sacc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+    for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
+      const uint2 v = hv ? __ldg(qrow + ks * 4 + c4) : make_uint2(0u, 0u);
+      qf[ks][nt][0] = v.x;
+      qf[ks][nt][1] = v.y;
+    }
   }
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sacc[nt][i] += sacc2[nt][i];
+}
 
-  // online softmax (base 2); slots past the context are excluded by select
+// Online-softmax step for one 16-token chunk whose scores S[16 tokens][8*NT
+// heads] are in `sacc` (m16n8 accumulator layout: token g holds elements 0-1,
+// token g + 8 elements 2-3), of which the first `valid` tokens belong to the
+// sequence: updates the running maxima and sums, rescales the accumulators
+// when a maximum moves, and returns P^T as B fragments (bf16: also the
+// residual P - bf16(P) in `pl`).
+template <typename T, int HEAD_DIM, int NT>
+__device__ __forceinline__ void softmax_chunk(WarpAcc<HEAD_DIM, NT>& acc, const float (&sacc)[NT][4], int valid,
+                                              float sl2, int lane, uint32_t (&pb)[NT][2],
+                                              uint32_t (&pl)[NT][2]) {
+  constexpr int KSTEPS = HEAD_DIM / 16;
+  const int g = lane >> 2;
+  // base 2; slots past the context are excluded by select
   const bool v0 = g < valid;
   const bool v1 = g + 8 < valid;
-    constexpr bool kSplitP = !std::is_same<T, __half>::value;  // bf16: P = P_hi + P_lo
-  uint32_t pb[NT][2], pl[NT][2];
+  constexpr bool kSplitP = !std::is_same<T, __half>::value;  // bf16: P = P_hi + P_lo
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const float x0 = v0 ? sacc[nt][0] * sl2 : -INFINITY;
@@ -208,7 +222,7 @@ __device__ __forceinline__ void attend_chunk(WarpAcc<HEAD_DIM, NT>& acc,
     const bool grew = __any_sync(FULL_MASK, (mn0 != acc.m[nt][0]) | (mn1 != acc.m[nt][1]));
     acc.m[nt][0] = mn0;
     acc.m[nt][1] = mn1;
-        const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);  // token g
+    const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);  // token g
     const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);  // token g + 8
     const uint32_t lo = pack2<T>(p0, p1);
     const uint32_t hi = pack2<T>(p2, p3);
@@ -238,6 +252,46 @@ __device__ __forceinline__ void attend_chunk(WarpAcc<HEAD_DIM, NT>& acc,
     pb[nt][0] = movmatrix_trans(lo);  // P^T tokens 0-7 as the B fragment
     pb[nt][1] = movmatrix_trans(hi);  // P^T tokens 8-15
   }
+}
+
+// Attend one 16-token chunk held in shared memory at `kb` (K boxes, then V
+// boxes at kb + half_bytes; 128-byte swizzle), of which the first `valid`
+// tokens belong to the sequence.  Updates the warp's running state.
+template <typename T, int HEAD_DIM, int NT>
+__device__ __forceinline__ void attend_chunk(WarpAcc<HEAD_DIM, NT>& acc,
+                                             const uint32_t (&qf)[HEAD_DIM / 16][NT][2], uint32_t kb,
+                                             uint32_t half_bytes, int valid, float sl2, int lane) {
+  constexpr int KSTEPS = HEAD_DIM / 16;
+  const int c4 = lane & 3;
+  const uint32_t vb = kb + half_bytes;
+  constexpr bool kSplitP = !std::is_same<T, __half>::value;
+
+  // S[16 tokens][8*NT heads] = K Q^T, as two independent MMA chains (even
+  // and odd k-steps) that are added at the end
+  float sacc[NT][4], sacc2[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[nt][i] = sacc2[nt][i] = 0.f;
+  // lane supplies row (lane & 15) at 16-byte unit 2*(ks%4) + lane/16 of box ks/4
+  const uint32_t ka = kb + (lane & 15) * 128;
+  const uint32_t kx = lane & 7;
+#pragma unroll
+  for (int ks = 0; ks < KSTEPS; ++ks) {
+    uint32_t a[4];
+    const uint32_t unit = ((ks & 3) * 2 + (lane >> 4)) ^ kx;
+    ldsm_x4(a, ka + (ks >> 2) * BOX_BYTES + unit * 16);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      mma_16816<T>((ks & 1) ? sacc2[nt] : sacc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[nt][i] += sacc2[nt][i];
+
+  uint32_t pb[NT][2], pl[NT][2];
+  softmax_chunk<T, HEAD_DIM, NT>(acc, sacc, valid, sl2, lane, pb, pl);
 
   // O^T[d][heads] += V^T P^T; V rows past the context are zeroed by select
   const int t0 = 2 * c4;
@@ -276,6 +330,104 @@ __device__ __forceinline__ void attend_chunk(WarpAcc<HEAD_DIM, NT>& acc,
   }
 }
 
+// Byte offset of 16-byte unit `unit` of row `row` in a swizzled box of
+// ROW_BYTES-byte rows.
+template <int ROW_BYTES>
+__device__ __forceinline__ uint32_t swizzled(uint32_t row, uint32_t unit) {
+  if constexpr (ROW_BYTES == 128) {
+    return row * 128u + ((unit ^ (row & 7u)) << 4);
+  } else {
+    return row * 64u + ((unit ^ ((row >> 1) & 3u)) << 4);
+  }
+}
+
+// O^T += V^T P^T over E4M3 codes.  ldmatrix.trans of 16-bit pairs hands a
+// lane the codes of tokens 2c, 2c+1 at dims 2g, 2g+1 of a 16-dim unit; a byte
+// permute regroups them by dim, so MMA row g stands for dim 2g of the unit and
+// row g + 8 for dim 2g + 1.  MASK: tokens past `valid` are zeroed by select.
+template <int HEAD_DIM, int NT, int ROW_BYTES, bool MASK>
+__device__ __forceinline__ void pv_e4m3(WarpAcc<HEAD_DIM, NT>& acc, const uint32_t (&pb)[NT][2], uint32_t vaddr,
+                                        uint32_t tok, uint32_t uo, uint32_t mlo, uint32_t mhi) {
+  constexpr int UNITS = ROW_BYTES / 16;
+  constexpr int BOXB = CHUNK * ROW_BYTES;
+#pragma unroll
+  for (int u = 0; u < HEAD_DIM / 16; u += 2) {
+    uint32_t r[4];  // tokens 0-7 / 8-15 of unit u, then of unit u + 1
+    ldsm_x4_trans(r, vaddr + (u / UNITS) * BOXB + swizzled<ROW_BYTES>(tok, (u % UNITS) + uo));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t t07 = __byte_perm(r[2 * h], 0u, 0x3120);      // (tok 2c, 2c+1) at dim 2g | at dim 2g+1
+      const uint32_t t815 = __byte_perm(r[2 * h + 1], 0u, 0x3120);  // tokens 2c+8, 2c+9
+      uint32_t a[4] = {e4m3x2_to_half2(t07), e4m3x2_to_half2(t07 >> 16), e4m3x2_to_half2(t815),
+                       e4m3x2_to_half2(t815 >> 16)};
+      if constexpr (MASK) {
+        a[0] &= mlo;
+        a[1] &= mlo;
+        a[2] &= mhi;
+        a[3] &= mhi;
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(acc.o[u + h][nt], a, pb[nt][0], pb[nt][1]);
+    }
+  }
+}
+
+// attend_chunk for E4M3 K and V boxes (codes widened exactly to float16 in
+// registers; the pool scales are applied outside: k_scale in `sl2`, v_scale
+// to the final output).  The chunk's K boxes sit at `kb`, its V boxes at
+// kb + half_bytes.
+template <int HEAD_DIM, int NT, int ROW_BYTES>
+__device__ __forceinline__ void attend_chunk_e4m3(WarpAcc<HEAD_DIM, NT>& acc,
+                                                  const uint32_t (&qf)[HEAD_DIM / 16][NT][2], uint32_t kb,
+                                                  uint32_t half_bytes, int valid, float sl2, int lane) {
+  constexpr int UNITS = ROW_BYTES / 16;
+  constexpr int BOXB = CHUNK * ROW_BYTES;
+  const int c4 = lane & 3;
+  // lane supplies token row `tok` of unit (u + uo): the four matrices are
+  // tokens {0-7, 8-15} x units {u, u + 1}
+  const uint32_t tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+  const uint32_t uo = lane >> 4;
+
+  // S = K Q^T: a lane receives the codes of tokens g and g + 8 at dims
+  // 4c .. 4c+3 of a unit; their low pair fills k indices 2c, 2c+1 and their
+  // high pair 2c+8, 2c+9 (load_q_frags_e4m3 orders q the same way)
+  float sacc[NT][4], sacc2[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[nt][i] = sacc2[nt][i] = 0.f;
+#pragma unroll
+  for (int u = 0; u < HEAD_DIM / 16; u += 2) {
+    uint32_t r[4];
+    ldsm_x4(r, kb + (u / UNITS) * BOXB + swizzled<ROW_BYTES>(tok, (u % UNITS) + uo));
+    const uint32_t a[4] = {e4m3x2_to_half2(r[0]), e4m3x2_to_half2(r[1]), e4m3x2_to_half2(r[0] >> 16),
+                           e4m3x2_to_half2(r[1] >> 16)};
+    const uint32_t b[4] = {e4m3x2_to_half2(r[2]), e4m3x2_to_half2(r[3]), e4m3x2_to_half2(r[2] >> 16),
+                           e4m3x2_to_half2(r[3] >> 16)};
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma_f16_16816(sacc[nt], a, qf[u][nt][0], qf[u][nt][1]);
+      mma_f16_16816(sacc2[nt], b, qf[u + 1][nt][0], qf[u + 1][nt][1]);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[nt][i] += sacc2[nt][i];
+
+  uint32_t pb[NT][2], pl[NT][2];
+  softmax_chunk<__half, HEAD_DIM, NT>(acc, sacc, valid, sl2, lane, pb, pl);
+
+  const int t0 = 2 * c4;
+  const uint32_t mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+  const uint32_t mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+  if (valid == CHUNK) {
+    pv_e4m3<HEAD_DIM, NT, ROW_BYTES, false>(acc, pb, kb + half_bytes, tok, uo, mlo, mhi);
+  } else {  // the last chunk of the sequence
+    pv_e4m3<HEAD_DIM, NT, ROW_BYTES, true>(acc, pb, kb + half_bytes, tok, uo, mlo, mhi);
+  }
+}
+
 // Sum the per-lane partial running sums over the 8 row groups of the warp.
 template <int HEAD_DIM, int NT>
 __device__ __forceinline__ void reduce_warp_sums(WarpAcc<HEAD_DIM, NT>& acc) {
@@ -288,8 +440,9 @@ __device__ __forceinline__ void reduce_warp_sums(WarpAcc<HEAD_DIM, NT>& acc) {
 }
 
 // Store one warp's state in the merge area: o [GMAX][mo_pitch] floats, m and
-// l [GMAX] (call after reduce_warp_sums).
-template <int HEAD_DIM, int NT>
+// l [GMAX] (call after reduce_warp_sums).  Accumulator row r of k-step dm is
+// dim dm*16 + r, or with E4M3 values (DIM_PAIRS) dim dm*16 + 2(r % 8) + r / 8.
+template <int HEAD_DIM, int NT, bool DIM_PAIRS = false>
 __device__ __forceinline__ void store_warp_state(const WarpAcc<HEAD_DIM, NT>& acc, float* mo, float* mm,
                                                  float* ml, int mo_pitch, int lane) {
   const int g = lane >> 2;
@@ -301,7 +454,7 @@ __device__ __forceinline__ void store_warp_state(const WarpAcc<HEAD_DIM, NT>& ac
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int head = nt * 8 + 2 * c4 + (i & 1);
-        const int d = dm * 16 + g + (i >> 1) * 8;
+        const int d = DIM_PAIRS ? dm * 16 + 2 * g + (i >> 1) : dm * 16 + g + (i >> 1) * 8;
         mo[head * mo_pitch + d] = acc.o[dm][nt][i];
       }
   if (g == 0) {
@@ -321,10 +474,13 @@ __device__ __forceinline__ void store_warp_state(const WarpAcc<HEAD_DIM, NT>& ac
 // CLUSTER = true: gridDim.y CTAs form a cluster per (kvh, s); CTA `part`
 //   takes chunks [part * n / C, (part + 1) * n / C) of the sequence's n chunks
 //   and the cluster merges the C results into `out`.
-template <typename T, int HEAD_DIM, int NT, int WARPS, int STAGES, bool CLUSTER>
+// KV: the cache element type, T or E4M3.
+template <typename T, typename KV, int HEAD_DIM, int NT, int WARPS, int STAGES, bool CLUSTER>
 __global__ void __launch_bounds__(WARPS * 32)
 paged_decode_kernel(const __grid_constant__ DecodeParams p) {
-  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
+  constexpr bool FP8 = kIsFp8<KV>;
+  static_assert(!FP8 || std::is_same<T, __half>::value, "E4M3 caches take float16 queries");
+  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES, kElemBytes<KV>>;
   constexpr int KSTEPS = HEAD_DIM / 16;
   constexpr int GMAX = Cfg::GMAX;
 
@@ -365,7 +521,11 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int nk_cap = first < cmax ? (cmax - first + WARPS - 1) / WARPS : 0;
 
   uint32_t qf[KSTEPS][NT][2];
-  load_q_frags<HEAD_DIM, NT>(qf, p.q, s, H, kvh, G, lane);
+  if constexpr (FP8) {
+    load_q_frags_e4m3<HEAD_DIM, NT>(qf, p.q, s, H, kvh, G, lane);
+  } else {
+    load_q_frags<HEAD_DIM, NT>(qf, p.q, s, H, kvh, G, lane);
+  }
 
   // ---- block-table window: lane j holds the physical block of this warp's
   //      chunk (kbase + j); the next window is fetched 32 chunks ahead.  Only
@@ -393,7 +553,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   if (nchunks == 0) {
     // Empty sequence -> zeros; impossible context length -> NaN.  Written once.
     if (part == 0) {
-            const T v = to_elem<T>(ctx_bad ? NAN : 0.f);
+      const T v = to_elem<T>(ctx_bad ? NAN : 0.f);
       T* o = static_cast<T*>(p.out) + (static_cast<size_t>(s) * H + kvh * G) * HEAD_DIM;
       for (int i = threadIdx.x; i < G * HEAD_DIM; i += WARPS * 32) o[i] = v;
     }
@@ -431,8 +591,8 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_arrive_expect_tx(&wbar[slot], Cfg::STAGE_BYTES);
 #pragma unroll
       for (int b = 0; b < Cfg::DBOX; ++b) {
-        tma_load_3d(dst + b * BOX_BYTES, &p.tmap_k, b * BOX_DIMS, kvh, y, &wbar[slot]);
-        tma_load_3d(dst + Cfg::HALF_BYTES + b * BOX_BYTES, &p.tmap_v, b * BOX_DIMS, kvh, y, &wbar[slot]);
+        tma_load_3d(dst + b * Cfg::BOX_B, &p.tmap_k, b * Cfg::BOX_ELEMS, kvh, y, &wbar[slot]);
+        tma_load_3d(dst + Cfg::HALF_BYTES + b * Cfg::BOX_B, &p.tmap_v, b * Cfg::BOX_ELEMS, kvh, y, &wbar[slot]);
       }
     }
     ++issued;
@@ -458,8 +618,12 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     }
     const int ch = first + k * WARPS;
     const int valid = min(CHUNK, ctx - ch * CHUNK);
-    attend_chunk<T, HEAD_DIM, NT>(acc, qf, smem_addr(wring + slot * Cfg::STAGE_BYTES), Cfg::HALF_BYTES, valid,
-                               sl2, lane);
+    const uint32_t stage = smem_addr(wring + slot * Cfg::STAGE_BYTES);
+    if constexpr (FP8) {
+      attend_chunk_e4m3<HEAD_DIM, NT, Cfg::ROW_BYTES>(acc, qf, stage, Cfg::HALF_BYTES, valid, sl2, lane);
+    } else {
+      attend_chunk<T, HEAD_DIM, NT>(acc, qf, stage, Cfg::HALF_BYTES, valid, sl2, lane);
+    }
 
     fence_proxy_async_smem();  // this lane's reads of the slot precede the refill's writes
     __syncwarp();
@@ -480,8 +644,8 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   float* mm = mo + WARPS * GMAX * Cfg::MO_PITCH;
   float* ml = mm + WARPS * GMAX;
   int* mbad = reinterpret_cast<int*>(ml + WARPS * GMAX);
-  store_warp_state<HEAD_DIM, NT>(acc, mo + warp * GMAX * Cfg::MO_PITCH, mm + warp * GMAX, ml + warp * GMAX,
-                                 Cfg::MO_PITCH, lane);
+  store_warp_state<HEAD_DIM, NT, FP8>(acc, mo + warp * GMAX * Cfg::MO_PITCH, mm + warp * GMAX, ml + warp * GMAX,
+                                      Cfg::MO_PITCH, lane);
   if (lane == 0) mbad[warp] = bad ? 1 : 0;
   __syncthreads();
 
@@ -504,7 +668,8 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
         O += mo[(w * GMAX + head) * Cfg::MO_PITCH + d] * f;
       }
     }
-    const float r = any_bad ? NAN : (L > 0.f ? O / L : 0.f);
+    float r = any_bad ? NAN : (L > 0.f ? O / L : 0.f);
+    if constexpr (FP8) r *= p.out_scale;  // V codes times v_scale
     const size_t qrow = static_cast<size_t>(s) * H + kvh * G + head;
     if (CLUSTER) {
       // an empty CTA publishes m = -inf, l = 0: weight 0 in the cluster merge
@@ -744,7 +909,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   } else {
     if (!active) return;
   }
-    store_vec<T, VEC>(static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.num_heads + h) * HEAD_DIM + lane * VEC,
+  store_vec<T, VEC>(static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.num_heads + h) * HEAD_DIM + lane * VEC,
                     acc, 1.f / Lw);
 }
 
@@ -772,27 +937,33 @@ inline cudaError_t encode_fn(EncodeTiledFn* out) {
   return cudaSuccess;
 }
 
-template <typename T>
+template <typename KV>
 constexpr CUtensorMapDataType tma_dtype() {
-  return std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return kIsFp8<KV> ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                    : (std::is_same<KV, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
-// A KV pool [N][B][Hk][d] seen as rows x heads x dims, boxes of 16 rows x 1
-// head x 64 dims, 128-byte swizzled.
-template <typename T>
-cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int head_dim, int num_kv_heads, int64_t rows) {
+// A KV pool [N][B][Hk][d] of KV elements seen as rows x heads x dims, boxes
+// of 16 rows x 1 head x one box row (128 bytes; 64 for 64 one-byte dims),
+// swizzled over the box row's width.
+template <typename KV, int HEAD_DIM>
+cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int num_kv_heads, int64_t rows) {
+  using Cfg = DecodeCfg<HEAD_DIM, 1, 1, 1, kElemBytes<KV>>;
   EncodeTiledFn enc = nullptr;
   cudaError_t e = encode_fn(&enc);
   if (e != cudaSuccess) return e;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
+  constexpr int ELEM = kElemBytes<KV>;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HEAD_DIM), static_cast<cuuint64_t>(num_kv_heads),
                               static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
-                                 static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
-  const cuuint32_t box[3] = {BOX_DIMS, 1, CHUNK};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(HEAD_DIM) * ELEM,
+                                 static_cast<cuuint64_t>(num_kv_heads) * HEAD_DIM * ELEM};
+  const cuuint32_t box[3] = {Cfg::BOX_ELEMS, 1, CHUNK};
   const cuuint32_t estride[3] = {1, 1, 1};
-  const CUresult r = enc(map, tma_dtype<T>(), 3, const_cast<void*>(pool), dims, strides, box, estride,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUtensorMapSwizzle swz = Cfg::ROW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUresult r = enc(map, tma_dtype<KV>(), 3, const_cast<void*>(pool), dims, strides, box, estride,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -815,22 +986,28 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
 #define PA_DECODE_STAGES 2
 #endif
 
+#ifndef PA_DECODE_FP8_STAGES
+#define PA_DECODE_FP8_STAGES 4
+#endif
+
 // CTA shape per head size: 4 warps x 2 stages (8 KB stages up to d = 128,
 // three CTAs per SM); d = 256 has 16 KB stages and uses 2 warps x 2 stages
-// to keep three CTAs per SM.
-template <int HEAD_DIM>
+// to keep three CTAs per SM.  E4M3 stages are half as large: 4 warps x 4
+// stages keep the same bytes in flight (2 stages for d = 256).
+template <int HEAD_DIM, int ELEM = 2>
 struct DecodeShape {
-  static constexpr int WARPS = HEAD_DIM > 128 ? 2 : PA_DECODE_WARPS;
-  static constexpr int STAGES = HEAD_DIM > 128 ? 2 : PA_DECODE_STAGES;
+  static constexpr int WARPS = ELEM == 1 ? 4 : (HEAD_DIM > 128 ? 2 : PA_DECODE_WARPS);
+  static constexpr int STAGES = ELEM == 1 ? (HEAD_DIM > 128 ? 2 : PA_DECODE_FP8_STAGES)
+                                          : (HEAD_DIM > 128 ? 2 : PA_DECODE_STAGES);
 };
 
-template <typename T, int HEAD_DIM>
+template <typename T, typename KV, int HEAD_DIM>
 cudaError_t fill_decode_params(const DecodeArgs& a, DecodeParams* pp) {
   DecodeParams& p = *pp;
   const int64_t pool_rows = static_cast<int64_t>(a.num_blocks) * a.block_size;
-  cudaError_t e = make_pool_map<T>(&p.tmap_k, a.k_cache, HEAD_DIM, a.num_kv_heads, pool_rows);
+  cudaError_t e = make_pool_map<KV, HEAD_DIM>(&p.tmap_k, a.k_cache, a.num_kv_heads, pool_rows);
   if (e != cudaSuccess) return e;
-  e = make_pool_map<T>(&p.tmap_v, a.v_cache, HEAD_DIM, a.num_kv_heads, pool_rows);
+  e = make_pool_map<KV, HEAD_DIM>(&p.tmap_v, a.v_cache, a.num_kv_heads, pool_rows);
   if (e != cudaSuccess) return e;
   p.out = a.out;
   p.q = a.q;
@@ -849,21 +1026,24 @@ cudaError_t fill_decode_params(const DecodeArgs& a, DecodeParams* pp) {
   p.num_blocks = a.num_blocks;
   p.partition_chunks = a.partition_size / CHUNK;
   p.max_num_partitions = a.max_num_partitions;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
+  const bool fp8 = kIsFp8<KV>;
+  p.scale_log2 = a.scale * (fp8 ? a.k_scale : 1.f) * 1.4426950408889634f;
+  p.out_scale = fp8 ? a.v_scale : 1.f;
   return cudaSuccess;
 }
 
-template <typename T, int HEAD_DIM, int NT, bool CLUSTER>
+template <typename T, typename KV, int HEAD_DIM, int NT, bool CLUSTER>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
-  constexpr int WARPS = DecodeShape<HEAD_DIM>::WARPS;
-  constexpr int STAGES = DecodeShape<HEAD_DIM>::STAGES;
-  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
-  auto kern = paged_decode_kernel<T, HEAD_DIM, NT, WARPS, STAGES, CLUSTER>;
+  constexpr int ELEM = kElemBytes<KV>;
+  constexpr int WARPS = DecodeShape<HEAD_DIM, ELEM>::WARPS;
+  constexpr int STAGES = DecodeShape<HEAD_DIM, ELEM>::STAGES;
+  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES, ELEM>;
+  auto kern = paged_decode_kernel<T, KV, HEAD_DIM, NT, WARPS, STAGES, CLUSTER>;
   static std::atomic<uint64_t> smem_set{0};
   cudaError_t e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return e;
   DecodeParams p;
-  e = fill_decode_params<T, HEAD_DIM>(a, &p);
+  e = fill_decode_params<T, KV, HEAD_DIM>(a, &p);
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_kv_heads, CLUSTER ? a.cluster_size : a.max_num_partitions, a.num_seqs);
   cudaLaunchConfig_t cfg = {};
@@ -890,11 +1070,12 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
 
 // Resident decode CTAs the device holds at once (SMs x CTAs per SM), cached
 // per device.
-template <typename T, int HEAD_DIM, int NT>
+template <typename T, typename KV, int HEAD_DIM, int NT>
 cudaError_t decode_slots(int* slots) {
-  constexpr int WARPS = DecodeShape<HEAD_DIM>::WARPS;
-  constexpr int STAGES = DecodeShape<HEAD_DIM>::STAGES;
-  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES>;
+  constexpr int ELEM = kElemBytes<KV>;
+  constexpr int WARPS = DecodeShape<HEAD_DIM, ELEM>::WARPS;
+  constexpr int STAGES = DecodeShape<HEAD_DIM, ELEM>::STAGES;
+  using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES, ELEM>;
   static std::atomic<int> cache[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -906,7 +1087,7 @@ cudaError_t decode_slots(int* slots) {
       return cudaSuccess;
     }
   }
-  auto kern = paged_decode_kernel<T, HEAD_DIM, NT, WARPS, STAGES, false>;
+  auto kern = paged_decode_kernel<T, KV, HEAD_DIM, NT, WARPS, STAGES, false>;
   static std::atomic<uint64_t> smem_set{0};
   e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return e;
@@ -924,14 +1105,14 @@ cudaError_t decode_slots(int* slots) {
 // Single-launch decode: one CTA per (sequence, KV head) when those fill the
 // resident slots; otherwise a cluster of up to 8 CTAs per pair, each with at
 // least 512 tokens of capacity.  Split-K (a workspace given): the plain grid.
-template <typename T, int HEAD_DIM, int NT>
+template <typename T, typename KV, int HEAD_DIM, int NT>
 cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
   if (a.cluster_size >= 0) {
-    return a.cluster_size > 0 ? launch_decode_t<T, HEAD_DIM, NT, true>(a, stream)
-                              : launch_decode_t<T, HEAD_DIM, NT, false>(a, stream);
+    return a.cluster_size > 0 ? launch_decode_t<T, KV, HEAD_DIM, NT, true>(a, stream)
+                              : launch_decode_t<T, KV, HEAD_DIM, NT, false>(a, stream);
   }
   int slots = 0;
-  cudaError_t e = decode_slots<T, HEAD_DIM, NT>(&slots);
+  cudaError_t e = decode_slots<T, KV, HEAD_DIM, NT>(&slots);
   if (e != cudaSuccess) return e;
   const int64_t pairs = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
   int64_t k = pairs > 0 ? slots / pairs : 1;
@@ -941,9 +1122,9 @@ cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
   b.cluster_size = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(8, k)));
   if (b.cluster_size == 1) {
     b.cluster_size = 0;
-    return launch_decode_t<T, HEAD_DIM, NT, false>(b, stream);
+    return launch_decode_t<T, KV, HEAD_DIM, NT, false>(b, stream);
   }
-  return launch_decode_t<T, HEAD_DIM, NT, true>(b, stream);
+  return launch_decode_t<T, KV, HEAD_DIM, NT, true>(b, stream);
 }
 
 template <typename T, int HEAD_DIM>
@@ -982,15 +1163,18 @@ cudaError_t launch_reduce_t(const ReduceArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// Entry points used by the per-dtype translation units.
-template <typename T>
+// Entry points used by the per-dtype translation units (KV = T for 16-bit
+// caches, E4M3 for one-byte caches).
+template <typename T, typename KV = T>
 cudaError_t launch_decode_typed(const DecodeArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
   const bool two = a.num_heads / a.num_kv_heads > 8;
   switch (a.head_dim) {
-    case 64: return two ? launch_decode_auto<T, 64, 2>(a, stream) : launch_decode_auto<T, 64, 1>(a, stream);
-    case 128: return two ? launch_decode_auto<T, 128, 2>(a, stream) : launch_decode_auto<T, 128, 1>(a, stream);
-    case 256: return two ? cudaErrorInvalidValue : launch_decode_auto<T, 256, 1>(a, stream);
+    case 64:
+      return two ? launch_decode_auto<T, KV, 64, 2>(a, stream) : launch_decode_auto<T, KV, 64, 1>(a, stream);
+    case 128:
+      return two ? launch_decode_auto<T, KV, 128, 2>(a, stream) : launch_decode_auto<T, KV, 128, 1>(a, stream);
+    case 256: return two ? cudaErrorInvalidValue : launch_decode_auto<T, KV, 256, 1>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -5,6 +5,13 @@
 //                             ("vLLM PagedAttention source walk-through",
 //                             section 3.2: append_token writes the token's KV
 //                             at block_table[pos / B], offset pos % B)
+//  reshape_and_cache_e4m3_kernel
+//                             the same into E4M3 caches: each element is
+//                             stored as the code nearest to x / scale ("when
+//                             the KV cache meets OS paging", section 6:
+//                             compression inside the block)
+//  copy_blocks_kernel         whole-block copies, the copy step of
+//                             copy-on-write
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -45,6 +52,54 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_con
   const uint4* src = (is_v ? p.value : p.key) + (static_cast<int64_t>(t) * p.num_kv_heads + h) * p.row_vecs;
   uint4* dst = (is_v ? p.v_cache : p.k_cache) + (slot * p.num_kv_heads + h) * p.row_vecs;
   for (int i = lane & 15; i < p.row_vecs; i += 16) dst[i] = __ldg(src + i);
+}
+
+// ======================================================= reshape_and_cache, E4M3
+struct ReshapeE4m3Params {
+  const uint4* key;  // 8 elements of 16 bits per vector
+  const uint4* value;
+  uint2* k_cache;    // 8 codes per vector
+  uint2* v_cache;
+  const int64_t* slot_mapping;
+  int64_t num_slots;
+  int num_tokens;
+  int num_kv_heads;
+  int row_vecs;  // head_dim / 8
+  float k_scale;
+  float v_scale;
+};
+
+// One warp per (token, KV head), lanes 0-15 on K and 16-31 on V: each lane
+// turns 8 elements (16 bytes) into 8 codes (8 bytes) per step.  The quotient
+// x / scale is rounded once to float32 (IEEE division), then to E4M3.
+template <typename T>
+__global__ void __launch_bounds__(256) reshape_and_cache_e4m3_kernel(const __grid_constant__ ReshapeE4m3Params p) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.num_tokens * p.num_kv_heads) return;
+  const int t = wid / p.num_kv_heads;
+  const int h = wid - t * p.num_kv_heads;
+  const int64_t slot = __ldg(p.slot_mapping + t);
+  if (slot < 0 || slot >= p.num_slots) return;  // padding, or out of the pool
+  const bool is_v = lane >= 16;
+  const float sc = is_v ? p.v_scale : p.k_scale;
+  const uint4* src = (is_v ? p.value : p.key) + (static_cast<int64_t>(t) * p.num_kv_heads + h) * p.row_vecs;
+  uint2* dst = (is_v ? p.v_cache : p.k_cache) + (slot * p.num_kv_heads + h) * p.row_vecs;
+  for (int i = lane & 15; i < p.row_vecs; i += 16) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = unpack2<T>(w[j]);
+      const uint32_t c0 = float_to_e4m3_sat(__fdiv_rn(f.x, sc));
+      const uint32_t c1 = float_to_e4m3_sat(__fdiv_rn(f.y, sc));
+      o[j >> 1] |= (c0 | (c1 << 8)) << ((j & 1) * 16);
+    }
+    dst[i] = make_uint2(o[0], o[1]);
+  }
 }
 
 // ================================================================ copy_blocks
@@ -98,8 +153,42 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+namespace {
+
+cudaError_t launch_reshape_e4m3(const ReshapeArgs& a, cudaStream_t stream) {
+  ReshapeE4m3Params p;
+  p.key = static_cast<const uint4*>(a.key);
+  p.value = static_cast<const uint4*>(a.value);
+  p.k_cache = static_cast<uint2*>(a.k_cache);
+  p.v_cache = static_cast<uint2*>(a.v_cache);
+  p.slot_mapping = a.slot_mapping;
+  p.num_slots = static_cast<int64_t>(a.num_blocks) * a.block_size;
+  p.num_tokens = a.num_tokens;
+  p.num_kv_heads = a.num_kv_heads;
+  p.row_vecs = a.head_dim / 8;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  const int64_t warps = static_cast<int64_t>(a.num_tokens) * a.num_kv_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((warps + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = a.dtype == PA_BF16 ? cudaLaunchKernelEx(&cfg, reshape_and_cache_e4m3_kernel<__nv_bfloat16>, p)
+                                     : cudaLaunchKernelEx(&cfg, reshape_and_cache_e4m3_kernel<__half>, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;
+  if (a.kv_dtype == PA_FP8_E4M3) return launch_reshape_e4m3(a, stream);
   ReshapeParams p;
   p.key = static_cast<const uint4*>(a.key);
   p.value = static_cast<const uint4*>(a.value);
@@ -127,6 +216,7 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) 
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.kv_dtype == PA_FP8_E4M3) return launch_decode_f16_e4m3(a, stream);
   return a.dtype == PA_BF16 ? launch_decode_bf16(a, stream) : launch_decode_f16(a, stream);
 }
 

@@ -19,6 +19,10 @@ struct ReshapeArgs {
   int block_size;
   int num_kv_heads;
   int head_dim;
+  int dtype;      // key / value: PA_FP16 or PA_BF16
+  int kv_dtype;   // the caches: dtype (a plain copy) or PA_FP8_E4M3
+  float k_scale;  // E4M3 caches: the stored code is the one nearest to x / scale
+  float v_scale;
 };
 
 struct CopyBlocksArgs {
@@ -31,7 +35,10 @@ struct CopyBlocksArgs {
 };
 
 struct DecodeArgs {
-  int dtype;  // PA_FP16 or PA_BF16
+  int dtype;     // q and out: PA_FP16 or PA_BF16
+  int kv_dtype;  // the caches: dtype, or PA_FP8_E4M3 (values = code * k_scale / v_scale)
+  float k_scale;
+  float v_scale;
   void* out;
   const void* q;
   const void* k_cache;
@@ -80,6 +87,8 @@ cudaError_t launch_decode_f16(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_splitk_reduce_f16(const ReduceArgs& a, cudaStream_t stream);
 cudaError_t launch_splitk_reduce_bf16(const ReduceArgs& a, cudaStream_t stream);
+// E4M3 caches with float16 queries (pa_decode_fp8.cu)
+cudaError_t launch_decode_f16_e4m3(const DecodeArgs& a, cudaStream_t stream);
 
 // Workspace geometry shared by the partition kernel and the reduce kernel:
 // o [S][H][P][d], then m [S][H][P], then l [S][H][P], float32.

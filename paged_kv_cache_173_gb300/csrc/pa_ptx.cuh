@@ -6,6 +6,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include <type_traits>
@@ -225,6 +226,21 @@ __device__ __forceinline__ T to_elem(float x) {
   } else {
     return __float2bfloat16_rn(x);
   }
+}
+
+// ---------------------------------------------------------------- E4M3 codes
+// Two E4M3 codes (bits 0-7 and 8-15 of x) widened to a packed float16 pair
+// (low half from bits 0-7).  Every E4M3 value, NaN included, is exact in
+// float16, so this loses nothing.
+__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t x) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x & 0xffffu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// The E4M3 code nearest to x (ties to even); finite values beyond 448 and
+// infinities saturate to +-448, NaN stays NaN.
+__device__ __forceinline__ uint8_t float_to_e4m3_sat(float x) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
 }
 
 }  // namespace pa

@@ -124,3 +124,49 @@ def test_reduce_rejects_bad_arguments(L):
 ])
 def test_reshape_rejects_bad_arguments(L, args, status):
     assert L.pa_reshape_and_cache(*args) == status
+
+
+def _decode_fp8(L, splitk=False, **kw):
+    args = dict(S=2, H=8, Hk=2, d=128, B=16, dtype=0, ks=0.03125, vs=0.03125, q=A)
+    args.update(kw)
+    head = (A, args["q"], A, A, A, 8, A, args["S"], args["H"], args["Hk"], args["d"], args["B"], 32, 0.1,
+            args["dtype"], args["ks"], args["vs"])
+    if splitk:
+        return L.pa_decode_splitk_fp8(*head, 64, 2, A, 10 ** 9, None)
+    return L.pa_decode_fp8(*head, None)
+
+
+@pytest.mark.parametrize("splitk", [False, True])
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=1), _lib.PA_ERR_UNSUPPORTED),          # E4M3 caches take float16 queries
+    (dict(dtype=2), _lib.PA_ERR_UNSUPPORTED),
+    (dict(ks=0.0), _lib.PA_ERR_INVALID_ARG),
+    (dict(vs=-1.0), _lib.PA_ERR_INVALID_ARG),
+    (dict(ks=float("inf")), _lib.PA_ERR_INVALID_ARG),
+    (dict(vs=float("nan")), _lib.PA_ERR_INVALID_ARG),
+    (dict(d=96), _lib.PA_ERR_UNSUPPORTED),
+    (dict(B=8), _lib.PA_ERR_UNSUPPORTED),
+    (dict(q=None), _lib.PA_ERR_INVALID_ARG),
+    (dict(S=0, q=None), _lib.PA_OK),
+])
+def test_fp8_decode_checks_arguments(L, splitk, kw, status):
+    assert _decode_fp8(L, splitk=splitk, **kw) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, A, A, A, A, 4, 8, 16, 2, 40, 0, 1.0, 1.0, None), _lib.PA_ERR_UNSUPPORTED),   # head_dim % 16
+    ((A, A, A, A, A, 4, 8, 16, 2, 128, 2, 1.0, 1.0, None), _lib.PA_ERR_UNSUPPORTED),  # key dtype
+    ((A, A, A, A, A, 4, 8, 16, 2, 128, 0, 0.0, 1.0, None), _lib.PA_ERR_INVALID_ARG),
+    ((A, A, A, A, A, 4, 8, 16, 2, 128, 0, 1.0, float("inf"), None), _lib.PA_ERR_INVALID_ARG),
+    ((A, A, A + 8, A, A, 4, 8, 16, 2, 128, 0, 1.0, 1.0, None), _lib.PA_ERR_INVALID_ARG),
+    ((A, A, A, A, A, 0, 8, 16, 2, 128, 1, 1.0, 1.0, None), _lib.PA_OK),              # empty
+])
+def test_fp8_reshape_checks_arguments(L, args, status):
+    assert L.pa_reshape_and_cache_fp8(*args) == status
+
+
+def test_copy_blocks_accepts_one_byte_caches(L):
+    assert L.pa_copy_blocks(A, A, A, 0, 8, 16, 2, 128, _lib.PA_FP8_E4M3, None) == _lib.PA_OK
+    assert L.pa_copy_blocks(A, A, A, 0, 8, 16, 2, 128, 3, None) == _lib.PA_ERR_UNSUPPORTED
+    # 1-byte elements: 16 * 1 * 8 = 128 bytes per block, a multiple of 16
+    assert L.pa_copy_blocks(A, A, A, 0, 8, 16, 1, 8, _lib.PA_FP8_E4M3, None) == _lib.PA_OK

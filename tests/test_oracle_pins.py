@@ -608,3 +608,14 @@ def test_fp8_cache_write_and_decode_equal_library_attention_on_dequantised_value
         vs = np.stack([deq(vc[b.block_tables[s, t // 16], t % 16]) for t in range(c)]) * b.v_scale
         ref = _sdpa_contiguous(b.q[s], ks, vs, b.scale, b.group_size)
         np.testing.assert_allclose(got[s], ref, rtol=0, atol=1e-12)
+
+
+def test_copy_blocks_of_one_byte_pools_matches_the_numpy_statement():
+    rng = np.random.default_rng(17)
+    k = rng.integers(0, 256, (6, 16, 2, 64), dtype=np.uint8)
+    v = rng.integers(0, 256, (6, 16, 2, 64), dtype=np.uint8)
+    m = np.array([[0, 3], [2, 5], [4, 4]])
+    got = c_oracle.copy_blocks(k, v, m)
+    want = numpy_oracle.copy_blocks(k, v, m)
+    assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1])
+    assert np.array_equal(got[0][3], k[0]) and np.array_equal(got[1][5], v[2])

@@ -356,10 +356,9 @@ __device__ __forceinline__ void pv_e4m3(WarpAcc<HEAD_DIM, NT>& acc, const uint32
     ldsm_x4_trans(r, vaddr + (u / UNITS) * BOXB + swizzled<ROW_BYTES>(tok, (u % UNITS) + uo));
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint32_t t07 = __byte_perm(r[2 * h], 0u, 0x3120);      // (tok 2c, 2c+1) at dim 2g | at dim 2g+1
-      const uint32_t t815 = __byte_perm(r[2 * h + 1], 0u, 0x3120);  // tokens 2c+8, 2c+9
-      uint32_t a[4] = {e4m3x2_to_half2(t07), e4m3x2_to_half2(t07 >> 16), e4m3x2_to_half2(t815),
-                       e4m3x2_to_half2(t815 >> 16)};
+      uint32_t a[4];  // (tok 2c, 2c+1) at dim 2g, at dim 2g+1; then tokens 2c+8, 2c+9
+      e4m3x4_to_half2x2(__byte_perm(r[2 * h], 0u, 0x3120), a[0], a[1]);
+      e4m3x4_to_half2x2(__byte_perm(r[2 * h + 1], 0u, 0x3120), a[2], a[3]);
       if constexpr (MASK) {
         a[0] &= mlo;
         a[1] &= mlo;
@@ -400,10 +399,11 @@ __device__ __forceinline__ void attend_chunk_e4m3(WarpAcc<HEAD_DIM, NT>& acc,
   for (int u = 0; u < HEAD_DIM / 16; u += 2) {
     uint32_t r[4];
     ldsm_x4(r, kb + (u / UNITS) * BOXB + swizzled<ROW_BYTES>(tok, (u % UNITS) + uo));
-    const uint32_t a[4] = {e4m3x2_to_half2(r[0]), e4m3x2_to_half2(r[1]), e4m3x2_to_half2(r[0] >> 16),
-                           e4m3x2_to_half2(r[1] >> 16)};
-    const uint32_t b[4] = {e4m3x2_to_half2(r[2]), e4m3x2_to_half2(r[3]), e4m3x2_to_half2(r[2] >> 16),
-                           e4m3x2_to_half2(r[3] >> 16)};
+    uint32_t a[4], b[4];  // k-step u from r[0], r[1]; k-step u + 1 from r[2], r[3]
+    e4m3x4_to_half2x2(r[0], a[0], a[2]);
+    e4m3x4_to_half2x2(r[1], a[1], a[3]);
+    e4m3x4_to_half2x2(r[2], b[0], b[2]);
+    e4m3x4_to_half2x2(r[3], b[1], b[3]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       mma_f16_16816(sacc[nt], a, qf[u][nt][0], qf[u][nt][1]);
@@ -986,17 +986,21 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
 #define PA_DECODE_STAGES 2
 #endif
 
+#ifndef PA_DECODE_FP8_WARPS
+#define PA_DECODE_FP8_WARPS 4
+#endif
 #ifndef PA_DECODE_FP8_STAGES
-#define PA_DECODE_FP8_STAGES 4
+#define PA_DECODE_FP8_STAGES 2
 #endif
 
 // CTA shape per head size: 4 warps x 2 stages (8 KB stages up to d = 128,
 // three CTAs per SM); d = 256 has 16 KB stages and uses 2 warps x 2 stages
-// to keep three CTAs per SM.  E4M3 stages are half as large: 4 warps x 4
-// stages keep the same bytes in flight (2 stages for d = 256).
+// to keep three CTAs per SM.  E4M3 stages are half as large: 4 warps x 2
+// stages fit five CTAs per SM (registers), which measured faster than
+// keeping the 16-bit kernel's bytes in flight with 4 stages.
 template <int HEAD_DIM, int ELEM = 2>
 struct DecodeShape {
-  static constexpr int WARPS = ELEM == 1 ? 4 : (HEAD_DIM > 128 ? 2 : PA_DECODE_WARPS);
+  static constexpr int WARPS = ELEM == 1 ? PA_DECODE_FP8_WARPS : (HEAD_DIM > 128 ? 2 : PA_DECODE_WARPS);
   static constexpr int STAGES = ELEM == 1 ? (HEAD_DIM > 128 ? 2 : PA_DECODE_FP8_STAGES)
                                           : (HEAD_DIM > 128 ? 2 : PA_DECODE_STAGES);
 };

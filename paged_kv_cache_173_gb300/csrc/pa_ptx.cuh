@@ -229,12 +229,15 @@ __device__ __forceinline__ T to_elem(float x) {
 }
 
 // ---------------------------------------------------------------- E4M3 codes
-// Two E4M3 codes (bits 0-7 and 8-15 of x) widened to a packed float16 pair
-// (low half from bits 0-7).  Every E4M3 value, NaN included, is exact in
-// float16, so this loses nothing.
-__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t x) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x & 0xffffu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four E4M3 codes (bytes 0-3 of x) widened to two packed float16 pairs:
+// lo = (byte 0, byte 1), hi = (byte 2, byte 3), the lower byte in the lower
+// half.  The register's halves feed the conversions directly.  Every E4M3
+// value, NaN included, is exact in float16, so this loses nothing.
+__device__ __forceinline__ void e4m3x4_to_half2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
 }
 
 // The E4M3 code nearest to x (ties to even); finite values beyond 448 and

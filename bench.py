@@ -47,9 +47,9 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.md")
 
 
 # ----------------------------------------------------------------- workload
-def make_workload(name: str, seed: int, partition_size: int, dtype: str = "fp16"):
+def make_workload(name: str, seed: int, partition_size: int, dtype: str = "fp16", kv_dtype: str = ""):
     from paged_kv_cache_173_gb300 import workloads
-    kw = dict(seed=seed, poison=False, partition_size=partition_size, dtype=dtype)
+    kw = dict(seed=seed, poison=False, partition_size=partition_size, dtype=dtype, kv_dtype=kv_dtype)
     if name == "llama3-8b":
         b = workloads.llama3_8b(**kw)
         desc = ("llama3-8b decode layer: S=64, H=32, Hk=8, d=128, B=16, ctx~U[128,2048], "
@@ -74,7 +74,33 @@ def make_workload(name: str, seed: int, partition_size: int, dtype: str = "fp16"
         raise SystemExit(f"unknown workload {name}")
     if dtype != "fp16":
         desc += f", {dtype}"
+    if kv_dtype == "fp8":
+        desc += f", E4M3 KV cache (k_scale = v_scale = {b.k_scale:g})"
     return b, desc
+
+
+def workload_key(args) -> str:
+    """Name of the workload and element types, as the traffic records key it."""
+    key = args.workload
+    if args.dtype != "fp16":
+        key += f"-{args.dtype}"
+    if args.kv_dtype == "fp8":
+        key += "-fp8kv"
+    return key
+
+
+def kv_ops(api, b):
+    """The cache write, decode and split-K calls for the batch's cache type."""
+    if b.kv_dtype == "fp8":
+        ks, vs = b.k_scale, b.v_scale
+        return (lambda key, value, kc, vc, sm: api.pa_reshape_and_cache_fp8(key, value, kc, vc, sm, ks, vs),
+                lambda out, q, kc, vc, bt, cl: api.pa_decode_fp8(out, q, kc, vc, bt, cl, b.scale, ks, vs),
+                lambda out, q, kc, vc, bt, cl, ps, ws, P: api.pa_decode_splitk_fp8(
+                    out, q, kc, vc, bt, cl, b.scale, ks, vs, ps, ws, P))
+    return (api.pa_reshape_and_cache,
+            lambda out, q, kc, vc, bt, cl: api.pa_decode(out, q, kc, vc, bt, cl, b.scale),
+            lambda out, q, kc, vc, bt, cl, ps, ws, P: api.pa_decode_splitk(out, q, kc, vc, bt, cl, b.scale,
+                                                                           ps, ws, P))
 
 
 def to_device(a: np.ndarray, dtype: str, dev):
@@ -301,8 +327,9 @@ def run_gpu(args, rank: int, world: int):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    b, desc = make_workload(args.workload, args.seed + rank, args.partition_size, args.dtype)
+    b, desc = make_workload(args.workload, args.seed + rank, args.partition_size, args.dtype, args.kv_dtype)
     kv_bytes = workloads.algorithmic_kv_bytes(b)
+    write_kv, decode_kv, splitk_kv = kv_ops(api, b)
     ps = b.partition_size
     P = api.max_num_partitions_for(b.max_blocks_per_seq, b.block_size, ps)
 
@@ -322,15 +349,15 @@ def run_gpu(args, rank: int, world: int):
 
     def reshape(r):
         kc, vc, _ = reps[r % R]
-        api.pa_reshape_and_cache(key, value, kc, vc, sm)
+        write_kv(key, value, kc, vc, sm)
 
     def decode(r):
         kc, vc, q = reps[r % R]
-        api.pa_decode(out, q, kc, vc, bt, cl, b.scale)
+        decode_kv(out, q, kc, vc, bt, cl)
 
     def decode_splitk(r):
         kc, vc, q = reps[r % R]
-        api.pa_decode_splitk(out, q, kc, vc, bt, cl, b.scale, ps, ws, P)
+        splitk_kv(out, q, kc, vc, bt, cl, ps, ws, P)
 
     def reduce(r):
         api.pa_splitk_reduce(out, ws, cl, M, B, ps, P)
@@ -365,7 +392,7 @@ def run_gpu(args, rank: int, world: int):
     value = whole_job_gbs(kv_bytes, K, world, ms)
     step_ms = ms / K
     achieved = kv_bytes / (t_decode * 1e-3) / 1e9
-    traffic = load_traffic(args.workload, decode_name)
+    traffic = load_traffic(workload_key(args), decode_name)
     res = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -381,6 +408,7 @@ def run_gpu(args, rank: int, world: int):
         "data": "synthetic",
         "config": {
             "workload": desc,
+            "kv_cache": "e4m3, one float scale per pool" if b.kv_dtype == "fp8" else b.dtype,
             "kv_bytes_per_step": kv_bytes,
             "path": best,
             "step": " -> ".join(n for n, _ in kern),
@@ -430,17 +458,17 @@ def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, path):
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_h.numel() * out_h.element_size()
     M, B, ps, R = b.max_blocks_per_seq, b.block_size, b.partition_size, len(reps)
+    write_kv, decode_kv, splitk_kv = kv_ops(api, b)
 
     def step(i):
         kc, vc, _ = reps[i % R]
         for k in host:
             devb[k].copy_(host[k], non_blocking=True)
-        api.pa_reshape_and_cache(devb["key"], devb["value"], kc, vc, devb["slot_mapping"])
+        write_kv(devb["key"], devb["value"], kc, vc, devb["slot_mapping"])
         if path == "decode":
-            api.pa_decode(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"], b.scale)
+            decode_kv(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"])
         else:
-            api.pa_decode_splitk(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"],
-                                 b.scale, ps, ws, P)
+            splitk_kv(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"], ps, ws, P)
             api.pa_splitk_reduce(out, ws, devb["context_lens"], M, B, ps, P)
         out_h.copy_(out, non_blocking=True)
 
@@ -472,7 +500,7 @@ def run_copy_blocks(args):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    b, desc = make_workload(args.workload, args.seed, args.partition_size, args.dtype)
+    b, desc = make_workload(args.workload, args.seed, args.partition_size, args.dtype, args.kv_dtype)
     kc = to_device(b.k_cache, b.dtype, dev)
     vc = to_device(b.v_cache, b.dtype, dev)
     N = b.num_blocks
@@ -494,7 +522,8 @@ def run_copy_blocks(args):
     value = moved * args.steps / (ms * 1e-3) / 1e9
     return {"metric": "pa_copy_blocks GB/s (bytes read + written)", "value": round(value, 1), "unit": UNIT,
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
-            "higher_is_better": True, "dtype": "bf16" if b.dtype == "bf16" else "f16", "data": "synthetic",
+            "higher_is_better": True, "dtype": "u8" if b.kv_dtype == "fp8" else ("bf16" if b.dtype == "bf16" else "f16"),
+            "data": "synthetic",
             "config": {"workload": desc, "pairs_per_step": n, "block_bytes": block_bytes,
                        "kernel_timing": mode},
             "roofline": {"kernel": "copy_blocks", "bound": "hbm", "achieved": round(value, 1), "peak": peak,
@@ -519,15 +548,21 @@ def oracle_step_runner(b):
     """Returns (run(n_seqs, offset) -> kv_bytes, cores): one oracle decode step
     (reshape_and_cache + decode) over a cyclic sample of n_seqs sequences."""
     from oracle import c_oracle
+    from paged_kv_cache_173_gb300 import workloads
     cores = c_oracle.max_threads()
     S = b.num_seqs
-    per_tok = 2 * b.num_kv_heads * b.head_dim * 2
+    per_tok = workloads.kv_bytes_per_token(b.num_kv_heads, b.head_dim, workloads.kv_elem_bytes(b))
     kc, vc = b.k_cache.copy(), b.v_cache.copy()  # working pools, written in place each step
 
     def run(n, off):
         idx = (np.arange(n) + off) % S
-        c_oracle.reshape_and_cache(b.key[idx], b.value[idx], kc, vc, b.slot_mapping[idx], inplace=True)
-        c_oracle.decode(b.q[idx], kc, vc, b.block_tables[idx], b.context_lens[idx], b.scale, dtype=b.dtype)
+        if b.kv_dtype == "fp8":
+            c_oracle.reshape_and_cache_fp8(b.key[idx], b.value[idx], kc, vc, b.slot_mapping[idx], b.k_scale,
+                                           b.v_scale, dtype=b.dtype, inplace=True)
+        else:
+            c_oracle.reshape_and_cache(b.key[idx], b.value[idx], kc, vc, b.slot_mapping[idx], inplace=True)
+        c_oracle.decode(b.q[idx], kc, vc, b.block_tables[idx], b.context_lens[idx], b.scale, dtype=b.dtype,
+                        k_scale=b.k_scale, v_scale=b.v_scale)
         return int(np.sum(b.context_lens[idx].astype(np.int64))) * per_tok
 
     return run, cores
@@ -553,7 +588,7 @@ def cpu_baseline(b, kv_bytes, budget_s: float):
 def run_reference(args, rank: int):
     if rank != 0:
         return None
-    b, desc = make_workload(args.workload, args.seed, args.partition_size, args.dtype)
+    b, desc = make_workload(args.workload, args.seed, args.partition_size, args.dtype, args.kv_dtype)
     run, cores = oracle_step_runner(b)
     t0 = time.perf_counter()
     run(1, 0)
@@ -594,6 +629,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="llama3-8b")
     p.add_argument("--partition-size", type=int, default=512)
     p.add_argument("--dtype", choices=["fp16", "bf16"], default="fp16")
+    p.add_argument("--kv-dtype", choices=["same", "fp8"], default="same",
+                   help="fp8: E4M3 KV pools with one float scale each (float16 queries)")
     p.add_argument("--op", choices=["step", "copy-blocks"], default="step",
                    help="step: the decode step (the headline); copy-blocks: time pa_copy_blocks")
     p.add_argument("--copy-pairs", type=int, default=1024)
@@ -610,6 +647,10 @@ def parse_args(argv=None):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.kv_dtype == "same":
+        args.kv_dtype = ""
+    if args.kv_dtype == "fp8" and args.dtype != "fp16":
+        raise SystemExit("--kv-dtype fp8 takes --dtype fp16")
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -84,12 +84,17 @@ def quantize_e4m3(x: float, scale: float) -> int:
 
 def reshape_and_cache_fp8(key: np.ndarray, value: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                           slot_mapping: np.ndarray, k_scale: float, v_scale: float,
-                          dtype: str = "fp16") -> Tuple[np.ndarray, np.ndarray]:
-    """Return copies of the E4M3 pools (uint8) after quantising and writing
-    the new tokens (key/value: float16, or bfloat16 bit patterns)."""
+                          dtype: str = "fp16", inplace: bool = False) -> Tuple[np.ndarray, np.ndarray]:
+    """Return the E4M3 pools (uint8) after quantising and writing the new
+    tokens (key/value: float16, or bfloat16 bit patterns): copies, or with
+    inplace=True the given (contiguous) pools themselves."""
     assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
-    kc = np.ascontiguousarray(k_cache).copy()
-    vc = np.ascontiguousarray(v_cache).copy()
+    if inplace:
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        kc, vc = k_cache, v_cache
+    else:
+        kc = np.ascontiguousarray(k_cache).copy()
+        vc = np.ascontiguousarray(v_cache).copy()
     N, B, Hk, d = kc.shape
     key = np.ascontiguousarray(key)
     value = np.ascontiguousarray(value)

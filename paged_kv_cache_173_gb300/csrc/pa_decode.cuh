@@ -101,7 +101,9 @@ struct DecodeCfg {
   static constexpr int BOX_B = CHUNK * ROW_BYTES;
   static constexpr int DBOX = HEAD_DIM / BOX_ELEMS;  // boxes per row of K (or V)
   static constexpr int HALF_BYTES = DBOX * BOX_B;
-  static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
+  static constexpr int CHUNK_BYTES = 2 * HALF_BYTES;   // K and V of one 16-token chunk
+  static constexpr int CPS = ELEM == 1 ? 2 : 1;        // chunks per stage
+  static constexpr int STAGE_BYTES = CPS * CHUNK_BYTES;
   static constexpr int RING_BYTES = WARPS * STAGES * STAGE_BYTES;
   static constexpr int GMAX = NT * 8;
   static constexpr int MO_PITCH = HEAD_DIM + 4;  // floats; spreads the merge writes over banks
@@ -186,30 +188,40 @@ __device__ __forceinline__ void load_q_frags_e4m3(uint32_t (&qf)[HEAD_DIM / 16][
   }
 }
 
-// Online-softmax step for one 16-token chunk whose scores S[16 tokens][8*NT
-// heads] are in `sacc` (m16n8 accumulator layout: token g holds elements 0-1,
-// token g + 8 elements 2-3), of which the first `valid` tokens belong to the
-// sequence: updates the running maxima and sums, rescales the accumulators
-// when a maximum moves, and returns P^T as B fragments (bf16: also the
-// residual P - bf16(P) in `pl`).
-template <typename T, int HEAD_DIM, int NT>
-__device__ __forceinline__ void softmax_chunk(WarpAcc<HEAD_DIM, NT>& acc, const float (&sacc)[NT][4], int valid,
-                                              float sl2, int lane, uint32_t (&pb)[NT][2],
-                                              uint32_t (&pl)[NT][2]) {
+// Online-softmax step over NSUB 16-token chunks whose scores S[16 tokens][8*NT
+// heads] are in sacc[sb] (m16n8 accumulator layout: token g holds elements
+// 0-1, token g + 8 elements 2-3), of which the first valid[sb] tokens belong
+// to the sequence: updates the running maxima and sums once for all of them,
+// rescales the accumulators when a maximum moves, and returns each chunk's
+// P^T as B fragments (bf16: also the residual P - bf16(P) in `pl`).
+template <typename T, int HEAD_DIM, int NT, int NSUB>
+__device__ __forceinline__ void softmax_step(WarpAcc<HEAD_DIM, NT>& acc, const float (&sacc)[NSUB][NT][4],
+                                             const int (&valid)[NSUB], float sl2, int lane,
+                                             uint32_t (&pb)[NSUB][NT][2], uint32_t (&pl)[NSUB][NT][2]) {
   constexpr int KSTEPS = HEAD_DIM / 16;
   const int g = lane >> 2;
-  // base 2; slots past the context are excluded by select
-  const bool v0 = g < valid;
-  const bool v1 = g + 8 < valid;
   constexpr bool kSplitP = !std::is_same<T, __half>::value;  // bf16: P = P_hi + P_lo
+  static_assert(!kSplitP || NSUB == 1, "bf16 takes one chunk per step");
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const float x0 = v0 ? sacc[nt][0] * sl2 : -INFINITY;
-    const float x1 = v0 ? sacc[nt][1] * sl2 : -INFINITY;
-    const float x2 = v1 ? sacc[nt][2] * sl2 : -INFINITY;
-    const float x3 = v1 ? sacc[nt][3] * sl2 : -INFINITY;
-    float mx0 = fmaxf(x0, x2);
-    float mx1 = fmaxf(x1, x3);
+    // base 2; slots past the context are excluded by select
+    float x[NSUB][4];
+#pragma unroll
+    for (int sb = 0; sb < NSUB; ++sb) {
+      const bool v0 = g < valid[sb];
+      const bool v1 = g + 8 < valid[sb];
+      x[sb][0] = v0 ? sacc[sb][nt][0] * sl2 : -INFINITY;
+      x[sb][1] = v0 ? sacc[sb][nt][1] * sl2 : -INFINITY;
+      x[sb][2] = v1 ? sacc[sb][nt][2] * sl2 : -INFINITY;
+      x[sb][3] = v1 ? sacc[sb][nt][3] * sl2 : -INFINITY;
+    }
+    float mx0 = fmaxf(x[0][0], x[0][2]);
+    float mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+    for (int sb = 1; sb < NSUB; ++sb) {
+      mx0 = fmaxf(mx0, fmaxf(x[sb][0], x[sb][2]));
+      mx1 = fmaxf(mx1, fmaxf(x[sb][1], x[sb][3]));
+    }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, off));
@@ -222,24 +234,31 @@ __device__ __forceinline__ void softmax_chunk(WarpAcc<HEAD_DIM, NT>& acc, const 
     const bool grew = __any_sync(FULL_MASK, (mn0 != acc.m[nt][0]) | (mn1 != acc.m[nt][1]));
     acc.m[nt][0] = mn0;
     acc.m[nt][1] = mn1;
-    const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);  // token g
-    const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);  // token g + 8
-    const uint32_t lo = pack2<T>(p0, p1);
-    const uint32_t hi = pack2<T>(p2, p3);
-    const float2 flo = unpack2<T>(lo);
-    const float2 fhi = unpack2<T>(hi);
-    if constexpr (kSplitP) {
-      // bf16 keeps 8 significant bits: P also goes in as the rounded residual,
-      // so P_hi + P_lo carries about 16 bits and the sum uses P itself
-      pl[nt][0] = movmatrix_trans(pack2<T>(p0 - flo.x, p1 - flo.y));
-      pl[nt][1] = movmatrix_trans(pack2<T>(p2 - fhi.x, p3 - fhi.y));
-      acc.l[nt][0] = acc.l[nt][0] * cr0 + (p0 + p2);
-      acc.l[nt][1] = acc.l[nt][1] * cr1 + (p1 + p3);
-    } else {
-      // the running sum adds the same rounded weights that multiply V
-      acc.l[nt][0] = acc.l[nt][0] * cr0 + (flo.x + fhi.x);
-      acc.l[nt][1] = acc.l[nt][1] * cr1 + (flo.y + fhi.y);
+    float sum0 = 0.f, sum1 = 0.f;
+    uint32_t lo[NSUB], hi[NSUB];
+#pragma unroll
+    for (int sb = 0; sb < NSUB; ++sb) {
+      const float p0 = ex2(x[sb][0] - mn0), p1 = ex2(x[sb][1] - mn1);  // token g
+      const float p2 = ex2(x[sb][2] - mn0), p3 = ex2(x[sb][3] - mn1);  // token g + 8
+      lo[sb] = pack2<T>(p0, p1);
+      hi[sb] = pack2<T>(p2, p3);
+      const float2 flo = unpack2<T>(lo[sb]);
+      const float2 fhi = unpack2<T>(hi[sb]);
+      if constexpr (kSplitP) {
+        // bf16 keeps 8 significant bits: P also goes in as the rounded residual,
+        // so P_hi + P_lo carries about 16 bits and the sum uses P itself
+        pl[sb][nt][0] = movmatrix_trans(pack2<T>(p0 - flo.x, p1 - flo.y));
+        pl[sb][nt][1] = movmatrix_trans(pack2<T>(p2 - fhi.x, p3 - fhi.y));
+        sum0 = sb == 0 ? (p0 + p2) : sum0 + (p0 + p2);
+        sum1 = sb == 0 ? (p1 + p3) : sum1 + (p1 + p3);
+      } else {
+        // the running sum adds the same rounded weights that multiply V
+        sum0 = sb == 0 ? (flo.x + fhi.x) : sum0 + (flo.x + fhi.x);
+        sum1 = sb == 0 ? (flo.y + fhi.y) : sum1 + (flo.y + fhi.y);
+      }
     }
+    acc.l[nt][0] = acc.l[nt][0] * cr0 + sum0;
+    acc.l[nt][1] = acc.l[nt][1] * cr1 + sum1;
     if (grew) {  // a running maximum moved: rescale the accumulators
 #pragma unroll
       for (int dm = 0; dm < KSTEPS; ++dm) {
@@ -249,8 +268,11 @@ __device__ __forceinline__ void softmax_chunk(WarpAcc<HEAD_DIM, NT>& acc, const 
         acc.o[dm][nt][3] *= cr1;
       }
     }
-    pb[nt][0] = movmatrix_trans(lo);  // P^T tokens 0-7 as the B fragment
-    pb[nt][1] = movmatrix_trans(hi);  // P^T tokens 8-15
+#pragma unroll
+    for (int sb = 0; sb < NSUB; ++sb) {
+      pb[sb][nt][0] = movmatrix_trans(lo[sb]);  // P^T tokens 0-7 as the B fragment
+      pb[sb][nt][1] = movmatrix_trans(hi[sb]);  // P^T tokens 8-15
+    }
   }
 }
 
@@ -268,11 +290,11 @@ __device__ __forceinline__ void attend_chunk(WarpAcc<HEAD_DIM, NT>& acc,
 
   // S[16 tokens][8*NT heads] = K Q^T, as two independent MMA chains (even
   // and odd k-steps) that are added at the end
-  float sacc[NT][4], sacc2[NT][4];
+  float sacc[1][NT][4], sacc2[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) sacc[nt][i] = sacc2[nt][i] = 0.f;
+    for (int i = 0; i < 4; ++i) sacc[0][nt][i] = sacc2[nt][i] = 0.f;
   // lane supplies row (lane & 15) at 16-byte unit 2*(ks%4) + lane/16 of box ks/4
   const uint32_t ka = kb + (lane & 15) * 128;
   const uint32_t kx = lane & 7;
@@ -283,15 +305,18 @@ __device__ __forceinline__ void attend_chunk(WarpAcc<HEAD_DIM, NT>& acc,
     ldsm_x4(a, ka + (ks >> 2) * BOX_BYTES + unit * 16);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
-      mma_16816<T>((ks & 1) ? sacc2[nt] : sacc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+      mma_16816<T>((ks & 1) ? sacc2[nt] : sacc[0][nt], a, qf[ks][nt][0], qf[ks][nt][1]);
   }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) sacc[nt][i] += sacc2[nt][i];
+    for (int i = 0; i < 4; ++i) sacc[0][nt][i] += sacc2[nt][i];
 
-  uint32_t pb[NT][2], pl[NT][2];
-  softmax_chunk<T, HEAD_DIM, NT>(acc, sacc, valid, sl2, lane, pb, pl);
+  uint32_t pb1[1][NT][2], pl1[1][NT][2];
+  const int valid1[1] = {valid};
+  softmax_step<T, HEAD_DIM, NT, 1>(acc, sacc, valid1, sl2, lane, pb1, pl1);
+  const uint32_t(&pb)[NT][2] = pb1[0];
+  const uint32_t(&pl)[NT][2] = pl1[0];
 
   // O^T[d][heads] += V^T P^T; V rows past the context are zeroed by select
   const int t0 = 2 * c4;
@@ -371,26 +396,17 @@ __device__ __forceinline__ void pv_e4m3(WarpAcc<HEAD_DIM, NT>& acc, const uint32
   }
 }
 
-// attend_chunk for E4M3 K and V boxes (codes widened exactly to float16 in
-// registers; the pool scales are applied outside: k_scale in `sl2`, v_scale
-// to the final output).  The chunk's K boxes sit at `kb`, its V boxes at
-// kb + half_bytes.
+// S = K Q^T for one 16-token chunk of E4M3 keys at `kb`.  A lane receives
+// the codes of tokens g and g + 8 at dims 4c .. 4c+3 of a unit; their low
+// pair fills k indices 2c, 2c+1 and their high pair 2c+8, 2c+9
+// (load_q_frags_e4m3 orders q the same way).  Even and odd k-steps run as
+// two MMA chains that are added at the end.
 template <int HEAD_DIM, int NT, int ROW_BYTES>
-__device__ __forceinline__ void attend_chunk_e4m3(WarpAcc<HEAD_DIM, NT>& acc,
-                                                  const uint32_t (&qf)[HEAD_DIM / 16][NT][2], uint32_t kb,
-                                                  uint32_t half_bytes, int valid, float sl2, int lane) {
+__device__ __forceinline__ void qk_e4m3(float (&sacc)[NT][4], const uint32_t (&qf)[HEAD_DIM / 16][NT][2],
+                                        uint32_t kb, uint32_t tok, uint32_t uo) {
   constexpr int UNITS = ROW_BYTES / 16;
   constexpr int BOXB = CHUNK * ROW_BYTES;
-  const int c4 = lane & 3;
-  // lane supplies token row `tok` of unit (u + uo): the four matrices are
-  // tokens {0-7, 8-15} x units {u, u + 1}
-  const uint32_t tok = (lane & 7) + (((lane >> 3) & 1) << 3);
-  const uint32_t uo = lane >> 4;
-
-  // S = K Q^T: a lane receives the codes of tokens g and g + 8 at dims
-  // 4c .. 4c+3 of a unit; their low pair fills k indices 2c, 2c+1 and their
-  // high pair 2c+8, 2c+9 (load_q_frags_e4m3 orders q the same way)
-  float sacc[NT][4], sacc2[NT][4];
+  float sacc2[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -414,17 +430,69 @@ __device__ __forceinline__ void attend_chunk_e4m3(WarpAcc<HEAD_DIM, NT>& acc,
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) sacc[nt][i] += sacc2[nt][i];
+}
 
-  uint32_t pb[NT][2], pl[NT][2];
-  softmax_chunk<__half, HEAD_DIM, NT>(acc, sacc, valid, sl2, lane, pb, pl);
+// Lane roles shared by the E4M3 ldmatrix loads: a lane supplies token row
+// `tok` of unit (u + uo), so the four matrices are tokens {0-7, 8-15} x
+// units {u, u + 1}.
+__device__ __forceinline__ uint32_t e4m3_tok(int lane) { return (lane & 7) + (((lane >> 3) & 1) << 3); }
+__device__ __forceinline__ uint32_t e4m3_uo(int lane) { return static_cast<uint32_t>(lane) >> 4; }
 
-  const int t0 = 2 * c4;
-  const uint32_t mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-  const uint32_t mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+// Select masks for the V fragments of a chunk with `valid` tokens: the
+// halves of tokens (2c, 2c+1) and (2c+8, 2c+9).
+__device__ __forceinline__ void v_masks(int valid, int lane, uint32_t& mlo, uint32_t& mhi) {
+  const int t0 = 2 * (lane & 3);
+  mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+  mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+}
+
+// attend_chunk for one 16-token chunk of E4M3 K and V boxes (codes widened
+// exactly to float16 in registers; the pool scales are applied outside:
+// k_scale in `sl2`, v_scale to the final output).  K boxes at `kb`, V boxes
+// at kb + half_bytes.
+template <int HEAD_DIM, int NT, int ROW_BYTES>
+__device__ __forceinline__ void attend_chunk_e4m3(WarpAcc<HEAD_DIM, NT>& acc,
+                                                  const uint32_t (&qf)[HEAD_DIM / 16][NT][2], uint32_t kb,
+                                                  uint32_t half_bytes, int valid, float sl2, int lane) {
+  const uint32_t tok = e4m3_tok(lane), uo = e4m3_uo(lane);
+  float sacc[1][NT][4];
+  qk_e4m3<HEAD_DIM, NT, ROW_BYTES>(sacc[0], qf, kb, tok, uo);
+  uint32_t pb[1][NT][2], pl[1][NT][2];
+  const int valid1[1] = {valid};
+  softmax_step<__half, HEAD_DIM, NT, 1>(acc, sacc, valid1, sl2, lane, pb, pl);
+  uint32_t mlo, mhi;
+  v_masks(valid, lane, mlo, mhi);
   if (valid == CHUNK) {
-    pv_e4m3<HEAD_DIM, NT, ROW_BYTES, false>(acc, pb, kb + half_bytes, tok, uo, mlo, mhi);
+    pv_e4m3<HEAD_DIM, NT, ROW_BYTES, false>(acc, pb[0], kb + half_bytes, tok, uo, mlo, mhi);
   } else {  // the last chunk of the sequence
-    pv_e4m3<HEAD_DIM, NT, ROW_BYTES, true>(acc, pb, kb + half_bytes, tok, uo, mlo, mhi);
+    pv_e4m3<HEAD_DIM, NT, ROW_BYTES, true>(acc, pb[0], kb + half_bytes, tok, uo, mlo, mhi);
+  }
+}
+
+// Two 16-token chunks of E4M3 codes in one stage (the first at `kb`, the
+// second at kb + chunk_bytes; K then V boxes in each), scored and folded
+// into the running softmax in one step.  The first chunk is full; the second
+// has `valid2` tokens.
+template <int HEAD_DIM, int NT, int ROW_BYTES>
+__device__ __forceinline__ void attend_pair_e4m3(WarpAcc<HEAD_DIM, NT>& acc,
+                                                 const uint32_t (&qf)[HEAD_DIM / 16][NT][2], uint32_t kb,
+                                                 uint32_t chunk_bytes, uint32_t half_bytes, int valid2, float sl2,
+                                                 int lane) {
+  const uint32_t tok = e4m3_tok(lane), uo = e4m3_uo(lane);
+  const uint32_t kb2 = kb + chunk_bytes;
+  float sacc[2][NT][4];
+  qk_e4m3<HEAD_DIM, NT, ROW_BYTES>(sacc[0], qf, kb, tok, uo);
+  qk_e4m3<HEAD_DIM, NT, ROW_BYTES>(sacc[1], qf, kb2, tok, uo);
+  uint32_t pb[2][NT][2], pl[2][NT][2];
+  const int valid[2] = {CHUNK, valid2};
+  softmax_step<__half, HEAD_DIM, NT, 2>(acc, sacc, valid, sl2, lane, pb, pl);
+  uint32_t mlo, mhi;
+  v_masks(valid2, lane, mlo, mhi);
+  pv_e4m3<HEAD_DIM, NT, ROW_BYTES, false>(acc, pb[0], kb + half_bytes, tok, uo, mlo, mhi);
+  if (valid2 == CHUNK) {
+    pv_e4m3<HEAD_DIM, NT, ROW_BYTES, false>(acc, pb[1], kb2 + half_bytes, tok, uo, mlo, mhi);
+  } else {
+    pv_e4m3<HEAD_DIM, NT, ROW_BYTES, true>(acc, pb[1], kb2 + half_bytes, tok, uo, mlo, mhi);
   }
 }
 
@@ -568,38 +636,49 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int c1 = CLUSTER ? cmax : min(c0 + p.partition_chunks, nchunks);
   const int nk = first < c1 ? (c1 - first + WARPS - 1) / WARPS : 0;  // <= nk_cap
 
+  // A stage holds CPS of the warp's chunks (its k-th chunk is chunk
+  // first + k * WARPS of the range); `issued` and `consumed` count stages.
+  constexpr int CPS = Cfg::CPS;
+  const int nst = (nk + CPS - 1) / CPS;
   int issued = 0;
   bool bad = false;
 
   auto issue_next = [&]() {
-    const int k = issued;
-    if (k > 0 && (k & 31) == 0) {
-      win_cur = win_nxt;
-      win_nxt = win_load(k + 32);
-    }
-    int phys = __shfl_sync(FULL_MASK, win_cur, k & 31);
-    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
-      bad = true;  // never read outside the pool; the result becomes NaN
-      phys = 0;
-    }
-    const int ch = first + k * WARPS;
-    const int row0 = (ch & ((1 << cpb_log2) - 1)) * CHUNK;
-    const int slot = k % STAGES;
-    if (lane == 0) {
-      uint8_t* dst = wring + slot * Cfg::STAGE_BYTES;
-      const int y = phys * p.block_size + row0;  // pool row of the chunk's first token
-      mbar_arrive_expect_tx(&wbar[slot], Cfg::STAGE_BYTES);
+    const int it = issued;
+    const int slot = it % STAGES;
+    const int nload = min(CPS, nk - it * CPS);  // >= 1
+    uint8_t* dst = wring + slot * Cfg::STAGE_BYTES;
+    if (lane == 0) mbar_arrive_expect_tx(&wbar[slot], nload * Cfg::CHUNK_BYTES);
 #pragma unroll
-      for (int b = 0; b < Cfg::DBOX; ++b) {
-        tma_load_3d(dst + b * Cfg::BOX_B, &p.tmap_k, b * Cfg::BOX_ELEMS, kvh, y, &wbar[slot]);
-        tma_load_3d(dst + Cfg::HALF_BYTES + b * Cfg::BOX_B, &p.tmap_v, b * Cfg::BOX_ELEMS, kvh, y, &wbar[slot]);
+    for (int j = 0; j < CPS; ++j) {
+      const int k = it * CPS + j;
+      if (j > 0 && k >= nk) break;  // warp-uniform
+      if (k > 0 && (k & 31) == 0) {
+        win_cur = win_nxt;
+        win_nxt = win_load(k + 32);
+      }
+      int phys = __shfl_sync(FULL_MASK, win_cur, k & 31);
+      if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
+        bad = true;  // never read outside the pool; the result becomes NaN
+        phys = 0;
+      }
+      const int ch = first + k * WARPS;
+      const int row0 = (ch & ((1 << cpb_log2) - 1)) * CHUNK;
+      if (lane == 0) {
+        uint8_t* cd = dst + j * Cfg::CHUNK_BYTES;
+        const int y = phys * p.block_size + row0;  // pool row of the chunk's first token
+#pragma unroll
+        for (int b = 0; b < Cfg::DBOX; ++b) {
+          tma_load_3d(cd + b * Cfg::BOX_B, &p.tmap_k, b * Cfg::BOX_ELEMS, kvh, y, &wbar[slot]);
+          tma_load_3d(cd + Cfg::HALF_BYTES + b * Cfg::BOX_B, &p.tmap_v, b * Cfg::BOX_ELEMS, kvh, y, &wbar[slot]);
+        }
       }
     }
     ++issued;
   };
 
 #pragma unroll 1
-  for (int i = 0; i < STAGES && i < nk; ++i) issue_next();
+  for (int i = 0; i < STAGES && i < nst; ++i) issue_next();
 
   WarpAcc<HEAD_DIM, NT> acc;
   acc.reset();
@@ -608,26 +687,33 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   int consumed = 0;
   bool timed_out = false;
 #pragma unroll 1
-  for (; consumed < nk; ++consumed) {
-    const int k = consumed;
-    const int slot = k % STAGES;
-    const bool ok = mbar_wait_bounded(&wbar[slot], (k / STAGES) & 1, WAIT_LIMIT_NS);
+  for (; consumed < nst; ++consumed) {
+    const int it = consumed;
+    const int slot = it % STAGES;
+    const bool ok = mbar_wait_bounded(&wbar[slot], (it / STAGES) & 1, WAIT_LIMIT_NS);
     if (!__all_sync(FULL_MASK, ok)) {  // a warp-uniform decision
       timed_out = true;
       break;
     }
-    const int ch = first + k * WARPS;
+    const int k0 = it * CPS;
+    const int ch = first + k0 * WARPS;
     const int valid = min(CHUNK, ctx - ch * CHUNK);
     const uint32_t stage = smem_addr(wring + slot * Cfg::STAGE_BYTES);
     if constexpr (FP8) {
-      attend_chunk_e4m3<HEAD_DIM, NT, Cfg::ROW_BYTES>(acc, qf, stage, Cfg::HALF_BYTES, valid, sl2, lane);
+      if (k0 + 1 < nk) {  // two chunks: the first is full (the second lies further in)
+        const int valid2 = min(CHUNK, ctx - (ch + WARPS) * CHUNK);
+        attend_pair_e4m3<HEAD_DIM, NT, Cfg::ROW_BYTES>(acc, qf, stage, Cfg::CHUNK_BYTES, Cfg::HALF_BYTES, valid2,
+                                                       sl2, lane);
+      } else {
+        attend_chunk_e4m3<HEAD_DIM, NT, Cfg::ROW_BYTES>(acc, qf, stage, Cfg::HALF_BYTES, valid, sl2, lane);
+      }
     } else {
       attend_chunk<T, HEAD_DIM, NT>(acc, qf, stage, Cfg::HALF_BYTES, valid, sl2, lane);
     }
 
     fence_proxy_async_smem();  // this lane's reads of the slot precede the refill's writes
     __syncwarp();
-    if (issued < nk) issue_next();
+    if (issued < nst) issue_next();
   }
 
   if (timed_out) {

@@ -492,27 +492,37 @@ def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, path):
 
 # ------------------------------------------------------------ copy_blocks
 def run_copy_blocks(args):
-    """Time pa_copy_blocks: K steps, each copying `--copy-pairs` whole blocks of
-    the workload's pool (src and dst drawn from distinct halves of the pool,
-    rotating over sets larger than L2).  Bytes = read + write of K and V."""
+    """Time pa_copy_blocks: K steps, each copying `--copy-pairs` whole blocks.
+    The pools have the workload's block shape and element type, with enough
+    blocks that the source half holds at least 4x the L2 of K and V; each
+    cycle of steps walks a permutation of the source half (and of the
+    destination half), so no block is read twice within a cycle.  Bytes =
+    read + write of K and V."""
     import torch
     from paged_kv_cache_173_gb300 import api
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     b, desc = make_workload(args.workload, args.seed, args.partition_size, args.dtype, args.kv_dtype)
-    kc = to_device(b.k_cache, b.dtype, dev)
-    vc = to_device(b.v_cache, b.dtype, dev)
-    N = b.num_blocks
+    shape = b.k_cache.shape[1:]
+    block_bytes = int(np.prod(shape)) * b.k_cache.itemsize
+    l2_bytes = 129 * 2 ** 20
+    N = max(b.num_blocks, 2 * math.ceil(4 * l2_bytes / (2 * block_bytes)))
+    dt = {1: torch.uint8, 2: torch.int16}[b.k_cache.itemsize]
+    kc = torch.randint(-100, 100, (N, *shape), dtype=torch.int16, device=dev).to(dt)
+    vc = torch.randint(-100, 100, (N, *shape), dtype=torch.int16, device=dev).to(dt)
+    if dt == torch.int16:  # bit patterns of the workload's 16-bit type
+        kc = kc.view(torch.bfloat16 if b.dtype == "bf16" else torch.float16)
+        vc = vc.view(torch.bfloat16 if b.dtype == "bf16" else torch.float16)
     half = N // 2
     n = min(args.copy_pairs, half)
-    block_bytes = kc[0].numel() * kc.element_size()
     rng = np.random.default_rng(args.seed)
+    src_perm = rng.permutation(half)
+    dst_perm = half + rng.permutation(N - half)
     sets = []
-    for _ in range(max(2, math.ceil(4 * 129 * 2 ** 20 / max(1, 4 * n * block_bytes)) + 1)):
-        src = rng.choice(half, size=n, replace=False)
-        dst = half + rng.choice(N - half, size=n, replace=False)
-        sets.append(torch.from_numpy(np.stack([src, dst], axis=1).astype(np.int64)).to(dev))
+    for i in range(half // n):
+        pairs = np.stack([src_perm[i * n:(i + 1) * n], dst_perm[i * n:(i + 1) * n]], axis=1)
+        sets.append(torch.from_numpy(pairs.astype(np.int64)).to(dev))
     stream = torch.cuda.Stream(dev)
     kernels = [("copy_blocks", lambda r: api.pa_copy_blocks(kc, vc, sets[r % len(sets)]))]
     clocks = ClockSampler(dev.index)
@@ -524,7 +534,9 @@ def run_copy_blocks(args):
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
             "higher_is_better": True, "dtype": "u8" if b.kv_dtype == "fp8" else ("bf16" if b.dtype == "bf16" else "f16"),
             "data": "synthetic",
-            "config": {"workload": desc, "pairs_per_step": n, "block_bytes": block_bytes,
+            "config": {"workload": desc, "pairs_per_step": n, "block_bytes": block_bytes, "pool_blocks": N,
+                       "l2": f"one cycle of {len(sets)} steps reads {half * 2 * block_bytes / 1e9:.2f} GB of "
+                             "distinct source blocks (> 4x the 129 MB L2)",
                        "kernel_timing": mode},
             "roofline": {"kernel": "copy_blocks", "bound": "hbm", "achieved": round(value, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,

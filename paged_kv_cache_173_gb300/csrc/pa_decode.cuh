@@ -102,7 +102,9 @@ struct DecodeCfg {
   static constexpr int DBOX = HEAD_DIM / BOX_ELEMS;  // boxes per row of K (or V)
   static constexpr int HALF_BYTES = DBOX * BOX_B;
   static constexpr int CHUNK_BYTES = 2 * HALF_BYTES;   // K and V of one 16-token chunk
-  static constexpr int CPS = ELEM == 1 ? 2 : 1;        // chunks per stage
+  // chunks per stage: E4M3 stages up to d = 128 hold two chunks (8 KB);
+  // d = 256 chunks are 8 KB already
+  static constexpr int CPS = (ELEM == 1 && HEAD_DIM <= 128) ? 2 : 1;
   static constexpr int STAGE_BYTES = CPS * CHUNK_BYTES;
   static constexpr int RING_BYTES = WARPS * STAGES * STAGE_BYTES;
   static constexpr int GMAX = NT * 8;
@@ -700,7 +702,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     const int valid = min(CHUNK, ctx - ch * CHUNK);
     const uint32_t stage = smem_addr(wring + slot * Cfg::STAGE_BYTES);
     if constexpr (FP8) {
-      if (k0 + 1 < nk) {  // two chunks: the first is full (the second lies further in)
+      if (CPS == 2 && k0 + 1 < nk) {  // two chunks: the first is full (the second lies further in)
         const int valid2 = min(CHUNK, ctx - (ch + WARPS) * CHUNK);
         attend_pair_e4m3<HEAD_DIM, NT, Cfg::ROW_BYTES>(acc, qf, stage, Cfg::CHUNK_BYTES, Cfg::HALF_BYTES, valid2,
                                                        sl2, lane);
@@ -1081,9 +1083,9 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
 
 // CTA shape per head size: 4 warps x 2 stages (8 KB stages up to d = 128,
 // three CTAs per SM); d = 256 has 16 KB stages and uses 2 warps x 2 stages
-// to keep three CTAs per SM.  E4M3 stages are half as large: 4 warps x 2
-// stages fit five CTAs per SM (registers), which measured faster than
-// keeping the 16-bit kernel's bytes in flight with 4 stages.
+// to keep three CTAs per SM.  E4M3 stages are 8 KB for every head size (two
+// chunks up to d = 128), so E4M3 keeps 4 warps x 2 stages throughout; the
+// sweep over 2-8 warps and 2-4 stages found nothing faster.
 template <int HEAD_DIM, int ELEM = 2>
 struct DecodeShape {
   static constexpr int WARPS = ELEM == 1 ? PA_DECODE_FP8_WARPS : (HEAD_DIM > 128 ? 2 : PA_DECODE_WARPS);

@@ -367,6 +367,18 @@ def run_gpu(args, rank: int, world: int):
         "splitk": [("reshape_and_cache", reshape), ("paged_decode_splitk", decode_splitk),
                    ("splitk_reduce", reduce)],
     }
+    if b.prefix_lens is not None:  # sequences share prompt blocks in consecutive groups
+        plens = t(b.prefix_lens)
+
+        def decode_prefix(r):
+            kc, vc, q = reps[r % R]
+            api.pa_decode_prefix_splitk(out, q, kc, vc, bt, cl, b.scale, b.seqs_per_group, plens, ps, ws, P,
+                                        k_scale=b.k_scale, v_scale=b.v_scale)
+
+        paths["prefix"] = [("reshape_and_cache", reshape), ("paged_decode_prefix", decode_prefix),
+                           ("splitk_reduce", reduce)]
+    if args.path not in ("auto", *paths):
+        raise SystemExit(f"--path {args.path} needs a workload with shared-prefix groups")
     want = list(paths) if args.path == "auto" else [args.path]
     stream = torch.cuda.Stream(dev)
     K, W = args.steps, args.warmup
@@ -391,7 +403,10 @@ def run_gpu(args, rank: int, world: int):
     ms = r0["ms"]
     value = whole_job_gbs(kv_bytes, K, world, ms)
     step_ms = ms / K
-    achieved = kv_bytes / (t_decode * 1e-3) / 1e9
+    # the shared-prefix path reads each shared block once: its algorithmic
+    # bytes are the unique bytes
+    roof_bytes = workloads.unique_kv_bytes(b) if best == "prefix" else kv_bytes
+    achieved = roof_bytes / (t_decode * 1e-3) / 1e9
     traffic = load_traffic(workload_key(args), decode_name)
     res = {
         "metric": METRIC,
@@ -412,7 +427,9 @@ def run_gpu(args, rank: int, world: int):
             "kv_bytes_per_step": kv_bytes,
             "path": best,
             "step": " -> ".join(n for n, _ in kern),
-            "partition_size": ps if best == "splitk" else None,
+            "partition_size": ps if best in ("splitk", "prefix") else None,
+            "roofline_bytes": ("unique KV bytes (each shared block once)" if best == "prefix"
+                               else "algorithmic KV bytes"),
             "l2": f"{R} rotating pool replicas ({R * pool_bytes / 1e9:.2f} GB) > 129 MB L2; steps back to back",
             "steps_per_graph": r0["G"],
             "kernel_timing": r0["mode"],
@@ -432,7 +449,7 @@ def run_gpu(args, rank: int, world: int):
             "traffic": traffic,
             "peak_kind": f"{peak_kind} (copy GB/s)",
         },
-        "gpu_launches": len(kern) * K,
+        "gpu_launches": (len(kern) + (1 if best == "prefix" else 0)) * K,
         "e2e": e2e,
         "clocks": r0["clocks"],
         "paths": {n: {"ms_per_step": round(v["ms"] / K, 5),
@@ -459,6 +476,10 @@ def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, path):
     d2h = out_h.numel() * out_h.element_size()
     M, B, ps, R = b.max_blocks_per_seq, b.block_size, b.partition_size, len(reps)
     write_kv, decode_kv, splitk_kv = kv_ops(api, b)
+    if path == "prefix":
+        host["prefix_lens"] = torch.from_numpy(b.prefix_lens).pin_memory()
+        devb["prefix_lens"] = torch.empty_like(host["prefix_lens"], device=dev)
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
 
     def step(i):
         kc, vc, _ = reps[i % R]
@@ -467,6 +488,11 @@ def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, path):
         write_kv(devb["key"], devb["value"], kc, vc, devb["slot_mapping"])
         if path == "decode":
             decode_kv(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"])
+        elif path == "prefix":
+            api.pa_decode_prefix_splitk(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"], b.scale,
+                                        b.seqs_per_group, devb["prefix_lens"], ps, ws, P, k_scale=b.k_scale,
+                                        v_scale=b.v_scale)
+            api.pa_splitk_reduce(out, ws, devb["context_lens"], M, B, ps, P)
         else:
             splitk_kv(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"], ps, ws, P)
             api.pa_splitk_reduce(out, ws, devb["context_lens"], M, B, ps, P)
@@ -646,9 +672,10 @@ def parse_args(argv=None):
     p.add_argument("--op", choices=["step", "copy-blocks"], default="step",
                    help="step: the decode step (the headline); copy-blocks: time pa_copy_blocks")
     p.add_argument("--copy-pairs", type=int, default=1024)
-    p.add_argument("--path", choices=["auto", "decode", "splitk"], default="auto",
-                   help="decode: reshape + pa_decode; splitk: reshape + pa_decode_splitk + reduce; "
-                        "auto: time both, report the faster")
+    p.add_argument("--path", choices=["auto", "decode", "splitk", "prefix"], default="auto",
+                   help="decode: reshape + pa_decode; splitk: reshape + pa_decode_splitk + reduce; prefix "
+                        "(shared-prefix workload): reshape + pa_decode_prefix_splitk + reduce; auto: time "
+                        "every path the workload has, report the fastest")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=2000)
     p.add_argument("--cpu-seconds", type=float, default=12.0)

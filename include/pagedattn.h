@@ -209,6 +209,56 @@ int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* 
                      size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_prefix_splitk -- pa_decode_splitk for batches whose sequences
+ * share prompt blocks: each shared block is read once per group instead of
+ * once per sequence.
+ *
+ * Parallel sampling (several outputs from one prompt) and shared prefixes
+ * let several block tables point at the same physical blocks ("Unveiling
+ * the NVIDIA driver stack: GPU page tables and vLLM PagedAttention",
+ * section 4; "PagedAttention: when the KV cache meets OS paging", section
+ * 4.3; "in-depth reading", section 2.4).  The result is the attention that
+ * pa_decode_splitk computes.  What changes is the bytes read: a shared
+ * prompt block is read once per group and KV head (for up to 16 / G
+ * sequences of the group per read, 8 / G at head_dim 256).
+ *
+ * Groups: sequences [j * seqs_per_group, min((j + 1) * seqs_per_group,
+ * num_seqs)) form group j; callers order the batch so that the sequences of
+ * one prompt are consecutive.  prefix_lens[j] (device, int32,
+ * ceil(num_seqs / seqs_per_group) entries) is the number of leading tokens
+ * that the group's sequences hold in the same physical blocks (the first
+ * prefix_lens[j] / block_size entries of their table rows are equal).
+ *
+ * Sequence s of group j has its first L = prefix_lens[j] tokens computed by
+ * the group's shared pass when L is a positive multiple of partition_size,
+ * L <= context_lens[s], and L <= the context length of the group's first
+ * sequence (both within max_blocks_per_seq * block_size).  Otherwise the
+ * whole sequence is computed on its own, exactly as by pa_decode_splitk.
+ * The shared pass reads the prefix through the group's first table row.
+ *
+ *   dtype, kv_dtype   PA_FP16 or PA_BF16 with kv_dtype == dtype, or dtype
+ *                     PA_FP16 with kv_dtype PA_FP8_E4M3 and the pool scales
+ *                     k_scale, v_scale (ignored for 16-bit caches)
+ *   seqs_per_group    >= 1
+ *
+ * Follow with pa_splitk_reduce (same partition_size, max_num_partitions,
+ * workspace; dtype of out) on the same stream.  Other arguments as
+ * pa_decode_splitk.
+ *
+ * Device-value outcomes: as pa_decode_splitk.  In addition, a sequence whose
+ * table entries over the shared prefix differ from the group's first row
+ * gets NaN.
+ */
+int pa_decode_prefix_splitk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int num_heads,
+                            int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                            float scale, int dtype, int kv_dtype, float k_scale, float v_scale,
+                            int seqs_per_group, const int32_t* prefix_lens, int partition_size,
+                            int max_num_partitions, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
  * pa_splitk_reduce -- merge the partitions left by pa_decode_splitk.
  *
  * For each (s, h) whose sequence has P = ceil(context_lens[s] /

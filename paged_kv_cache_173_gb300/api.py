@@ -232,6 +232,33 @@ def pa_decode_splitk_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tens
     _lib.check("pa_decode_splitk_fp8", st)
 
 
+def pa_decode_prefix_splitk(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                            seqs_per_group: int, prefix_lens: torch.Tensor, partition_size: int,
+                            workspace: torch.Tensor, max_num_partitions: Optional[int] = None,
+                            k_scale: float = 1.0, v_scale: float = 1.0,
+                            stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Split-K decode that reads each group's shared prompt blocks once: sequences
+    [j*seqs_per_group, (j+1)*seqs_per_group) share their first prefix_lens[j] tokens
+    (int32 [ceil(S / seqs_per_group)], multiples of partition_size).  E4M3 pools
+    (uint8 / float8_e4m3fn) take k_scale and v_scale.  Follow with pa_splitk_reduce."""
+    codes = k_cache.dtype in _CODE_DTYPES
+    dev, S, H, d, N, B, Hk, M, (po, pq, pk, pv, pbt), pcl = _decode_common(
+        out, q, k_cache, v_cache, block_tables, context_lens, codes=codes)
+    ngroups = -(-S // int(seqs_per_group)) if seqs_per_group > 0 else 0
+    if prefix_lens.shape != (ngroups,):
+        raise ValueError(f"prefix_lens must be [{ngroups}] (one entry per group)")
+    P = max_num_partitions or max_num_partitions_for(M, B, partition_size)
+    ws = _need(workspace, "workspace", workspace.dtype, dev)
+    dt = _dtype_code(q)
+    kv = PA_FP8_E4M3 if codes else dt
+    st = _lib.lib().pa_decode_prefix_splitk(
+        po, pq, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N, float(scale), dt, kv, float(k_scale), float(v_scale),
+        int(seqs_per_group), _need(prefix_lens, "prefix_lens", torch.int32, dev), int(partition_size), int(P), ws,
+        workspace.numel() * workspace.element_size(), _stream_ptr(q, stream))
+    _lib.check("pa_decode_prefix_splitk", st)
+
+
 def pa_status_string(status: int) -> str:
     return _lib.status_name(status)
 

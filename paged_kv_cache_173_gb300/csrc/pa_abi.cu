@@ -128,6 +128,8 @@ pa::DecodeArgs decode_args(void* out, const void* q, const void* k_cache, const 
                            int num_blocks, float scale, int dtype, int kv_dtype, float k_scale,
                            float v_scale) {
   pa::DecodeArgs a{};
+  a.prefix_lens = nullptr;
+  a.seqs_per_group = 1;
   a.dtype = dtype;
   a.kv_dtype = kv_dtype;
   a.k_scale = k_scale;
@@ -354,6 +356,45 @@ int pa_decode_splitk_fp8(void* out, const void* q, const void* k_cache, const vo
                      num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, PA_FP8_E4M3,
                      k_scale, v_scale, partition_size, max_num_partitions, workspace, workspace_bytes,
                      stream);
+}
+
+int pa_decode_prefix_splitk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int num_heads,
+                            int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                            float scale, int dtype, int kv_dtype, float k_scale, float v_scale,
+                            int seqs_per_group, const int32_t* prefix_lens, int partition_size,
+                            int max_num_partitions, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (kv_dtype == PA_FP8_E4M3) {
+    const int st = check_fp8_decode(dtype, k_scale, v_scale);
+    if (st != PA_OK) return st;
+  } else if (kv_dtype != dtype) {
+    return fail(PA_ERR_UNSUPPORTED, "kv_dtype %d must equal dtype %d or be PA_FP8_E4M3", kv_dtype, dtype);
+  }
+  int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                        dtype);
+  if (st != PA_OK) return st;
+  st = check_splitk(max_blocks_per_seq, block_size, partition_size, max_num_partitions, workspace,
+                    workspace_bytes, num_seqs, num_heads, head_dim);
+  if (st != PA_OK) return st;
+  if (seqs_per_group <= 0) return fail(PA_ERR_INVALID_ARG, "seqs_per_group %d must be positive", seqs_per_group);
+  if (num_seqs == 0) return ok();
+  if (!prefix_lens) return fail(PA_ERR_INVALID_ARG, "prefix_lens is NULL");
+  if (!aligned(prefix_lens, 4)) return fail(PA_ERR_INVALID_ARG, "prefix_lens must be 4-byte aligned");
+  pa::DecodeArgs a = decode_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                 num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                 dtype, kv_dtype, kv_dtype == PA_FP8_E4M3 ? k_scale : 1.f,
+                                 kv_dtype == PA_FP8_E4M3 ? v_scale : 1.f);
+  a.ws = static_cast<float*>(workspace);
+  a.partition_size = partition_size;
+  a.max_num_partitions = max_num_partitions;
+  a.cluster_size = 0;
+  a.prefix_lens = prefix_lens;
+  a.seqs_per_group = seqs_per_group;
+  return cuda_status(pa::launch_decode_prefix(a, static_cast<cudaStream_t>(stream)),
+                     "shared-prefix decode launch");
 }
 
 int pa_splitk_reduce(void* out, const void* workspace, size_t workspace_bytes,

@@ -75,7 +75,27 @@ struct DecodeParams {
   int max_num_partitions;
   float scale_log2;  // scale * k_scale * log2(e): scores are kept in base-2 units
   float out_scale;   // v_scale of an E4M3 V pool (1 otherwise)
+  // Shared-prefix decode: sequences [j * seqs_per_group, (j + 1) * seqs_per_group)
+  // form group j, whose first prefix_lens[j] tokens sit in the same blocks.
+  const int32_t* prefix_lens;  // null: no shared pass
+  int seqs_per_group;
+  int members_per_cta;  // shared pass: sequences of a group per CTA
+  int subgroups;        // shared pass: CTAs per group along grid z
+  int num_seqs;
 };
+
+enum DecodeMode { MODE_GRID = 0, MODE_CLUSTER = 1, MODE_SHARED = 2 };
+
+// Tokens of a sequence that its group's shared pass covers: the group's
+// prefix length lp when it is a positive multiple of the partition size that
+// both the sequence and the group's first sequence reach (within the
+// table's capacity), else 0.  The shared pass and the per-sequence pass
+// both decide with this function, so they always agree.
+__device__ __forceinline__ int shared_len(int lp, int ctx, int ctx_lead, int cap, int partition_tokens) {
+  const bool ok = lp > 0 && lp % partition_tokens == 0 && lp <= ctx && lp <= ctx_lead && ctx <= cap &&
+                  ctx_lead <= cap;
+  return ok ? lp : 0;
+}
 
 // Shared-memory stage of one 16-token chunk of one KV head: TMA boxes of 16
 // rows x 64 dims (128 bytes per row, 2 KB per box), 128-byte swizzled: the
@@ -144,20 +164,27 @@ struct WarpAcc {
   }
 };
 
-// Query fragments (B operand of S = K Q^T): lane holds head nt*8 + lane/4,
+// Row of q (and of out) of query j of a CTA whose queries start at sequence
+// s0: sequence s0 + j / G, head kvh * G + j % G.  A per-sequence CTA has
+// queries j < G, the heads of one group.
+__device__ __forceinline__ size_t query_row(int s0, int j, int H, int kvh, int G) {
+  return static_cast<size_t>(s0 + j / G) * H + kvh * G + j % G;
+}
+
+// Query fragments (B operand of S = K Q^T): lane holds query nt*8 + lane/4,
 // dims ks*16 + {2c, 2c+1} and ks*16 + {2c+8, 2c+9} with c = lane % 4;
-// heads past the group are zero.
+// queries past nq are zero.
 template <int HEAD_DIM, int NT>
 __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HEAD_DIM / 16][NT][2], const void* q,
-                                             int s, int H, int kvh, int G, int lane) {
+                                             int s0, int H, int kvh, int G, int nq, int lane) {
   const int g = lane >> 2;
   const int c4 = lane & 3;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hq = nt * 8 + g;
-    const bool hv = hq < G;
+    const bool hv = hq < nq;
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        static_cast<const uint16_t*>(q) + (static_cast<size_t>(s) * H + kvh * G + (hv ? hq : 0)) * HEAD_DIM);
+        static_cast<const uint16_t*>(q) + query_row(s0, hv ? hq : 0, H, kvh, G) * HEAD_DIM);
 #pragma unroll
     for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
       qf[ks][nt][0] = hv ? __ldg(qrow + ks * 8 + c4) : 0u;
@@ -171,16 +198,16 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HEAD_DIM / 16][NT][2
 // the key fragments arrive (attend_chunk_e4m3), so each lane loads four
 // consecutive dims at once.
 template <int HEAD_DIM, int NT>
-__device__ __forceinline__ void load_q_frags_e4m3(uint32_t (&qf)[HEAD_DIM / 16][NT][2], const void* q, int s,
-                                                  int H, int kvh, int G, int lane) {
+__device__ __forceinline__ void load_q_frags_e4m3(uint32_t (&qf)[HEAD_DIM / 16][NT][2], const void* q, int s0,
+                                                  int H, int kvh, int G, int nq, int lane) {
   const int g = lane >> 2;
   const int c4 = lane & 3;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hq = nt * 8 + g;
-    const bool hv = hq < G;
+    const bool hv = hq < nq;
     const uint2* qrow = reinterpret_cast<const uint2*>(
-        static_cast<const uint16_t*>(q) + (static_cast<size_t>(s) * H + kvh * G + (hv ? hq : 0)) * HEAD_DIM);
+        static_cast<const uint16_t*>(q) + query_row(s0, hv ? hq : 0, H, kvh, G) * HEAD_DIM);
 #pragma unroll
     for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
       const uint2 v = hv ? __ldg(qrow + ks * 4 + c4) : make_uint2(0u, 0u);
@@ -538,16 +565,24 @@ __device__ __forceinline__ void store_warp_state(const WarpAcc<HEAD_DIM, NT>& ac
   }
 }
 
-// CLUSTER = false: CTA (kvh, part, s) covers partition `part` of
-//   partition_chunks chunks; a sequence with one partition writes `out`,
-//   otherwise the partition's (o, m, l) go to the split-K workspace.
-// CLUSTER = true: gridDim.y CTAs form a cluster per (kvh, s); CTA `part`
+// MODE_GRID: CTA (kvh, part, s) covers partition `part` of partition_chunks
+//   chunks; a sequence with one partition writes `out`, otherwise the
+//   partition's (o, m, l) go to the split-K workspace.  With prefix_lens set,
+//   the partitions that the shared pass covers are skipped.
+// MODE_CLUSTER: gridDim.y CTAs form a cluster per (kvh, s); CTA `part`
 //   takes chunks [part * n / C, (part + 1) * n / C) of the sequence's n chunks
 //   and the cluster merges the C results into `out`.
+// MODE_SHARED: CTA (kvh, part, z) covers partition `part` of the shared
+//   prefix of group z / subgroups for members_per_cta of its sequences
+//   (subgroup z % subgroups): it reads the prefix through the group's first
+//   table row once and scores every member's queries against it, writing
+//   each member's partition row (or `out` for a one-partition sequence).
 // KV: the cache element type, T or E4M3.
-template <typename T, typename KV, int HEAD_DIM, int NT, int WARPS, int STAGES, bool CLUSTER>
+template <typename T, typename KV, int HEAD_DIM, int NT, int WARPS, int STAGES, int MODE>
 __global__ void __launch_bounds__(WARPS * 32)
 paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr bool CLUSTER = MODE == MODE_CLUSTER;
+  constexpr bool SHARED = MODE == MODE_SHARED;
   constexpr bool FP8 = kIsFp8<KV>;
   static_assert(!FP8 || std::is_same<T, __half>::value, "E4M3 caches take float16 queries");
   using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES, kElemBytes<KV>>;
@@ -562,7 +597,6 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 
   const int kvh = blockIdx.x;
   const int part = blockIdx.y;
-  const int s = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
@@ -572,12 +606,40 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   // be running: everything up to here overlapped with its tail.
   grid_dependency_wait();
 
+  // s: the sequence whose table row the CTA reads; ctx: the tokens of that
+  // row it covers; queries j < nq belong to sequence s0 + j / G (query_row).
   // Loads that do not depend on the context length go out first, so that
   // their latencies overlap with the one of context_lens[s].
-  const int ctx = __ldg(p.context_lens + s);
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  const int partition_tokens = p.partition_chunks * CHUNK;
+  int s, s0, ctx, nq = G;
+  int lp = 0, ctx_lead = 0;  // the group's prefix length and first sequence's context
+  if constexpr (SHARED) {
+    const int gi = static_cast<int>(blockIdx.z) / p.subgroups;
+    const int lead = gi * p.seqs_per_group;
+    s0 = lead + (static_cast<int>(blockIdx.z) - gi * p.subgroups) * p.members_per_cta;
+    const int nm = min(min(lead + p.seqs_per_group, p.num_seqs) - s0, p.members_per_cta);
+    lp = __ldg(p.prefix_lens + gi);
+    ctx_lead = __ldg(p.context_lens + lead);
+    s = lead;
+    ctx = shared_len(lp, ctx_lead, ctx_lead, cap, partition_tokens);
+    nq = nm > 0 ? nm * G : 0;
+    if (nq == 0 || ctx == 0) {  // no member here, or the group shares nothing
+      allow_dependent_launch();
+      return;
+    }
+  } else {
+    s = static_cast<int>(blockIdx.z);
+    s0 = s;
+    if (!CLUSTER && p.prefix_lens != nullptr) {
+      const int gi = s / p.seqs_per_group;
+      lp = __ldg(p.prefix_lens + gi);
+      ctx_lead = __ldg(p.context_lens + gi * p.seqs_per_group);
+    }
+    ctx = __ldg(p.context_lens + s);
+  }
   const int cpb_log2 = p.chunks_per_block_log2;
   const int table_chunks = p.max_blocks_per_seq << cpb_log2;
-  const int cap = p.max_blocks_per_seq * p.block_size;
   const bool ctx_bad = ctx < 0 || ctx > cap;
   const int nchunks = ctx_bad ? 0 : (ctx + CHUNK - 1) / CHUNK;
   const int nclu = CLUSTER ? static_cast<int>(gridDim.y) : 1;
@@ -592,9 +654,9 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 
   uint32_t qf[KSTEPS][NT][2];
   if constexpr (FP8) {
-    load_q_frags_e4m3<HEAD_DIM, NT>(qf, p.q, s, H, kvh, G, lane);
+    load_q_frags_e4m3<HEAD_DIM, NT>(qf, p.q, s0, H, kvh, G, nq, lane);
   } else {
-    load_q_frags<HEAD_DIM, NT>(qf, p.q, s, H, kvh, G, lane);
+    load_q_frags<HEAD_DIM, NT>(qf, p.q, s0, H, kvh, G, nq, lane);
   }
 
   // ---- block-table window: lane j holds the physical block of this warp's
@@ -620,6 +682,14 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 
   const int nparts = CLUSTER ? nclu : (nchunks + p.partition_chunks - 1) / p.partition_chunks;
 
+  if constexpr (MODE == MODE_GRID) {
+    // partitions of a shared prefix are written by the shared pass
+    if (part * partition_tokens < shared_len(lp, ctx, ctx_lead, cap, partition_tokens)) {
+      allow_dependent_launch();
+      return;
+    }
+  }
+
   if (nchunks == 0) {
     // Empty sequence -> zeros; impossible context length -> NaN.  Written once.
     if (part == 0) {
@@ -634,9 +704,28 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     allow_dependent_launch();
     return;
   }
-  const bool single = !CLUSTER && nparts == 1;
+  const bool single = MODE == MODE_GRID && nparts == 1;
   const int c1 = CLUSTER ? cmax : min(c0 + p.partition_chunks, nchunks);
   const int nk = first < c1 ? (c1 - first + WARPS - 1) / WARPS : 0;  // <= nk_cap
+
+  // Shared pass: members whose table entries over this partition differ from
+  // the first sequence's get NaN (one bit per member of the CTA).
+  int* mismatch = reinterpret_cast<int*>(smem + Cfg::BAR_BYTES - sizeof(int));
+  if constexpr (SHARED) {
+    static_assert(WARPS * STAGES * 8 + sizeof(int) <= Cfg::BAR_BYTES, "barrier area");
+    if (threadIdx.x == 0) *mismatch = 0;
+    __syncthreads();
+    const int blk0 = c0 >> cpb_log2;
+    const int nblk = ((c1 - 1) >> cpb_log2) - blk0 + 1;
+    const int nm = nq / G;
+    const int32_t* lead_row = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq + blk0;
+    for (int i = threadIdx.x; i < nm * nblk; i += WARPS * 32) {
+      const int mi = i / nblk;
+      const int b = i - mi * nblk;
+      const int32_t* row = p.block_tables + static_cast<size_t>(s0 + mi) * p.max_blocks_per_seq + blk0;
+      if (__ldg(row + b) != __ldg(lead_row + b)) atomicOr(mismatch, 1 << mi);
+    }
+  }
 
   // A stage holds CPS of the warp's chunks (its k-th chunk is chunk
   // first + k * WARPS of the range); `issued` and `consumed` count stages.
@@ -741,8 +830,8 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
   for (int w = 0; w < WARPS; ++w) any_bad |= mbad[w] != 0;
 
-  for (int idx = threadIdx.x; idx < G * HEAD_DIM; idx += WARPS * 32) {
-    const int head = idx / HEAD_DIM;
+  for (int idx = threadIdx.x; idx < nq * HEAD_DIM; idx += WARPS * 32) {
+    const int head = idx / HEAD_DIM;  // the CTA's query
     const int d = idx - head * HEAD_DIM;
     float M = -INFINITY;
 #pragma unroll
@@ -758,8 +847,23 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     }
     float r = any_bad ? NAN : (L > 0.f ? O / L : 0.f);
     if constexpr (FP8) r *= p.out_scale;  // V codes times v_scale
-    const size_t qrow = static_cast<size_t>(s) * H + kvh * G + head;
-    if (CLUSTER) {
+    const size_t qrow = query_row(s0, head, H, kvh, G);
+    if constexpr (SHARED) {
+      const int m = s0 + head / G;  // the member sequence
+      const int ctx_m = __ldg(p.context_lens + m);
+      if (shared_len(lp, ctx_m, ctx_lead, cap, partition_tokens) == 0) continue;  // decoded on its own
+      const bool nan = any_bad || ((*mismatch >> (head / G)) & 1);
+      if (ctx_m <= partition_tokens) {  // one partition in all: this is the result
+        static_cast<T*>(p.out)[qrow * HEAD_DIM + d] = to_elem<T>(nan ? NAN : r);
+      } else {
+        const size_t row = qrow * p.max_num_partitions + part;
+        p.ws_o[row * HEAD_DIM + d] = nan ? NAN : r;
+        if (d == 0) {
+          p.ws_m[row] = nan ? 0.f : M;
+          p.ws_l[row] = nan ? 1.f : L;
+        }
+      }
+    } else if (CLUSTER) {
       // an empty CTA publishes m = -inf, l = 0: weight 0 in the cluster merge
       float* cta = reinterpret_cast<float*>(ring + Cfg::CTA_OFFSET);
       cta[head * HEAD_DIM + d] = r;
@@ -1121,23 +1225,44 @@ cudaError_t fill_decode_params(const DecodeArgs& a, DecodeParams* pp) {
   const bool fp8 = kIsFp8<KV>;
   p.scale_log2 = a.scale * (fp8 ? a.k_scale : 1.f) * 1.4426950408889634f;
   p.out_scale = fp8 ? a.v_scale : 1.f;
+  p.prefix_lens = a.prefix_lens;
+  p.seqs_per_group = a.seqs_per_group > 0 ? a.seqs_per_group : 1;
+  p.members_per_cta = 1;
+  p.subgroups = 1;
+  p.num_seqs = a.num_seqs;
   return cudaSuccess;
 }
 
-template <typename T, typename KV, int HEAD_DIM, int NT, bool CLUSTER>
+// Members of a group whose queries one shared-pass CTA holds: as many whole
+// query groups as fit in 8 * NT query rows, at most the group size.
+template <int NT>
+int members_per_cta(const DecodeArgs& a) {
+  const int G = a.num_heads / a.num_kv_heads;
+  return std::max(1, std::min(a.seqs_per_group, 8 * NT / G));
+}
+
+template <typename T, typename KV, int HEAD_DIM, int NT, int MODE>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr bool CLUSTER = MODE == MODE_CLUSTER;
   constexpr int ELEM = kElemBytes<KV>;
   constexpr int WARPS = DecodeShape<HEAD_DIM, ELEM>::WARPS;
   constexpr int STAGES = DecodeShape<HEAD_DIM, ELEM>::STAGES;
   using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES, ELEM>;
-  auto kern = paged_decode_kernel<T, KV, HEAD_DIM, NT, WARPS, STAGES, CLUSTER>;
+  auto kern = paged_decode_kernel<T, KV, HEAD_DIM, NT, WARPS, STAGES, MODE>;
   static std::atomic<uint64_t> smem_set{0};
   cudaError_t e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return e;
   DecodeParams p;
   e = fill_decode_params<T, KV, HEAD_DIM>(a, &p);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_kv_heads, CLUSTER ? a.cluster_size : a.max_num_partitions, a.num_seqs);
+  unsigned gz = static_cast<unsigned>(a.num_seqs);
+  if constexpr (MODE == MODE_SHARED) {
+    const int groups = (a.num_seqs + p.seqs_per_group - 1) / p.seqs_per_group;
+    p.members_per_cta = members_per_cta<NT>(a);
+    p.subgroups = (std::min(a.seqs_per_group, a.num_seqs) + p.members_per_cta - 1) / p.members_per_cta;
+    gz = static_cast<unsigned>(groups) * static_cast<unsigned>(p.subgroups);
+  }
+  dim3 grid(a.num_kv_heads, CLUSTER ? a.cluster_size : a.max_num_partitions, gz);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(WARPS * 32);
@@ -1179,7 +1304,7 @@ cudaError_t decode_slots(int* slots) {
       return cudaSuccess;
     }
   }
-  auto kern = paged_decode_kernel<T, KV, HEAD_DIM, NT, WARPS, STAGES, false>;
+  auto kern = paged_decode_kernel<T, KV, HEAD_DIM, NT, WARPS, STAGES, MODE_GRID>;
   static std::atomic<uint64_t> smem_set{0};
   e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return e;
@@ -1200,8 +1325,8 @@ cudaError_t decode_slots(int* slots) {
 template <typename T, typename KV, int HEAD_DIM, int NT>
 cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
   if (a.cluster_size >= 0) {
-    return a.cluster_size > 0 ? launch_decode_t<T, KV, HEAD_DIM, NT, true>(a, stream)
-                              : launch_decode_t<T, KV, HEAD_DIM, NT, false>(a, stream);
+    return a.cluster_size > 0 ? launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER>(a, stream)
+                              : launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID>(a, stream);
   }
   int slots = 0;
   cudaError_t e = decode_slots<T, KV, HEAD_DIM, NT>(&slots);
@@ -1214,9 +1339,9 @@ cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
   b.cluster_size = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(8, k)));
   if (b.cluster_size == 1) {
     b.cluster_size = 0;
-    return launch_decode_t<T, KV, HEAD_DIM, NT, false>(b, stream);
+    return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID>(b, stream);
   }
-  return launch_decode_t<T, KV, HEAD_DIM, NT, true>(b, stream);
+  return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER>(b, stream);
 }
 
 template <typename T, int HEAD_DIM>
@@ -1267,6 +1392,35 @@ cudaError_t launch_decode_typed(const DecodeArgs& a, cudaStream_t stream) {
     case 128:
       return two ? launch_decode_auto<T, KV, 128, 2>(a, stream) : launch_decode_auto<T, KV, 128, 1>(a, stream);
     case 256: return two ? cudaErrorInvalidValue : launch_decode_auto<T, KV, 256, 1>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Shared-prefix split-K: the shared pass (query tiles of NTS x 8 rows: the
+// members of a group times G), then the per-sequence pass, which skips the
+// partitions the shared pass wrote.
+template <typename T, typename KV, int HEAD_DIM, int NTS, int NT>
+cudaError_t launch_prefix_t(const DecodeArgs& a, cudaStream_t stream) {
+  cudaError_t e = launch_decode_t<T, KV, HEAD_DIM, NTS, MODE_SHARED>(a, stream);
+  if (e != cudaSuccess) return e;
+  return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID>(a, stream);
+}
+
+template <typename T, typename KV = T>
+cudaError_t launch_decode_prefix_typed(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  const int G = a.num_heads / a.num_kv_heads;
+  const bool two = G > 8;
+  // one query tile when a whole group's queries fit in 8 rows, else two
+  const bool two_s = std::min(a.seqs_per_group, 16 / G) * G > 8;
+  switch (a.head_dim) {
+    case 64:
+      if (two) return launch_prefix_t<T, KV, 64, 2, 2>(a, stream);
+      return two_s ? launch_prefix_t<T, KV, 64, 2, 1>(a, stream) : launch_prefix_t<T, KV, 64, 1, 1>(a, stream);
+    case 128:
+      if (two) return launch_prefix_t<T, KV, 128, 2, 2>(a, stream);
+      return two_s ? launch_prefix_t<T, KV, 128, 2, 1>(a, stream) : launch_prefix_t<T, KV, 128, 1, 1>(a, stream);
+    case 256: return two ? cudaErrorInvalidValue : launch_prefix_t<T, KV, 256, 1, 1>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

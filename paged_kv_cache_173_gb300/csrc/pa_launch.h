@@ -58,6 +58,8 @@ struct DecodeArgs {
   int max_num_partitions;  // grid extent along partitions (split-K)
   int cluster_size;        // > 0: one cluster of this many CTAs per (sequence, KV head);
                            // 0: plain grid; < 0: chosen from occupancy
+  const int32_t* prefix_lens;  // shared-prefix split-K: [ceil(num_seqs / seqs_per_group)], else null
+  int seqs_per_group;
 };
 
 struct ReduceArgs {
@@ -89,6 +91,9 @@ cudaError_t launch_splitk_reduce_f16(const ReduceArgs& a, cudaStream_t stream);
 cudaError_t launch_splitk_reduce_bf16(const ReduceArgs& a, cudaStream_t stream);
 // E4M3 caches with float16 queries (pa_decode_fp8.cu)
 cudaError_t launch_decode_f16_e4m3(const DecodeArgs& a, cudaStream_t stream);
+// shared-prefix split-K (pa_decode_prefix.cu): the shared pass, then the
+// per-sequence pass
+cudaError_t launch_decode_prefix(const DecodeArgs& a, cudaStream_t stream);
 
 // Workspace geometry shared by the partition kernel and the reduce kernel:
 // o [S][H][P][d], then m [S][H][P], then l [S][H][P], float32.

@@ -86,6 +86,8 @@ class PagedBatch:
     unique_blocks: int  # distinct physical blocks referenced by the tables
     dtype: str = "fp16"  # "fp16": float16 arrays; "bf16": uint16 bfloat16 bit patterns
     kv_dtype: str = ""  # "": the caches have `dtype`; "fp8": uint8 E4M3 codes scaled by k/v_scale
+    seqs_per_group: int = 1  # sequences [j*g, (j+1)*g) form group j ...
+    prefix_lens: Optional[np.ndarray] = None  # ... sharing their first prefix_lens[j] tokens (int32)
     k_scale: float = 1.0
     v_scale: float = 1.0
 
@@ -139,7 +141,9 @@ def build_batch(
     ``share_groups``: lists of sequence indices whose first
     ``shared_prefix_len`` tokens (a whole number of blocks) live in the same
     physical blocks (parallel sampling from one prompt).  The first sequence of
-    a group draws the prefix blocks; the others point at them.
+    a group draws the prefix blocks; the others point at them.  When the groups
+    are consecutive runs of one size g, the batch records g and the shared
+    length per group (``seqs_per_group``, ``prefix_lens``).
     """
     if rng is None:
         rng = np.random.default_rng(seed)
@@ -234,6 +238,14 @@ def build_batch(
         kb[~valid] = nan
         vb[~valid] = nan
 
+    seqs_per_group, prefix_lens = 1, None
+    if share_groups:
+        g = len(share_groups[0])
+        if all(list(grp) == list(range(i * g, i * g + len(grp))) for i, grp in enumerate(share_groups)) and \
+                all(len(grp) == g for grp in share_groups[:-1]) and len(share_groups) == -(-S // g):
+            seqs_per_group = g
+            prefix_lens = np.full(len(share_groups), shared_prefix_len, dtype=np.int32)
+
     return PagedBatch(
         name=name, num_seqs=S, num_heads=H, num_kv_heads=Hk, head_dim=d, block_size=B,
         num_blocks=N, max_blocks_per_seq=M, scale=float(np.float32(1.0 / math.sqrt(d))),
@@ -241,7 +253,7 @@ def build_batch(
         context_lens=ctx.astype(np.int32), key=key, value=value, slot_mapping=slot_mapping,
         partition_size=int(partition_size), unique_blocks=int(unique_blocks), dtype=dtype,
         kv_dtype=kv_dtype, k_scale=FP8_SCALE if kv_dtype == "fp8" else 1.0,
-        v_scale=FP8_SCALE if kv_dtype == "fp8" else 1.0,
+        v_scale=FP8_SCALE if kv_dtype == "fp8" else 1.0, seqs_per_group=seqs_per_group, prefix_lens=prefix_lens,
     )
 
 

@@ -46,6 +46,9 @@ def lib() -> ctypes.CDLL:
                                                       ctypes.c_float, ctypes.c_float]
         L.pa_oracle_reshape_and_cache_fp8.restype = _I
         L.pa_oracle_decode.restype = _I
+        L.pa_oracle_prefill.argtypes = [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I64,
+                                        ctypes.c_double, _I, _I, _I, ctypes.c_double, ctypes.c_double]
+        L.pa_oracle_prefill.restype = _I
         L.pa_oracle_copy_blocks.argtypes = [_P, _P, _P, _I64, _I64, _I, _I, _I]
         L.pa_oracle_copy_blocks.restype = _I
         L.pa_oracle_max_threads.argtypes = []
@@ -180,6 +183,33 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables
                                 float(v_scale))
     if rc:
         raise OracleError(f"decode precondition failed ({rc})")
+    return out
+
+
+def prefill(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables: np.ndarray,
+            context_lens: np.ndarray, query_start_loc: np.ndarray, scale: float, num_threads: int = 0,
+            dtype: str = "fp16", k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
+    """float64 prefill output [rows, H, d]: row i of sequence s (rows
+    query_start_loc[s] .. query_start_loc[s+1]) attends causally up to its
+    position ctx - qlen + i.  Element types as decode()."""
+    cache_dtype = "fp8" if k_cache.dtype == np.uint8 else dtype
+    assert q.itemsize == 2 and k_cache.dtype == v_cache.dtype
+    q = np.ascontiguousarray(q)
+    k_cache = np.ascontiguousarray(k_cache)
+    v_cache = np.ascontiguousarray(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    R, H, d = q.shape
+    N, B, Hk, _ = k_cache.shape
+    S = int(cl.size)
+    assert qsl.size == S + 1 and int(qsl[-1]) == R
+    out = np.zeros((R, H, d), dtype=np.float64)
+    rc = lib().pa_oracle_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), int(bt.shape[1]),
+                                 _ptr(cl), _ptr(qsl), S, H, Hk, d, B, N, float(scale), int(num_threads),
+                                 DTYPES[dtype], DTYPES[cache_dtype], float(k_scale), float(v_scale))
+    if rc:
+        raise OracleError(f"prefill precondition failed ({rc})")
     return out
 
 

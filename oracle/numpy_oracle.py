@@ -75,3 +75,18 @@ def copy_blocks(k_cache, v_cache, block_mapping):
             kc[dst] = kc[src]
             vc[dst] = vc[src]
     return kc, vc
+
+
+def prefill_bruteforce(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale) -> np.ndarray:
+    """Prefill, row by row: row i of sequence s sits at position
+    ctx - qlen + i and is decode attention over positions 0..that position."""
+    q = np.asarray(q)
+    out = np.zeros(q.shape, dtype=np.float64)
+    for s in range(len(context_lens)):
+        r0, r1 = int(query_start_loc[s]), int(query_start_loc[s + 1])
+        ctx = int(context_lens[s])
+        for i, r in enumerate(range(r0, r1)):
+            pos = ctx - (r1 - r0) + i
+            out[r] = decode_bruteforce(q[r:r + 1], k_cache, v_cache, np.asarray(block_tables)[s:s + 1],
+                                       [pos + 1], scale)[0]
+    return out

@@ -34,6 +34,12 @@
  *    h / (num_heads / num_kv_heads) (grouped-query attention with consecutive
  *    groups; the pages do not fix the mapping).
  *
+ *  - Prefill: each query row of a prompt (or of a chunk of it) attends to
+ *    every earlier position of its sequence and to its own; with the
+ *    queries' own K/V already in the cache, a row at position p is decode
+ *    attention over the first p + 1 tokens ("in-depth reading", section
+ *    5.1, item 5; "vAttention", paged prefill).
+ *
  *  - FP8 caches: the block's contents are compressed and the attention
  *    kernel dequantises them ("PagedAttention: when the KV cache meets OS
  *    paging", section 6, the layer diagram).  The page names FP8 and nothing
@@ -376,6 +382,61 @@ int pa_oracle_decode(double* out, const uint16_t* q, const void* k_cache, const 
 #pragma omp critical
 #endif
             rc = r;
+        }
+    }
+    return rc;
+}
+
+/* Paged prefill, whole or chunked.  Sequence s has query rows [qsl[s],
+ * qsl[s + 1]) of q and out (qlen rows), and context_lens[s] tokens in its
+ * table, the last qlen of which are the queries' own tokens (written to the
+ * cache beforehand).  Query row i of the sequence sits at position
+ * pos = ctx - qlen + i and attends to positions 0..pos, its own included
+ * (the causal order of the prompt; "Efficient Memory Management for LLM
+ * Serving with PagedAttention -- in-depth reading", section 5.1, item 5:
+ * chunked prefill; "vAttention", the paged prefill kernels it measures).
+ * Each (row, head) is therefore decode attention over the first pos + 1
+ * tokens of the table, computed by decode_one.
+ * out: [total_rows][num_heads][head_dim] float64; q: the same shape in
+ * dtype 0 / 1 bit patterns; caches as pa_oracle_decode. */
+int pa_oracle_prefill(double* out, const uint16_t* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                      const int32_t* query_start_loc, int num_seqs, int num_heads, int num_kv_heads,
+                      int head_dim, int block_size, int64_t num_blocks, double scale, int num_threads,
+                      int dtype, int cache_dtype, double k_scale, double v_scale) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || num_heads % num_kv_heads != 0 ||
+        (dtype != ORACLE_FP16 && dtype != ORACLE_BF16) || cache_dtype < 0 || cache_dtype > 2)
+        return ORACLE_BAD_ARG;
+    if (num_seqs > 0 && query_start_loc[0] != 0) return ORACLE_BAD_ARG;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int qlen = query_start_loc[s + 1] - query_start_loc[s];
+        if (qlen < 0 || qlen > context_lens[s]) return ORACLE_BAD_CONTEXT;
+    }
+    const int group = num_heads / num_kv_heads;
+    const int64_t rows = num_seqs > 0 ? query_start_loc[num_seqs] : 0;
+    const int64_t work = rows * num_heads;
+    int rc = ORACLE_OK;
+#ifdef _OPENMP
+    const int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nt)
+#endif
+    for (int64_t w = 0; w < work; ++w) {
+        const int64_t r = w / num_heads;
+        const int h = (int)(w % num_heads);
+        int s = 0;  /* the sequence of row r: the last s with query_start_loc[s] <= r */
+        while (s + 1 < num_seqs && query_start_loc[s + 1] <= r) ++s;
+        const int qlen = query_start_loc[s + 1] - query_start_loc[s];
+        const int pos = context_lens[s] - qlen + (int)(r - query_start_loc[s]);
+        const int e = decode_one(out + w * head_dim, q + w * head_dim, k_cache, v_cache,
+                                 block_tables + (int64_t)s * max_blocks_per_seq, max_blocks_per_seq, pos + 1,
+                                 num_kv_heads, h / group, head_dim, block_size, num_blocks, scale, dtype,
+                                 cache_dtype, k_scale, v_scale);
+        if (e != ORACLE_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            rc = e;
         }
     }
     return rc;

@@ -90,6 +90,9 @@ class PagedBatch:
     prefix_lens: Optional[np.ndarray] = None  # ... sharing their first prefix_lens[j] tokens (int32)
     k_scale: float = 1.0
     v_scale: float = 1.0
+    # prefill batches: q is [T, H, d], rows query_start_loc[s] .. query_start_loc[s+1]
+    # belong to sequence s (its last qlen positions); None for decode batches
+    query_start_loc: Optional[np.ndarray] = None
 
     @property
     def group_size(self) -> int:
@@ -255,6 +258,97 @@ def build_batch(
         kv_dtype=kv_dtype, k_scale=FP8_SCALE if kv_dtype == "fp8" else 1.0,
         v_scale=FP8_SCALE if kv_dtype == "fp8" else 1.0, seqs_per_group=seqs_per_group, prefix_lens=prefix_lens,
     )
+
+
+def build_prefill_batch(
+    *,
+    name: str,
+    seed: int,
+    context_lens: Sequence[int],
+    query_lens: Sequence[int],
+    num_heads: int,
+    num_kv_heads: int,
+    head_dim: int,
+    block_size: int,
+    max_blocks_per_seq: Optional[int] = None,
+    pool_factor: float = 1.25,
+    poison: bool = True,
+    rng: Optional[np.random.Generator] = None,
+    dtype: str = "fp16",
+    kv_dtype: str = "",
+) -> PagedBatch:
+    """One prefill step: sequence s has context_lens[s] tokens, of which the
+    last query_lens[s] are new (a whole prompt when they are equal, a chunk of
+    one otherwise).  Draw order: a permutation of the physical ids, q [T, H, d]
+    (T = sum of query_lens), the K pool, the V pool, the new tokens' K and V.
+    The new tokens' slots (and every slot past a context) hold NaN until the
+    cache write fills them."""
+    rng = rng or np.random.default_rng(seed)
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    ql = np.asarray(query_lens, dtype=np.int64)
+    S = int(ctx.size)
+    assert ql.size == S and (ql >= 0).all() and (ql <= ctx).all()
+    B, Hk, H, d = int(block_size), int(num_kv_heads), int(num_heads), int(head_dim)
+    assert H % Hk == 0 and dtype in ("fp16", "bf16") and kv_dtype in ("", "fp8")
+    assert kv_dtype == "" or dtype == "fp16"
+    nblk = [(int(c) + B - 1) // B for c in ctx]
+    M = int(max_blocks_per_seq or max(1, max(nblk)))
+    assert all(n <= M for n in nblk)
+    need = sum(nblk)
+    N = max(need + 1, int(math.ceil(need * pool_factor)))
+    perm = rng.permutation(N).astype(np.int32)
+    tables = np.full((S, M), -1, dtype=np.int32)
+    nxt = 0
+    for s in range(S):
+        tables[s, :nblk[s]] = perm[nxt:nxt + nblk[s]]
+        nxt += nblk[s]
+    T = int(ql.sum())
+    qsl = np.zeros(S + 1, dtype=np.int32)
+    qsl[1:] = np.cumsum(ql)
+    q = _normal_f16(rng, (T, H, d), dtype=dtype)
+    if kv_dtype == "fp8":
+        k_cache = f32_to_e4m3_codes(_normal_f16(rng, (N, B, Hk, d)).astype(np.float32) / np.float32(FP8_SCALE))
+        v_cache = f32_to_e4m3_codes(_normal_f16(rng, (N, B, Hk, d)).astype(np.float32) / np.float32(FP8_SCALE))
+    else:
+        k_cache = _normal_f16(rng, (N, B, Hk, d), dtype=dtype)
+        v_cache = _normal_f16(rng, (N, B, Hk, d), dtype=dtype)
+    key = _normal_f16(rng, (T, Hk, d), dtype=dtype)
+    value = _normal_f16(rng, (T, Hk, d), dtype=dtype)
+    slot_mapping = np.empty(T, dtype=np.int64)
+    for s in range(S):
+        for i in range(int(ql[s])):
+            pos = int(ctx[s] - ql[s]) + i
+            slot_mapping[qsl[s] + i] = int(tables[s, pos // B]) * B + pos % B
+    if poison:
+        valid = np.zeros((N, B), dtype=bool)
+        for s in range(S):
+            for pos in range(int(ctx[s] - ql[s])):  # the cached part
+                valid[tables[s, pos // B], pos % B] = True
+        if kv_dtype == "fp8":
+            kb, vb, nan = k_cache, v_cache, E4M3_NAN_BITS
+        else:
+            kb, vb = k_cache.view(np.uint16), v_cache.view(np.uint16)
+            nan = FP16_NAN_BITS if dtype == "fp16" else BF16_NAN_BITS
+        kb[~valid] = nan
+        vb[~valid] = nan
+    return PagedBatch(
+        name=name, num_seqs=S, num_heads=H, num_kv_heads=Hk, head_dim=d, block_size=B, num_blocks=N,
+        max_blocks_per_seq=M, scale=float(np.float32(1.0 / math.sqrt(d))), q=q, k_cache=k_cache,
+        v_cache=v_cache, block_tables=tables, context_lens=ctx.astype(np.int32), key=key, value=value,
+        slot_mapping=slot_mapping, partition_size=0, unique_blocks=int(need), dtype=dtype, kv_dtype=kv_dtype,
+        k_scale=FP8_SCALE if kv_dtype == "fp8" else 1.0, v_scale=FP8_SCALE if kv_dtype == "fp8" else 1.0,
+        query_start_loc=qsl)
+
+
+def prefill_flops(batch: PagedBatch) -> int:
+    """Multiply-adds of QK^T and PV, times 2: each query row at position p
+    scores p + 1 keys and sums p + 1 values, per head, over d dims."""
+    ctx = batch.context_lens.astype(np.int64)
+    ql = np.diff(batch.query_start_loc.astype(np.int64))
+    keys = 0
+    for c, n in zip(ctx, ql):  # rows at positions c-n .. c-1 see c-n+1 .. c keys
+        keys += n * (c - n) + n * (n + 1) // 2
+    return int(4 * batch.head_dim * batch.num_heads * keys)
 
 
 # ---------------------------------------------------------------------------

@@ -619,3 +619,106 @@ def test_copy_blocks_of_one_byte_pools_matches_the_numpy_statement():
     want = numpy_oracle.copy_blocks(k, v, m)
     assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1])
     assert np.array_equal(got[0][3], k[0]) and np.array_equal(got[1][5], v[2])
+
+
+# --------------------------------------------------------------------------
+# prefill (whole prompts and chunks of them)
+# --------------------------------------------------------------------------
+
+def _prefill_batch(seed, ctx, qlen, H=4, Hk=2, d=64, B=16):
+    return workloads.build_prefill_batch(name="pf", seed=seed, context_lens=ctx, query_lens=qlen, num_heads=H,
+                                         num_kv_heads=Hk, head_dim=d, block_size=B)
+
+
+def _causal_sdpa(q, K, V, first_pos, scale, group, flag=False):
+    """Library attention of one sequence's query rows q [n, H, d] at positions
+    first_pos.. over K/V [ctx, Hk, d], with a boolean causal mask (or, for a
+    whole prompt, the library's own causal flag)."""
+    n = q.shape[0]
+    ctx = K.shape[0]
+    qt = torch.from_numpy(np.asarray(q, dtype=np.float64)).permute(1, 0, 2)[None]
+    kt = torch.from_numpy(np.asarray(K, dtype=np.float64)).permute(1, 0, 2).repeat_interleave(group, dim=0)[None]
+    vt = torch.from_numpy(np.asarray(V, dtype=np.float64)).permute(1, 0, 2).repeat_interleave(group, dim=0)[None]
+    if flag:
+        assert first_pos == 0 and n == ctx
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True, scale=float(scale))
+    else:
+        mask = torch.from_numpy(np.arange(ctx)[None, :] <= (first_pos + np.arange(n))[:, None])
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=float(scale))
+    return o[0].permute(1, 0, 2).numpy()
+
+
+def _prefill_pins(prefill_fn):
+    """Names of the prefill pins that `prefill_fn(q, kc, vc, bt, cl, qsl, scale)` fails."""
+    failed = []
+    # library attention with a causal mask: whole prompts and chunks, GQA 2
+    b = _prefill_batch(41, ctx=[1, 37, 40, 23], qlen=[1, 37, 9, 1])
+    kc, vc = _written(b)
+    got = prefill_fn(b.q, kc, vc, b.block_tables, b.context_lens, b.query_start_loc, b.scale)
+    qsl = b.query_start_loc
+    for s in range(b.num_seqs):
+        c, n = int(b.context_lens[s]), int(qsl[s + 1] - qsl[s])
+        K = np.stack([kc[b.block_tables[s, t // 16], t % 16] for t in range(c)]).astype(np.float64)
+        V = np.stack([vc[b.block_tables[s, t // 16], t % 16] for t in range(c)]).astype(np.float64)
+        ref = _causal_sdpa(b.q[qsl[s]:qsl[s + 1]], K, V, c - n, b.scale, b.group_size, flag=(c == n))
+        if not (np.isfinite(got[qsl[s]:qsl[s + 1]]).all() and
+                np.allclose(got[qsl[s]:qsl[s + 1]], ref, rtol=0, atol=1e-12)):
+            failed.append(f"library-causal-{s}")
+    # the first row of a whole prompt returns V[0] exactly
+    s = 1
+    v0 = vc[b.block_tables[s, 0], 0].astype(np.float64)
+    if not np.array_equal(got[qsl[s]], np.repeat(v0, b.group_size, axis=0)):
+        failed.append("first-row")
+    return failed
+
+
+def test_prefill_pins_pass_on_both_oracles():
+    assert _prefill_pins(c_oracle.prefill) == []
+    assert _prefill_pins(numpy_oracle.prefill_bruteforce) == []
+
+
+@pytest.mark.parametrize("mutant", ["not_causal", "exclusive", "chunk_offset_ignored"])
+def test_prefill_pins_catch_planted_mistakes(mutant):
+    def mutated(q, kc, vc, bt, cl, qsl, scale):
+        cl = np.asarray(cl)
+        if mutant == "not_causal":  # every row reads the whole context
+            rows = np.repeat(np.arange(len(cl)), np.diff(qsl))
+            return numpy_oracle.decode_bruteforce(q, kc, vc, np.asarray(bt)[rows], cl[rows], scale)
+        out = np.zeros(q.shape, dtype=np.float64)
+        for s in range(len(cl)):
+            for i, r in enumerate(range(qsl[s], qsl[s + 1])):
+                pos = (cl[s] - (qsl[s + 1] - qsl[s]) + i) if mutant == "exclusive" else i
+                n = pos if mutant == "exclusive" else pos + 1
+                out[r] = numpy_oracle.decode_bruteforce(q[r:r + 1], kc, vc, np.asarray(bt)[s:s + 1], [n], scale)[0]
+        return out
+    assert _prefill_pins(mutated) != []
+
+
+def test_prefill_rows_ignore_every_later_key():
+    b = _prefill_batch(42, ctx=[60], qlen=[60])
+    kc, vc = _written(b)
+    base = c_oracle.prefill(b.q, kc, vc, b.block_tables, b.context_lens, b.query_start_loc, b.scale)
+    p = 29
+    kc2, vc2 = kc.copy(), vc.copy()
+    for t in range(p + 1, 60):  # change every key and value after position p
+        blk = b.block_tables[0, t // 16]
+        kc2[blk, t % 16] = np.float16(3.0)
+        vc2[blk, t % 16] = np.float16(-7.0)
+    moved = c_oracle.prefill(b.q, kc2, vc2, b.block_tables, b.context_lens, b.query_start_loc, b.scale)
+    assert np.array_equal(base[:p + 1], moved[:p + 1])
+    assert not np.array_equal(base[p + 1:], moved[p + 1:])
+
+
+def test_one_row_chunks_equal_decode():
+    b = _prefill_batch(43, ctx=[5, 70, 33], qlen=[1, 1, 1], H=8, Hk=2)
+    kc, vc = _written(b)
+    pf = c_oracle.prefill(b.q, kc, vc, b.block_tables, b.context_lens, b.query_start_loc, b.scale)
+    dec = c_oracle.decode(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+    assert np.array_equal(pf, dec)
+
+
+def test_prefill_flops_count_the_causal_triangle():
+    b = _prefill_batch(44, ctx=[5, 40, 33], qlen=[5, 8, 1])
+    # keys seen: 1+2+3+4+5, then 8 rows seeing 33..40, then one row seeing 33
+    keys = 15 + sum(range(33, 41)) + 33
+    assert workloads.prefill_flops(b) == 4 * b.head_dim * b.num_heads * keys

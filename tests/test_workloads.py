@@ -88,3 +88,20 @@ def test_llama2_70b_batch(bs):
     b = workloads.llama2_70b(num_seqs=2, ctx=1000, block_size=bs)
     _check_common(b)
     assert b.group_size == 8 and b.block_size == bs
+
+
+def test_prefill_batch_layout_and_poison():
+    b = workloads.build_prefill_batch(name="pf", seed=3, context_lens=[20, 50, 16], query_lens=[20, 7, 1],
+                                      num_heads=4, num_kv_heads=2, head_dim=64, block_size=16)
+    assert list(b.query_start_loc) == [0, 20, 27, 28]
+    assert b.q.shape == (28, 4, 64) and b.key.shape == (28, 2, 64)
+    # each new token's slot is its position in its sequence's table, and holds NaN before the write
+    for s, (c, n) in enumerate([(20, 20), (50, 7), (16, 1)]):
+        for i in range(n):
+            pos = c - n + i
+            slot = b.slot_mapping[b.query_start_loc[s] + i]
+            assert slot == b.block_tables[s, pos // 16] * 16 + pos % 16
+            assert np.isnan(b.k_cache.reshape(-1, 2, 64)[slot]).all()
+        for pos in range(c - n):  # the cached part is finite
+            blk = b.block_tables[s, pos // 16]
+            assert np.isfinite(b.k_cache[blk, pos % 16]).all()

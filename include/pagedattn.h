@@ -259,6 +259,47 @@ int pa_decode_prefix_splitk(void* out, const void* q, const void* k_cache, const
                             void* stream);
 
 /*
+ * pa_prefill -- paged attention for prompt tokens: whole prompts, or chunks
+ * of them appended to a cached context (chunked prefill).
+ *
+ * Prefill computes attention for many new tokens of a sequence at once; each
+ * attends to every earlier position of its sequence and to its own ("in-depth
+ * reading", section 5.1, item 5: chunked prefill; "vAttention: dynamic memory
+ * management without PagedAttention", the paged prefill kernels it measures).
+ * The keys and values come from the pools through the block table, as in
+ * decode; write the new tokens' K/V first with pa_reshape_and_cache.
+ *
+ * Sequence s owns query rows [query_start_loc[s], query_start_loc[s + 1]) of
+ * q and out (qlen rows, 0 <= qlen <= context_lens[s]); its last qlen
+ * positions are those rows' tokens.  Row i sits at position
+ * p = context_lens[s] - qlen + i, and
+ *
+ *   out[row][h][:] = sum_{k <= p} softmax_k(scale * q[row][h] . K_k) * V_k,
+ *
+ * with K_k, V_k the pool rows of position k of sequence s, KV head h / G.
+ *
+ *   q, out            [rows][num_heads][head_dim] of dtype, rows =
+ *                     query_start_loc[num_seqs]
+ *   query_start_loc   [num_seqs + 1] int32, non-decreasing, starting at 0
+ *   max_query_len     >= every qlen (sizes the grid; rows past it are not
+ *                     computed)
+ *   head_dim          64 or 128; num_heads / num_kv_heads must divide 64
+ *
+ * Other arguments as pa_decode.  Scores, softmax and accumulation are
+ * float32; the attention weights enter P.V rounded to dtype.
+ *
+ * Device-value outcomes: a context length below qlen or above
+ * max_blocks_per_seq * block_size, or a block id read from the table outside
+ * [0, num_blocks), gives NaN in the affected rows.  A sequence with qlen <= 0
+ * writes nothing.  Nothing is read out of bounds.
+ */
+int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+               const int32_t* query_start_loc, int num_seqs, int max_query_len, int num_heads,
+               int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale, int dtype,
+               void* stream);
+
+/*
  * pa_splitk_reduce -- merge the partitions left by pa_decode_splitk.
  *
  * For each (s, h) whose sequence has P = ceil(context_lens[s] /

@@ -259,6 +259,29 @@ def pa_decode_prefix_splitk(out: torch.Tensor, q: torch.Tensor, k_cache: torch.T
     _lib.check("pa_decode_prefix_splitk", st)
 
 
+def pa_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+               block_tables: torch.Tensor, context_lens: torch.Tensor, query_start_loc: torch.Tensor,
+               max_query_len: int, scale: float, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Paged prefill: q/out [rows, H, d]; sequence s owns rows query_start_loc[s] ..
+    query_start_loc[s+1] (its last positions) and each row attends causally."""
+    dev = _cuda_device(q)
+    R, H, d = q.shape
+    N, B, Hk, d2 = k_cache.shape
+    S = int(context_lens.shape[0])
+    if d2 != d or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("q/out [rows, H, d] must match the pools [N, B, Hk, d]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or query_start_loc.shape != (S + 1,):
+        raise ValueError("block_tables must be [S, M] and query_start_loc [S + 1]")
+    dt = q.dtype
+    st = _lib.lib().pa_prefill(
+        _need(out, "out", dt, dev), _need(q, "q", dt, dev), _need(k_cache, "k_cache", dt, dev),
+        _need(v_cache, "v_cache", dt, dev), _need(block_tables, "block_tables", torch.int32, dev),
+        int(block_tables.shape[1]), _need(context_lens, "context_lens", torch.int32, dev),
+        _need(query_start_loc, "query_start_loc", torch.int32, dev), S, int(max_query_len), H, Hk, d, B, N,
+        float(scale), _dtype_code(q), _stream_ptr(q, stream))
+    _lib.check("pa_prefill", st)
+
+
 def pa_status_string(status: int) -> str:
     return _lib.status_name(status)
 

@@ -76,6 +76,26 @@ struct ReduceArgs {
   int max_num_partitions;
 };
 
+struct PrefillArgs {
+  int dtype;  // PA_FP16 or PA_BF16
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;
+  int max_blocks_per_seq;
+  int num_seqs;
+  int max_query_len;
+  int num_heads;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int num_blocks;
+  float scale;
+};
+
 // Record a formatted message as the calling thread's last error; returns status.
 int set_last_error(int status, const char* fmt, ...);
 
@@ -91,6 +111,8 @@ cudaError_t launch_splitk_reduce_f16(const ReduceArgs& a, cudaStream_t stream);
 cudaError_t launch_splitk_reduce_bf16(const ReduceArgs& a, cudaStream_t stream);
 // E4M3 caches with float16 queries (pa_decode_fp8.cu)
 cudaError_t launch_decode_f16_e4m3(const DecodeArgs& a, cudaStream_t stream);
+// paged prefill (pa_prefill.cu)
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 // shared-prefix split-K (pa_decode_prefix.cu): the shared pass, then the
 // per-sequence pass
 cudaError_t launch_decode_prefix(const DecodeArgs& a, cudaStream_t stream);

@@ -170,3 +170,25 @@ def test_copy_blocks_accepts_one_byte_caches(L):
     assert L.pa_copy_blocks(A, A, A, 0, 8, 16, 2, 128, 3, None) == _lib.PA_ERR_UNSUPPORTED
     # 1-byte elements: 16 * 1 * 8 = 128 bytes per block, a multiple of 16
     assert L.pa_copy_blocks(A, A, A, 0, 8, 16, 1, 8, _lib.PA_FP8_E4M3, None) == _lib.PA_OK
+
+
+def _prefill(L, **kw):
+    a = dict(S=2, maxq=64, H=8, Hk=2, d=128, B=16, qsl=A, dtype=0)
+    a.update(kw)
+    return L.pa_prefill(A, A, A, A, A, 8, A, a["qsl"], a["S"], a["maxq"], a["H"], a["Hk"], a["d"], a["B"], 32, 0.1,
+                        a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=256), _lib.PA_ERR_UNSUPPORTED),          # prefill: head_dim 64 or 128
+    (dict(H=6, Hk=2), _lib.PA_ERR_UNSUPPORTED),      # a query group of 3 does not divide 64
+    (dict(dtype=2), _lib.PA_ERR_UNSUPPORTED),
+    (dict(qsl=None), _lib.PA_ERR_INVALID_ARG),
+    (dict(qsl=A + 2), _lib.PA_ERR_INVALID_ARG),
+    (dict(maxq=-1), _lib.PA_ERR_INVALID_ARG),
+    (dict(B=8), _lib.PA_ERR_UNSUPPORTED),
+    (dict(S=0, qsl=None), _lib.PA_OK),
+    (dict(maxq=0, qsl=None), _lib.PA_OK),
+])
+def test_prefill_checks_arguments(L, kw, status):
+    assert _prefill(L, **kw) == status

@@ -570,6 +570,137 @@ def run_copy_blocks(args):
             "gpu_launches": args.steps, "clocks": clocks.summary(*walls)}
 
 
+# ---------------------------------------------------------------- prefill
+PREFILL_WORKLOADS = {
+    # name: (contexts, query lengths, H, Hk, d, B, description)
+    "prefill-llama3-8b": ([2048] * 8, [2048] * 8, 32, 8, 128, 16,
+                          "Llama-3-8B prompts: 8 x 2048 new tokens, H=32, Hk=8, d=128, B=16"),
+    "chunked-prefill-llama3-8b": ([2048] * 16, [512] * 16, 32, 8, 128, 16,
+                                  "Llama-3-8B chunked prefill: 16 sequences x (1536 cached + 512 new), B=16"),
+    "prefill-long": ([16384] * 2, [16384] * 2, 32, 8, 128, 16,
+                     "long prompts: 2 x 16384 new tokens, H=32, Hk=8, d=128, B=16"),
+}
+
+
+def run_prefill(args):
+    """Time one prefill step: reshape_and_cache of every new token, then
+    pa_prefill; FLOPs = 4 d H x (keys each query row attends to)."""
+    import torch
+    from paged_kv_cache_173_gb300 import api, workloads
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    name = args.workload if args.workload in PREFILL_WORKLOADS else "prefill-llama3-8b"
+    ctx, ql, H, Hk, d, B, desc = PREFILL_WORKLOADS[name]
+    b = workloads.build_prefill_batch(name=name, seed=args.seed, context_lens=ctx, query_lens=ql, num_heads=H,
+                                      num_kv_heads=Hk, head_dim=d, block_size=B, poison=False, dtype=args.dtype)
+    flops = workloads.prefill_flops(b)
+    t = lambda a: to_device(a, b.dtype, dev)  # noqa: E731
+    l2_bytes = 129 * 2 ** 20
+    pool_bytes = 2 * b.k_cache.nbytes
+    R = max(2, min(4, math.ceil(2 * l2_bytes / pool_bytes) + 1))
+    reps = [(t(b.k_cache), t(b.v_cache)) for _ in range(R)]
+    q, key, value, sm = t(b.q), t(b.key), t(b.value), t(b.slot_mapping)
+    bt, cl, qsl = t(b.block_tables), t(b.context_lens), t(b.query_start_loc)
+    maxq = int(np.diff(b.query_start_loc).max())
+    out = torch.empty_like(q)
+
+    def reshape(r):
+        kc, vc = reps[r % R]
+        api.pa_reshape_and_cache(key, value, kc, vc, sm)
+
+    def prefill(r):
+        kc, vc = reps[r % R]
+        api.pa_prefill(out, q, kc, vc, bt, cl, qsl, maxq, b.scale)
+
+    kernels = [("reshape_and_cache", reshape), ("paged_prefill", prefill)]
+    stream = torch.cuda.Stream(dev)
+    clocks = ClockSampler(dev.index)
+    K, W = args.steps, args.warmup
+    ms, per, walls, mode, G = time_path(torch, dev, stream, kernels, R, K, W, clocks)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured cuBLAS bf16 burst"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback"
+    step_ms = ms / K
+    value = flops * K / (ms * 1e-3) / 1e12
+    achieved = flops / (float(per[1]) * 1e-3) / 1e12
+
+    # e2e: the public calls with pinned host inputs and the output read back
+    host = {k: to_device(getattr(b, k), b.dtype, "cpu").pin_memory()
+            for k in ("q", "key", "value", "slot_mapping", "block_tables", "context_lens", "query_start_loc")}
+    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_h = torch.empty_like(host["q"]).pin_memory()
+
+    def e2e_step(i):
+        kc, vc = reps[i % R]
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        api.pa_reshape_and_cache(devb["key"], devb["value"], kc, vc, devb["slot_mapping"])
+        api.pa_prefill(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"], devb["query_start_loc"],
+                       maxq, b.scale)
+        out_h.copy_(out, non_blocking=True)
+
+    n = max(3, min(K, 50))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            e2e_step(i)
+        e1.record()
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / n
+    res = {
+        "metric": "paged prefill TFLOP/s (causal attention FLOPs)", "value": round(value, 1), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if b.dtype == "bf16" else "f16",
+        "data": "synthetic",
+        "config": {"workload": desc, "flops_per_step": flops, "step": "reshape_and_cache -> paged_prefill",
+                   "l2": f"{R} rotating pool replicas ({R * pool_bytes / 1e9:.2f} GB); steps back to back",
+                   "steps_per_graph": G, "kernel_timing": mode},
+        "kernel_ms": {n_: round(float(v), 4) for (n_, _), v in zip(kernels, per)},
+        "roofline": {"kernel": "paged_prefill", "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_kind": f"{peak_kind} (fp16 MMAs take the bf16 figure: the same nominal rate)"},
+        "gpu_launches": 2 * K,
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(sum(v.numel() * v.element_size() for v in host.values())),
+                "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()), "steps": n,
+                "ms_per_step": round(e2e_ms, 4)},
+        "clocks": clocks.summary(*walls),
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = prefill_cpu_baseline(b, budget_s=args.cpu_seconds)
+    return res
+
+
+def prefill_cpu_baseline(b, budget_s: float):
+    """The oracle on the host cores: the first n rows of sequence 0 as a
+    prompt of n tokens, n grown until the sample takes about budget_s / 3."""
+    from oracle import c_oracle
+    from paged_kv_cache_173_gb300 import workloads
+    kc, vc = c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
+    ql0 = int(b.query_start_loc[1])
+    n, elapsed, done = 16, 0.0, 0
+    while True:
+        qsl = np.array([0, n], np.int32)
+        t0 = time.perf_counter()
+        c_oracle.prefill(b.q[:n], kc, vc, b.block_tables[:1], np.array([n], np.int32), qsl, b.scale, dtype=b.dtype)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        done += 4 * b.head_dim * b.num_heads * (n * (n + 1) // 2)
+        if elapsed > budget_s or n >= ql0:
+            break
+        n = min(ql0, n * 2)
+    return {"value": round(done / elapsed / 1e12, 6), "unit": "TFLOP/s", "cores": c_oracle.max_threads(),
+            "kind": "oracle", "sample": f"float64 C oracle prefill of the first 16..{n} rows of one prompt, "
+                                        f"{elapsed:.1f} s, host {_cpu_model()}"}
+
+
 # ------------------------------------------------------------ CPU oracle
 def _cpu_model() -> str:
     try:
@@ -669,8 +800,10 @@ def parse_args(argv=None):
     p.add_argument("--dtype", choices=["fp16", "bf16"], default="fp16")
     p.add_argument("--kv-dtype", choices=["same", "fp8"], default="same",
                    help="fp8: E4M3 KV pools with one float scale each (float16 queries)")
-    p.add_argument("--op", choices=["step", "copy-blocks"], default="step",
-                   help="step: the decode step (the headline); copy-blocks: time pa_copy_blocks")
+    p.add_argument("--op", choices=["step", "copy-blocks", "prefill"], default="step",
+                   help="step: the decode step (the headline); copy-blocks: time pa_copy_blocks; prefill: "
+                        "reshape + pa_prefill on --workload prefill-llama3-8b, chunked-prefill-llama3-8b "
+                        "or prefill-long")
     p.add_argument("--copy-pairs", type=int, default=1024)
     p.add_argument("--path", choices=["auto", "decode", "splitk", "prefix"], default="auto",
                    help="decode: reshape + pa_decode; splitk: reshape + pa_decode_splitk + reduce; prefix "
@@ -708,6 +841,9 @@ def main(argv=None):
     __graft_entry__.build()
     if args.op == "copy-blocks":
         print(json.dumps(run_copy_blocks(args)), flush=True)
+        return 0
+    if args.op == "prefill":
+        print(json.dumps(run_prefill(args)), flush=True)
         return 0
     res = run_gpu(args, rank, world)
     if rank == 0:

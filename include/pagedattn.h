@@ -278,15 +278,17 @@ int pa_decode_prefix_splitk(void* out, const void* q, const void* k_cache, const
  *
  * with K_k, V_k the pool rows of position k of sequence s, KV head h / G.
  *
- *   q, out            [rows][num_heads][head_dim] of dtype, rows =
+ *   q, out            [num_rows][num_heads][head_dim] of dtype, num_rows =
  *                     query_start_loc[num_seqs]
  *   query_start_loc   [num_seqs + 1] int32, non-decreasing, starting at 0
  *   max_query_len     >= every qlen (sizes the grid; rows past it are not
  *                     computed)
- *   head_dim          64 or 128; num_heads / num_kv_heads must divide 64
+ *   head_dim          64 or 128; num_heads / num_kv_heads must divide 128
  *
  * Other arguments as pa_decode.  Scores, softmax and accumulation are
- * float32; the attention weights enter P.V rounded to dtype.
+ * float32 (the products accumulate in tensor memory); the attention weights
+ * enter P.V rounded to fp16, or for bf16 as a rounded value plus its rounded
+ * residual.
  *
  * Device-value outcomes: a context length below qlen or above
  * max_blocks_per_seq * block_size, or a block id read from the table outside
@@ -295,9 +297,9 @@ int pa_decode_prefix_splitk(void* out, const void* q, const void* k_cache, const
  */
 int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-               const int32_t* query_start_loc, int num_seqs, int max_query_len, int num_heads,
-               int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale, int dtype,
-               void* stream);
+               const int32_t* query_start_loc, int num_seqs, int num_rows, int max_query_len,
+               int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+               float scale, int dtype, void* stream);
 
 /*
  * pa_splitk_reduce -- merge the partitions left by pa_decode_splitk.

@@ -42,7 +42,7 @@ SIGNATURES = {
                                   _I, _P, _SZ, _P]),
     "pa_decode_prefix_splitk": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _F, _F,
                                      _I, _P, _I, _I, _P, _SZ, _P]),
-    "pa_prefill": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "pa_prefill": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
     "pa_last_error": (ctypes.c_char_p, []),
 }

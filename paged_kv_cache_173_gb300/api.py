@@ -277,7 +277,7 @@ def pa_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cach
         _need(out, "out", dt, dev), _need(q, "q", dt, dev), _need(k_cache, "k_cache", dt, dev),
         _need(v_cache, "v_cache", dt, dev), _need(block_tables, "block_tables", torch.int32, dev),
         int(block_tables.shape[1]), _need(context_lens, "context_lens", torch.int32, dev),
-        _need(query_start_loc, "query_start_loc", torch.int32, dev), S, int(max_query_len), H, Hk, d, B, N,
+        _need(query_start_loc, "query_start_loc", torch.int32, dev), S, R, int(max_query_len), H, Hk, d, B, N,
         float(scale), _dtype_code(q), _stream_ptr(q, stream))
     _lib.check("pa_prefill", st)
 

@@ -399,9 +399,9 @@ int pa_decode_prefix_splitk(void* out, const void* q, const void* k_cache, const
 
 int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-               const int32_t* query_start_loc, int num_seqs, int max_query_len, int num_heads,
-               int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale, int dtype,
-               void* stream) {
+               const int32_t* query_start_loc, int num_seqs, int num_rows, int max_query_len,
+               int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+               float scale, int dtype, void* stream) {
   int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                         num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                         dtype);
@@ -409,15 +409,17 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
   if (head_dim != 64 && head_dim != 128)
     return fail(PA_ERR_UNSUPPORTED, "prefill supports head_dim 64 or 128 (got %d)", head_dim);
   const int G = num_heads / num_kv_heads;
-  if (64 % G != 0)
-    return fail(PA_ERR_UNSUPPORTED, "prefill needs a query group size dividing 64 (got %d)", G);
-  if (max_query_len < 0) return fail(PA_ERR_INVALID_ARG, "max_query_len %d is negative", max_query_len);
-  if (num_seqs == 0 || max_query_len == 0) return ok();
+  if (128 % G != 0)
+    return fail(PA_ERR_UNSUPPORTED, "prefill needs a query group size dividing 128 (got %d)", G);
+  if (max_query_len < 0 || num_rows < 0)
+    return fail(PA_ERR_INVALID_ARG, "max_query_len (%d) and num_rows (%d) must be >= 0", max_query_len, num_rows);
+  if (num_seqs == 0 || max_query_len == 0 || num_rows == 0) return ok();
   if (!query_start_loc) return fail(PA_ERR_INVALID_ARG, "query_start_loc is NULL");
   if (!aligned(query_start_loc, 4)) return fail(PA_ERR_INVALID_ARG, "query_start_loc must be 4-byte aligned");
-  pa::PrefillArgs a{dtype, out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
-                    max_blocks_per_seq, num_seqs, max_query_len, num_heads, num_kv_heads, head_dim,
-                    block_size, num_blocks, scale};
+  pa::PrefillArgs a{dtype,      out,       q,           k_cache,      v_cache,      block_tables,
+                    context_lens, query_start_loc, max_blocks_per_seq, num_seqs, num_rows,
+                    max_query_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                    false};
   return cuda_status(pa::launch_prefill(a, static_cast<cudaStream_t>(stream)), "prefill launch");
 }
 

@@ -87,6 +87,7 @@ struct PrefillArgs {
   const int32_t* query_start_loc;
   int max_blocks_per_seq;
   int num_seqs;
+  int num_rows;
   int max_query_len;
   int num_heads;
   int num_kv_heads;
@@ -94,6 +95,7 @@ struct PrefillArgs {
   int block_size;
   int num_blocks;
   float scale;
+  bool use_mma_sync;  // the m16n8k16 kernel instead of the tcgen05 one
 };
 
 // Record a formatted message as the calling thread's last error; returns status.

@@ -175,13 +175,13 @@ def test_copy_blocks_accepts_one_byte_caches(L):
 def _prefill(L, **kw):
     a = dict(S=2, maxq=64, H=8, Hk=2, d=128, B=16, qsl=A, dtype=0)
     a.update(kw)
-    return L.pa_prefill(A, A, A, A, A, 8, A, a["qsl"], a["S"], a["maxq"], a["H"], a["Hk"], a["d"], a["B"], 32, 0.1,
-                        a["dtype"], None)
+    return L.pa_prefill(A, A, A, A, A, 8, A, a["qsl"], a["S"], 100, a["maxq"], a["H"], a["Hk"], a["d"], a["B"], 32,
+                        0.1, a["dtype"], None)
 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(d=256), _lib.PA_ERR_UNSUPPORTED),          # prefill: head_dim 64 or 128
-    (dict(H=6, Hk=2), _lib.PA_ERR_UNSUPPORTED),      # a query group of 3 does not divide 64
+    (dict(H=6, Hk=2), _lib.PA_ERR_UNSUPPORTED),      # a query group of 3 does not divide 128
     (dict(dtype=2), _lib.PA_ERR_UNSUPPORTED),
     (dict(qsl=None), _lib.PA_ERR_INVALID_ARG),
     (dict(qsl=A + 2), _lib.PA_ERR_INVALID_ARG),

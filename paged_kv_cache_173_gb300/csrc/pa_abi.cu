@@ -31,6 +31,9 @@ int ok() {
 
 int cuda_status(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return ok();
+  // a launch-configuration error is not sticky: clear it so that it is not
+  // reported again by the caller's next launch
+  (void)cudaGetLastError();
   return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 

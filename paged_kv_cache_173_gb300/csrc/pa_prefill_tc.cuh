@@ -2,15 +2,18 @@
 // O += P V accumulate in tensor memory (TMEM); the softmax runs on one thread
 // per query row between them.
 //
-//  paged_prefill_tc_kernel  one CTA per (query tile, KV head, sequence), 160
+//  paged_prefill_tc_kernel  one CTA per (query tile, KV head, sequence), 320
 //                           threads.  A tile is 128 query rows: 128 / G new
 //                           tokens of the sequence times the G query heads of
 //                           the KV head, loaded by TMA as one box per 64 dims.
-//                           Warp 4 (one lane) loads K/V stages of 64 keys by
-//                           TMA through the block table and issues the MMAs;
-//                           warps 0-3 own TMEM lanes 0-127, one query row per
-//                           thread: they read the row's scores, apply the
-//                           causal mask and the online softmax, and write P to
+//                           Warp 9 loads K/V stages of 64 keys by TMA through
+//                           the block table (a 32-lane register window of
+//                           block ids); one lane of warp 8 issues the MMAs;
+//                           warps 0-7 run the softmax, two threads per query
+//                           row (warps w and w + 4 share TMEM lanes 32 (w % 4)
+//                           .. + 31 and take half of the keys each): they
+//                           read the row's scores, apply the causal mask and
+//                           the online softmax, and write P (two buffers) to
 //                           shared memory for the P V MMA.
 //
 // TMEM columns: S of block j in [64 (j % 2), 64 (j % 2) + 64) (two buffers, so
@@ -33,8 +36,8 @@ namespace {
 
 constexpr int TC_ROWS = 128;   // query rows per CTA (the MMA's M)
 constexpr int TC_KEYS = 64;    // keys per stage (the Q K^T MMA's N)
-constexpr int TC_THREADS = 160;
-constexpr int TC_STAGES = 4;
+constexpr int TC_SOFT = 256;    // softmax threads: two per query row (warps w and w + 4)
+constexpr int TC_THREADS = TC_SOFT + 64;  // + warp 8 (MMA issue) and warp 9 (loads)
 constexpr float TC_RESCALE_LOG2 = 8.f;  // rescale O when a row maximum grows by more than 2^8
 
 struct PrefillTcParams {
@@ -62,17 +65,35 @@ struct TcCfg {
   static constexpr int KATOM = TC_KEYS * 128;            // 64 keys x 128 B
   static constexpr int KBYTES = DBOX * KATOM;            // K (or V) of one stage
   static constexpr int STAGE_BYTES = 2 * KBYTES;
-  static constexpr int PBYTES = TC_ROWS * TC_KEYS * 2;   // P: 128 rows x 64 keys
+  // K/V stages in flight: 4, or 3 where bf16's second P tile would not fit
+  static constexpr int STAGES = (std::is_same<T, __half>::value || HEAD_DIM < 128) ? 4 : 3;
+  static constexpr int PBYTES = TC_ROWS * TC_KEYS * 2;   // one P tile: 128 rows x 64 keys
   static constexpr int NP = std::is_same<T, __half>::value ? 1 : 2;  // bf16: P and its residual
+  static constexpr int PBUF = NP * PBYTES;               // one of the two P buffers
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = DBOX * QATOM;
-  static constexpr int P_OFF = KV_OFF + TC_STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = P_OFF + NP * PBYTES;
+  static constexpr int P_OFF = KV_OFF + STAGES * STAGE_BYTES;
+  static constexpr int XCH_OFF = P_OFF + 2 * PBUF;      // [2 blocks][2 halves][128 rows] float row maxima
+  static constexpr int BAR_OFF = XCH_OFF + 2 * 2 * TC_ROWS * 4;
   static constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256;
   static constexpr uint32_t TMEM_COLS = 256;  // S0, S1 (64 each), O (<= 128)
   static constexpr uint32_t ID_S = umma_idesc_f16(TC_ROWS, TC_KEYS, !std::is_same<T, __half>::value, false);
   static constexpr uint32_t ID_PV = umma_idesc_f16(TC_ROWS, HEAD_DIM, !std::is_same<T, __half>::value, true);
 };
+
+#ifndef PA_TC_WAIT
+#define PA_TC_WAIT 0
+#endif
+// The waits on the prefill pipeline's critical path.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity) {
+#if PA_TC_WAIT == 0
+  return mbar_wait_bounded(bar, parity, WAIT_LIMIT_NS);
+#elif PA_TC_WAIT == 1
+  return mbar_wait_try(bar, parity, WAIT_LIMIT_NS);
+#else
+  return mbar_wait_spin(bar, parity, WAIT_LIMIT_NS);
+#endif
+}
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -88,13 +109,13 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
-  uint64_t* full = bars;                 // [TC_STAGES] K/V of a stage landed
-  uint64_t* empty = bars + TC_STAGES;    // [TC_STAGES] the stage's MMAs are done
-  uint64_t* sfull = bars + 2 * TC_STAGES;  // [2] S of a block is in TMEM
-  uint64_t* pfull = sfull + 2;           // P of the block is in shared memory (128 arrivals)
-  uint64_t* pvdone = pfull + 1;          // the block's P V has completed
-  uint64_t* qbar = pvdone + 1;           // Q landed
-  uint64_t* drain = qbar + 1;            // every MMA issued has completed
+  uint64_t* full = bars;                   // [C::STAGES] K/V of a stage landed
+  uint64_t* empty = bars + C::STAGES;      // [C::STAGES] the stage's MMAs are done
+  uint64_t* sfull = bars + 2 * C::STAGES;  // [2] S of block j is in TMEM buffer j % 2
+  uint64_t* pfull = sfull + 2;             // [2] P of block j is in buffer j % 2 (TC_SOFT arrivals)
+  uint64_t* pvdone = pfull + 2;            // [2] P V of block j (buffer j % 2) has completed
+  uint64_t* qbar = pvdone + 2;             // Q landed
+  uint64_t* drain = qbar + 1;              // every MMA issued has completed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::BAR_OFF + 128);
   volatile int* flags = reinterpret_cast<volatile int*>(sm + C::BAR_OFF + 132);  // [0] bad block, [1] timeout
 
@@ -124,14 +145,15 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
   const int nblk = (kend + TC_KEYS - 1) / TC_KEYS;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < TC_STAGES; ++i) {
+    for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(&sfull[0], 1);
-    mbar_init(&sfull[1], 1);
-    mbar_init(pfull, 128);
-    mbar_init(pvdone, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&pfull[i], TC_SOFT);
+      mbar_init(&pvdone[i], 1);
+    }
     mbar_init(qbar, 1);
     mbar_init(drain, 1);
     flags[0] = 0;
@@ -144,28 +166,49 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
   tc_fence_after_sync();
   const uint32_t tmem = *tslot;
   const uint32_t tO = tmem + 128;
-
   const uint32_t sQ = smem_addr(sm + C::Q_OFF);
   const uint32_t sP = smem_addr(sm + C::P_OFF);
-  const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
 
-  if (warp == 4) {
-    // ------------------------------------------------ loads and MMAs (one lane)
+  if (warp == 9) {
+    // ------------------------------------------------ K/V loads (lane 0 issues)
+    // lane i holds the physical block of 16-token unit (wbase + i)
+    const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
+    const int units = (kend + CHUNK - 1) / CHUNK;
+    auto win_load = [&](int wbase) -> int {
+      const int u = wbase + lane;
+      return u < units ? __ldg(bt + (u * CHUNK) / p.block_size) : 0;
+    };
+    int wbase = 0;
+    int win = win_load(0);
     if (lane == 0 && nblk > 0) {
-      auto fail = [&]() { flags[1] = 1; };
-      auto load_stage = [&](int j) {
-        const int slot = j % TC_STAGES;
-        uint8_t* kd = sm + C::KV_OFF + slot * C::STAGE_BYTES;
-        const int nsub = min(TC_KEYS / CHUNK, (kend - j * TC_KEYS + CHUNK - 1) / CHUNK);
-        mbar_arrive_expect_tx(&full[slot], nsub * 2 * C::DBOX * BOX_BYTES);
-        for (int sub = 0; sub < nsub; ++sub) {
-          const int key0 = j * TC_KEYS + sub * CHUNK;
-          int phys = __ldg(bt + key0 / p.block_size);
-          if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
-            flags[0] = 1;  // never read outside the pool; the tile's outputs become NaN
-            phys = 0;
-          }
-          const int y = phys * p.block_size + key0 % p.block_size;
+      mbar_arrive_expect_tx(qbar, C::DBOX * C::QATOM);
+      for (int db = 0; db < C::DBOX; ++db)
+        tma_load_3d(sm + C::Q_OFF + db * C::QATOM, &p.tmap_q, db * BOX_DIMS, kvh * G, q0 + t0, qbar);
+    }
+    int loaded = 0;
+    for (int j = 0; j < nblk; ++j) {
+      const int slot = j % C::STAGES;
+      if (j >= C::STAGES &&
+          !__all_sync(FULL_MASK, tc_wait(&empty[slot], ((j / C::STAGES) - 1) & 1))) {
+        if (lane == 0) flags[1] = 1;
+        break;
+      }
+      if (4 * j >= wbase + 32) {  // the next 32 units (8 stages)
+        wbase += 32;
+        win = win_load(wbase);
+      }
+      const int nsub = min(TC_KEYS / CHUNK, units - 4 * j);
+      uint8_t* kd = sm + C::KV_OFF + slot * C::STAGE_BYTES;
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], nsub * 2 * C::DBOX * BOX_BYTES);
+      for (int sub = 0; sub < nsub; ++sub) {
+        int phys = __shfl_sync(FULL_MASK, win, 4 * j + sub - wbase);
+        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
+          if (lane == 0) flags[0] = 1;  // never read outside the pool; the tile's outputs become NaN
+          phys = 0;
+        }
+        const int key0 = j * TC_KEYS + sub * CHUNK;
+        const int y = phys * p.block_size + key0 % p.block_size;
+        if (lane == 0) {
 #pragma unroll
           for (int db = 0; db < C::DBOX; ++db) {
             tma_load_3d(kd + db * C::KATOM + sub * BOX_BYTES, &p.tmap_k, db * BOX_DIMS, kvh, y, &full[slot]);
@@ -173,19 +216,19 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
                         &full[slot]);
           }
         }
-      };
-      mbar_arrive_expect_tx(qbar, C::DBOX * C::QATOM);
-      for (int db = 0; db < C::DBOX; ++db)
-        tma_load_3d(sm + C::Q_OFF + db * C::QATOM, &p.tmap_q, db * BOX_DIMS, kvh * G, q0 + t0, qbar);
-      int loaded = 0;  // stages whose copies were issued
-      int landed = 0;  // stages whose copies were waited for
-      for (; loaded < TC_STAGES && loaded < nblk; ++loaded) load_stage(loaded);
-
-      bool ok = mbar_wait_bounded(qbar, 0, WAIT_LIMIT_NS);
+      }
+      loaded = j + 1;
+    }
+    // the copies of the last stages land before the shared memory is released
+    for (int j = max(0, loaded - C::STAGES); j < loaded; ++j)
+      (void)tc_wait(&full[j % C::STAGES], (j / C::STAGES) & 1);
+  } else if (warp == 8) {
+    // ------------------------------------------------ MMA issue (lane 0)
+    if (lane == 0 && nblk > 0) {
+      bool ok = tc_wait(qbar, 0);
       auto issue_qk = [&](int j) -> bool {
-        const int slot = j % TC_STAGES;
-        if (!mbar_wait_bounded(&full[slot], (j / TC_STAGES) & 1, WAIT_LIMIT_NS)) return false;
-        landed = j + 1;
+        const int slot = j % C::STAGES;
+        if (!tc_wait(&full[slot], (j / C::STAGES) & 1)) return false;
         tc_fence_after_sync();
         const uint32_t kb = smem_addr(sm + C::KV_OFF + slot * C::STAGE_BYTES);
 #pragma unroll
@@ -200,141 +243,135 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
       if (ok) ok = issue_qk(0);
       if (ok && nblk > 1) ok = issue_qk(1);
       for (int j = 0; ok && j < nblk; ++j) {
-        const int slot = j % TC_STAGES;
-        if (!mbar_wait_bounded(pfull, j & 1, WAIT_LIMIT_NS)) {
+        const int b = j & 1;
+        if (!tc_wait(&pfull[b], (j >> 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t vb = smem_addr(sm + C::KV_OFF + slot * C::STAGE_BYTES + C::KBYTES);
+        const uint32_t vb = smem_addr(sm + C::KV_OFF + (j % C::STAGES) * C::STAGE_BYTES + C::KBYTES);
+        const uint32_t pb = sP + b * C::PBUF;
 #pragma unroll
         for (int kk = 0; kk < TC_KEYS / 16; ++kk) {
           const uint64_t bdesc = umma_desc_sw128(vb + kk * 2048, C::KATOM, 1024);
-          umma_f16(tO, umma_desc_sw128(sP + (kk << 5), 16, 1024), bdesc, C::ID_PV, j > 0 || kk > 0);
+          umma_f16(tO, umma_desc_sw128(pb + (kk << 5), 16, 1024), bdesc, C::ID_PV, j > 0 || kk > 0);
           if constexpr (BF16)
-            umma_f16(tO, umma_desc_sw128(sP + C::PBYTES + (kk << 5), 16, 1024), bdesc, C::ID_PV, true);
+            umma_f16(tO, umma_desc_sw128(pb + C::PBYTES + (kk << 5), 16, 1024), bdesc, C::ID_PV, true);
         }
-        umma_commit(pvdone);
-        umma_commit(&empty[slot]);
-        if (j + 2 < nblk && !issue_qk(j + 2)) {
-          ok = false;
-          break;
-        }
-        if (j + TC_STAGES < nblk) {
-          if (!mbar_wait_bounded(&empty[slot], (j / TC_STAGES) & 1, WAIT_LIMIT_NS)) {
-            ok = false;
-            break;
-          }
-          load_stage(j + TC_STAGES);
-          ++loaded;
-        }
+        umma_commit(&pvdone[b]);
+        umma_commit(&empty[j % C::STAGES]);
+        if (j + 2 < nblk && !issue_qk(j + 2)) ok = false;
       }
-      if (!ok) {
-        fail();
-        // let the copies still in flight land before the shared memory is released
-        for (int j = landed; j < loaded; ++j)
-          (void)mbar_wait_bounded(&full[j % TC_STAGES], (j / TC_STAGES) & 1, WAIT_LIMIT_NS);
-      }
-      umma_commit(drain);  // let every MMA finish before the TMEM is released
-      if (!mbar_wait_bounded(drain, 0, WAIT_LIMIT_NS)) fail();
+      if (!ok) flags[1] = 1;
+      umma_commit(drain);  // every MMA finishes before the TMEM is released
+      if (!tc_wait(drain, 0)) flags[1] = 1;
     }
   } else {
-    // ------------------------------------------------ softmax, one row per thread
-    const int r = threadIdx.x;  // TMEM lane = query row of the tile
+    // ------------------------------------------------ softmax: two threads per query row
+    // warp w (0-7) reads TMEM lanes 32 (w % 4) .. + 31: row r; half h = w / 4 takes keys
+    // [32 h, 32 h + 32) of every block and O columns [h DO / 2, (h + 1) DO / 2)
+    constexpr int HK = TC_KEYS / 2;
+    constexpr int HO = DO / 2;
+    const int h = warp >> 2;
+    const int r = 32 * (warp & 3) + lane;
     const int t = t0 + r / G;
     const bool rv = t < t1;
     const int pos = rv ? base + t : -1;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    float* xch = reinterpret_cast<float*>(sm + C::XCH_OFF);  // [block % 2][half][row]
     const float sl2 = p.scale_log2;
-    float m_used = -INFINITY, l = 0.f;
+    float m_used = -INFINITY, l = 0.f;  // log2 units; l over this half's keys
+    // Every softmax thread runs every block, so that all of them meet at the
+    // named barrier each time; after a wait gives up (ok false, warp-uniform)
+    // a warp skips its remaining waits and its results become NaN.
     bool ok = true;
+    auto softmax_sync = []() { asm volatile("bar.sync 1, %0;" ::"n"(TC_SOFT) : "memory"); };
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      if (ok) ok = __all_sync(FULL_MASK, tc_wait(bar, parity));
+    };
     for (int j = 0; j < nblk; ++j) {
-      if (!__all_sync(FULL_MASK, mbar_wait_bounded(&sfull[j & 1], (j >> 1) & 1, WAIT_LIMIT_NS))) {
-        ok = false;
-        break;
-      }
+      const int b = j & 1;
+      wait(&sfull[b], (j >> 1) & 1);
       tc_fence_after_sync();
-      float x[TC_KEYS];
+      uint32_t v[HK / 16][16];
 #pragma unroll
-      for (int c = 0; c < TC_KEYS; c += 16) {
-        uint32_t v[16];
-        tmem_ld16(tmem + 64 * (j & 1) + lane_off + c, v);
-        tmem_wait_ld();
+      for (int c = 0; c < HK / 16; ++c) tmem_ld16(tmem + 64 * b + HK * h + lane_off + 16 * c, v[c]);
+      tmem_wait_ld();
+      float x[HK];  // raw scores of keys k0 + HK h + c; masked ones become -inf
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]) * sl2;
-      }
-      const int k0 = j * TC_KEYS;
-      float mx = -INFINITY;
-      if (k0 + TC_KEYS - 1 > base + t0) {  // a key here may lie past some row of the tile
+      for (int c = 0; c < HK; ++c) x[c] = __uint_as_float(v[c >> 4][c & 15]);
+      const int k0 = j * TC_KEYS + HK * h;
+      if (k0 + HK - 1 > base + t0) {  // a key here may lie past some row of the tile
 #pragma unroll
-        for (int c = 0; c < TC_KEYS; ++c) {
+        for (int c = 0; c < HK; ++c)
           if (k0 + c > pos) x[c] = -INFINITY;
-          mx = fmaxf(mx, x[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < TC_KEYS; ++c) mx = fmaxf(mx, x[c]);
       }
-      const float m_new = fmaxf(m_used, mx);
-      if (j > 0) {
-        if (!__all_sync(FULL_MASK, mbar_wait_bounded(pvdone, (j - 1) & 1, WAIT_LIMIT_NS))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const bool need = m_new > m_used + TC_RESCALE_LOG2;
-        if (__any_sync(FULL_MASK, need)) {  // rescale this warp's O rows in TMEM
+      float mq[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mq[i] = x[i];
+#pragma unroll
+      for (int c = 4; c < HK; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+      float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      xch[(b * 2 + h) * TC_ROWS + r] = mx;
+      softmax_sync();  // both halves of every row have published their maxima
+      mx = fmaxf(mx, xch[(b * 2 + (h ^ 1)) * TC_ROWS + r]);
+      const float m_new = fmaxf(m_used, mx * sl2);
+      if (j >= 2) wait(&pvdone[b], ((j - 2) >> 1) & 1);  // P buffer b is free once P V of block j - 2 is done
+      if (j == 0) {
+        m_used = m_new;
+      } else {
+        const bool need = m_new > m_used + TC_RESCALE_LOG2;  // the same in both halves of a row
+        if (__any_sync(FULL_MASK, need)) {
+          // O must hold the P V of block j - 1 before this warp rescales its half rows
+          wait(&pvdone[b ^ 1], ((j - 1) >> 1) & 1);
+          tc_fence_after_sync();
           const float f = need ? ex2(m_used - m_new) : 1.f;
 #pragma unroll 1
-          for (int c = 0; c < DO; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(tO + lane_off + c, v);
+          for (int c = 0; c < HO; c += 16) {
+            uint32_t w[16];
+            tmem_ld16(tO + HO * h + lane_off + c, w);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-            tmem_st16(tO + lane_off + c, v);
+            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * f);
+            tmem_st16(tO + HO * h + lane_off + c, w);
           }
           tmem_wait_st();
           l *= f;
           if (need) m_used = m_new;
         }
-      } else {
-        m_used = m_new;
       }
-      const float b = m_used == -INFINITY ? 0.f : m_used;  // a row that has seen no key yet
-      // P row (64 keys, 128 bytes) into the 128-byte-swizzled K-major tile
-      uint8_t* prow = sm + C::P_OFF + r * 128;
+      const float nb = m_used == -INFINITY ? 0.f : -m_used;  // a row that has seen no key yet
+      // this half of the P row (32 keys, 64 bytes) into buffer b, 128-byte-swizzled K-major;
+      // the sums add the float32 weights
+      uint8_t* prow = sm + C::P_OFF + b * C::PBUF + r * 128;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int u = 0; u < TC_KEYS / 8; ++u) {
+      for (int u = 0; u < HK / 8; ++u) {
         uint32_t w[4], wr[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float p0 = ex2(x[8 * u + 2 * i] - b);
-          const float p1 = ex2(x[8 * u + 2 * i + 1] - b);
+          const float p0 = ex2(fmaf(x[8 * u + 2 * i], sl2, nb));
+          const float p1 = ex2(fmaf(x[8 * u + 2 * i + 1], sl2, nb));
+          ls[i] += p0 + p1;
           w[i] = pack2<T>(p0, p1);
-          const float2 f2 = unpack2<T>(w[i]);
           if constexpr (BF16) {
+            const float2 f2 = unpack2<T>(w[i]);
             wr[i] = pack2<T>(p0 - f2.x, p1 - f2.y);
-            l += p0 + p1;
-          } else {
-            l += f2.x + f2.y;  // the sum adds the rounded weights that multiply V
           }
         }
-        const int pu = (u ^ (r & 7)) << 4;
+        const int pu = ((4 * h + u) ^ (r & 7)) << 4;
         *reinterpret_cast<uint4*>(prow + pu) = make_uint4(w[0], w[1], w[2], w[3]);
         if constexpr (BF16) *reinterpret_cast<uint4*>(prow + C::PBYTES + pu) = make_uint4(wr[0], wr[1], wr[2], wr[3]);
       }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       // keys at or past kend in the last stage hold stale data: zero those V rows
       if (j == nblk - 1 && kend < (j + 1) * TC_KEYS) {
-        const int slot = j % TC_STAGES;
-        if (!__all_sync(FULL_MASK, mbar_wait_bounded(&full[slot], (j / TC_STAGES) & 1, WAIT_LIMIT_NS))) {
-          ok = false;
-          break;
-        }
+        const int slot = j % C::STAGES;
+        wait(&full[slot], (j / C::STAGES) & 1);
         uint8_t* vd = sm + C::KV_OFF + slot * C::STAGE_BYTES + C::KBYTES;
         const int key_lo = kend - j * TC_KEYS;
         const int units = (TC_KEYS - key_lo) * 8;  // 16-byte units per atom
-        for (int i = r; i < units * C::DBOX; i += 128) {
+        for (int i = threadIdx.x; i < units * C::DBOX; i += TC_SOFT) {
           const int db = i / units;
           const int rem = i - db * units;
           *reinterpret_cast<uint4*>(vd + db * C::KATOM + (key_lo + rem / 8) * 128 + (rem % 8) * 16) =
@@ -343,33 +380,36 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
       }
       fence_proxy_async_smem();  // P (and the zeroed rows) become visible to the tensor core
       tc_fence_before_sync();
-      mbar_arrive(pfull);
+      mbar_arrive(&pfull[b]);
     }
     // ------------------------------------------------ O / l, stored after the barrier below
-    float o[DO];
-    const bool have = ok && nblk > 0 &&
-                      __all_sync(FULL_MASK, mbar_wait_bounded(pvdone, (nblk - 1) & 1, WAIT_LIMIT_NS));
+    float o[HO];
+    if (nblk > 0) wait(&pvdone[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1);
+    const bool have = ok && nblk > 0;
     if (have) {
       tc_fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < DO; c += 16) {
-        uint32_t v[16];
-        tmem_ld16(tO + lane_off + c, v);
+      for (int c = 0; c < HO; c += 16) {
+        uint32_t w[16];
+        tmem_ld16(tO + HO * h + lane_off + c, w);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[c + i] = __uint_as_float(v[i]);
+        for (int i = 0; i < 16; ++i) o[c + i] = __uint_as_float(w[i]);
       }
     }
+    xch[h * TC_ROWS + r] = l;  // the row sum is the two halves' sums
     tc_fence_before_sync();
-    __syncthreads();  // the control lane's flags are visible past this point
+    __syncthreads();  // the other warps' flags and the partial sums are visible past this point
     if (rv) {
-      const float inv = (!have || ctx_bad || flags[0] || flags[1]) ? NAN : 1.f / l;
-      T* dst = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + t) * H + kvh * G + r % G) * HEAD_DIM;
+      const float lt = l + xch[(h ^ 1) * TC_ROWS + r];
+      const float inv = (!have || ctx_bad || flags[0] || flags[1]) ? NAN : 1.f / lt;
+      T* dst = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + t) * H + kvh * G + r % G) * HEAD_DIM + HO * h;
 #pragma unroll
-      for (int c = 0; c < DO; c += 8) {
+      for (int c = 0; c < HO; c += 8) {
         uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = have ? pack2<T>(o[c + 2 * i] * inv, o[c + 2 * i + 1] * inv) : pack2<T>(NAN, NAN);
+        for (int i = 0; i < 4; ++i)
+          w[i] = have ? pack2<T>(o[c + 2 * i] * inv, o[c + 2 * i + 1] * inv) : pack2<T>(NAN, NAN);
         *reinterpret_cast<uint4*>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
@@ -378,7 +418,7 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
     allow_dependent_launch();
     return;
   }
-  // the control warp: meet the softmax warps at their two barriers
+  // the MMA and load warps meet the softmax warps at their two barriers
   tc_fence_before_sync();
   __syncthreads();
   __syncthreads();

@@ -85,6 +85,41 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Wait for the phase with the given parity with as little wake-up latency
+// as possible: test_wait never suspends the thread; the clock is read every
+// 256 probes.  Gives up (returns false) after `limit_ns` nanoseconds.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t a = smem_addr(bar);
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 255u) == 0) {
+      const uint64_t t = global_timer_ns();
+      if (i == 0) t0 = t;
+      else if (t - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// try_wait without a suspend-time hint: the hardware picks how long a
+// probe may block.  Gives up after `limit_ns` nanoseconds.
+__device__ __forceinline__ bool mbar_wait_try(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ------------------------------------------------------------- bulk copies --
 // Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned); completion is counted in bytes on `bar`.

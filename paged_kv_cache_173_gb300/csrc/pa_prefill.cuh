@@ -432,7 +432,7 @@ cudaError_t launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   if (p.tiles == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.tiles, a.num_kv_heads, a.num_seqs);
-  cfg.blockDim = dim3(TC_THREADS);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -2,25 +2,21 @@
 // O += P V accumulate in tensor memory (TMEM); the softmax runs on one thread
 // per query row between them.
 //
-//  paged_prefill_tc_kernel  one CTA per (query tile, KV head, sequence), 320
-//                           threads.  A tile is 128 query rows: 128 / G new
-//                           tokens of the sequence times the G query heads of
-//                           the KV head, loaded by TMA as one box per 64 dims.
-//                           Warp 9 loads K/V stages of 64 keys by TMA through
-//                           the block table (a 32-lane register window of
-//                           block ids); one lane of warp 8 issues the MMAs;
-//                           warps 0-7 run the softmax, two threads per query
-//                           row (warps w and w + 4 share TMEM lanes 32 (w % 4)
-//                           .. + 31 and take half of the keys each): they
-//                           read the row's scores, apply the causal mask and
-//                           the online softmax, and write P (two buffers) to
-//                           shared memory for the P V MMA.
-//
-// TMEM columns: S of block j in [64 (j % 2), 64 (j % 2) + 64) (two buffers, so
-// the next block's Q K^T overlaps this block's softmax), O in [128, 128 + d).
-// The running maximum used for the exponent moves only when a row's maximum
-// grows by more than 2^8 (then O and l of that row are rescaled in place), so
-// P stays within [0, 256] and the rescale is rare.
+//  paged_prefill_tc_kernel  one CTA per (query tile, KV head, sequence).  A
+//                           tile is 128 query rows: 128 / G new tokens of the
+//                           sequence times the G query heads of the KV head,
+//                           loaded by TMA as one box per 64 dims.  The last
+//                           warp loads: lane 0 streams K blocks of 64 keys
+//                           through the block table into a ring of K stages,
+//                           lane 1 streams V into a ring of its own, so that a
+//                           K stage is refilled as soon as its Q K^T is done,
+//                           long before that block's P V.  One lane of the
+//                           warp before it issues the MMAs.  The softmax warps
+//                           (one or two threads per query row) read the row's
+//                           scores from TMEM, apply the causal mask and the
+//                           online softmax, and write P to shared memory for
+//                           the P V MMA.  fp16 at d = 128 runs two CTAs per SM:
+//                           one CTA's softmax overlaps the other's MMAs.
 //
 // The method is the one of paged_prefill_kernel (pa_prefill.cuh): each new
 // token attends to the positions up to its own ("in-depth reading", section
@@ -36,8 +32,6 @@ namespace {
 
 constexpr int TC_ROWS = 128;   // query rows per CTA (the MMA's M)
 constexpr int TC_KEYS = 64;    // keys per stage (the Q K^T MMA's N)
-constexpr int TC_SOFT = 256;    // softmax threads: two per query row (warps w and w + 4)
-constexpr int TC_THREADS = TC_SOFT + 64;  // + warp 8 (MMA issue) and warp 9 (loads)
 constexpr float TC_RESCALE_LOG2 = 8.f;  // rescale O when a row maximum grows by more than 2^8
 
 struct PrefillTcParams {
@@ -58,25 +52,79 @@ struct PrefillTcParams {
   float scale_log2;
 };
 
+#ifndef PA_TC16_SPLIT
+#define PA_TC16_SPLIT 1
+#endif
+#ifndef PA_TC16_KSTAGES
+#define PA_TC16_KSTAGES 2
+#endif
+#ifndef PA_TC16_VSTAGES
+#define PA_TC16_VSTAGES 2
+#endif
+#ifndef PA_TC16_PBUFS
+#define PA_TC16_PBUFS 1
+#endif
+#ifndef PA_TC16_CTAS
+#define PA_TC16_CTAS 2
+#endif
+
+// Shape of one CTA:
+//   SPLIT    softmax threads per query row (1: warps 0-3; 2: warps w and w + 4
+//            share TMEM lanes 32 (w % 4) .. + 31 and take half the keys each)
+//   KSTAGES  K stages in flight: a K stage is free again once its Q K^T is done
+//   VSTAGES  V stages in flight: free once the block's P V is done
+//   PBUFS    P buffers (2: block j + 1's softmax writes P while block j's P V runs)
+//   CTAS     CTAs per SM the shape is sized for (shared memory, TMEM,
+//            registers): two CTAs interleave one's softmax with the other's MMAs
+// fp16 at d = 128 runs two CTAs per SM; its layout fills the shared memory
+// only when the dynamic base is 1024-byte aligned (NOSLACK), which the kernel
+// checks before it touches TMA or TMEM.
+template <typename T, int HEAD_DIM>
+struct TcShape {
+  static constexpr bool F16 = std::is_same<T, __half>::value;
+  static constexpr bool TUNED = F16 && HEAD_DIM == 128;
+  static constexpr int SPLIT = TUNED ? PA_TC16_SPLIT : (F16 ? 1 : (HEAD_DIM == 128 ? 2 : 1));
+  static constexpr int KSTAGES = TUNED ? PA_TC16_KSTAGES : 3;
+  static constexpr int VSTAGES = TUNED ? PA_TC16_VSTAGES : 3;
+  static constexpr int PBUFS = TUNED ? PA_TC16_PBUFS : 2;
+  static constexpr int CTAS = TUNED ? PA_TC16_CTAS : (F16 ? 2 : 1);
+};
+
 template <typename T, int HEAD_DIM>
 struct TcCfg {
+  using Shape = TcShape<T, HEAD_DIM>;
+  static constexpr int SPLIT = Shape::SPLIT;
+  static constexpr int KSTAGES = Shape::KSTAGES;
+  static constexpr int VSTAGES = Shape::VSTAGES;
+  static constexpr int PBUFS = Shape::PBUFS;
+  static constexpr int CTAS = Shape::CTAS;
+  static constexpr int SOFT = 128 * SPLIT;               // softmax threads
+  static constexpr int THREADS = SOFT + 64;              // + the MMA warp and the load warp
+  static constexpr int MMA_WARP = SOFT / 32;
+  static constexpr int LOAD_WARP = SOFT / 32 + 1;
   static constexpr int DBOX = HEAD_DIM / BOX_DIMS;       // 64-dim atoms per row
   static constexpr int QATOM = TC_ROWS * 128;            // 128 rows x 128 B
   static constexpr int KATOM = TC_KEYS * 128;            // 64 keys x 128 B
-  static constexpr int KBYTES = DBOX * KATOM;            // K (or V) of one stage
-  static constexpr int STAGE_BYTES = 2 * KBYTES;
-  // K/V stages in flight: 4, or 3 where bf16's second P tile would not fit
-  static constexpr int STAGES = (std::is_same<T, __half>::value || HEAD_DIM < 128) ? 4 : 3;
+  static constexpr int KBYTES = DBOX * KATOM;            // K (or V) of one block
   static constexpr int PBYTES = TC_ROWS * TC_KEYS * 2;   // one P tile: 128 rows x 64 keys
   static constexpr int NP = std::is_same<T, __half>::value ? 1 : 2;  // bf16: P and its residual
-  static constexpr int PBUF = NP * PBYTES;               // one of the two P buffers
+  static constexpr int PBUF = NP * PBYTES;               // one P buffer
   static constexpr int Q_OFF = 0;
-  static constexpr int KV_OFF = DBOX * QATOM;
-  static constexpr int P_OFF = KV_OFF + STAGES * STAGE_BYTES;
-  static constexpr int XCH_OFF = P_OFF + 2 * PBUF;      // [2 blocks][2 halves][128 rows] float row maxima
-  static constexpr int BAR_OFF = XCH_OFF + 2 * 2 * TC_ROWS * 4;
-  static constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256;
+  static constexpr int K_OFF = DBOX * QATOM;
+  static constexpr int V_OFF = K_OFF + KSTAGES * KBYTES;
+  static constexpr int P_OFF = V_OFF + VSTAGES * KBYTES;
+  // SPLIT 2: [2 blocks][2 halves][128 rows] row maxima, then [2 halves][128 rows] row sums
+  static constexpr int XCH_OFF = P_OFF + PBUFS * PBUF;
+  static constexpr int BAR_OFF = XCH_OFF + (SPLIT == 2 ? 3 * 2 * TC_ROWS * 4 : 0);
+  static constexpr int NBARS = 2 * KSTAGES + 2 * VSTAGES + 8;
+  static constexpr int SLOT_OFF = BAR_OFF + 8 * NBARS;     // TMEM base address, then two flags
+  static constexpr int LAYOUT_BYTES = SLOT_OFF + 16;
+  // the shared memory of one SM (228 KB) holds CTAS CTAs, each with 1 KB reserved
+  static constexpr bool NOSLACK = CTAS * (LAYOUT_BYTES + 1024 + 1024) > 228 * 1024;
+  static constexpr int SMEM_BYTES = LAYOUT_BYTES + (NOSLACK ? 0 : 1024);
+  static_assert(CTAS * (SMEM_BYTES + 1024) <= 228 * 1024, "CTAS CTAs do not fit in one SM");
   static constexpr uint32_t TMEM_COLS = 256;  // S0, S1 (64 each), O (<= 128)
+  static_assert(CTAS * TMEM_COLS <= 512, "tensor memory");
   static constexpr uint32_t ID_S = umma_idesc_f16(TC_ROWS, TC_KEYS, !std::is_same<T, __half>::value, false);
   static constexpr uint32_t ID_PV = umma_idesc_f16(TC_ROWS, HEAD_DIM, !std::is_same<T, __half>::value, true);
 };
@@ -100,24 +148,29 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 template <typename T, int HEAD_DIM>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(TcCfg<T, HEAD_DIM>::THREADS, TcCfg<T, HEAD_DIM>::CTAS)
 paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
   using C = TcCfg<T, HEAD_DIM>;
   constexpr bool BF16 = !std::is_same<T, __half>::value;
   constexpr int DO = HEAD_DIM;  // O columns
+  constexpr int KS = C::KSTAGES;
+  constexpr int VS = C::VSTAGES;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const bool misaligned = C::NOSLACK && (smem_addr(smem_raw) & 1023u) != 0;
+  uint8_t* sm = smem_raw + (C::NOSLACK ? 0u : ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
-  uint64_t* full = bars;                   // [C::STAGES] K/V of a stage landed
-  uint64_t* empty = bars + C::STAGES;      // [C::STAGES] the stage's MMAs are done
-  uint64_t* sfull = bars + 2 * C::STAGES;  // [2] S of block j is in TMEM buffer j % 2
-  uint64_t* pfull = sfull + 2;             // [2] P of block j is in buffer j % 2 (TC_SOFT arrivals)
-  uint64_t* pvdone = pfull + 2;            // [2] P V of block j (buffer j % 2) has completed
-  uint64_t* qbar = pvdone + 2;             // Q landed
-  uint64_t* drain = qbar + 1;              // every MMA issued has completed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::BAR_OFF + 128);
-  volatile int* flags = reinterpret_cast<volatile int*>(sm + C::BAR_OFF + 132);  // [0] bad block, [1] timeout
+  uint64_t* kfull = bars;             // [KS] K of a block landed
+  uint64_t* kempty = kfull + KS;      // [KS] that block's Q K^T is done
+  uint64_t* vfull = kempty + KS;      // [VS] V of a block landed
+  uint64_t* vempty = vfull + VS;      // [VS] that block's P V is done
+  uint64_t* sfull = vempty + VS;      // [2] S of block j is in TMEM buffer j % 2
+  uint64_t* pfull = sfull + 2;        // [2] P of block j is written (C::SOFT arrivals)
+  uint64_t* pvdone = pfull + 2;       // [2] P V of block j has completed
+  uint64_t* qbar = pvdone + 2;        // Q landed
+  uint64_t* drain = qbar + 1;         // every MMA issued has completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::SLOT_OFF);
+  volatile int* flags = reinterpret_cast<volatile int*>(sm + C::SLOT_OFF + 4);  // [0] bad block, [1] timeout
 
   const int tile = p.tiles - 1 - static_cast<int>(blockIdx.x);  // the longest tiles start first
   const int kvh = blockIdx.y;
@@ -139,19 +192,32 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
     return;
   }
   const int t1 = min(qlen, t0 + p.tile_tokens);
+  if (misaligned) {  // the layout needs an aligned base: refuse, with NaN rows
+    for (int i = threadIdx.x; i < (t1 - t0) * G * DO; i += blockDim.x) {
+      const int row = i / DO;
+      static_cast<T*>(p.out)[(static_cast<size_t>(q0 + t0 + row / G) * H + kvh * G + row % G) * DO + i % DO] =
+          to_elem<T>(NAN);
+    }
+    allow_dependent_launch();
+    return;
+  }
   const bool ctx_bad = ctx < qlen || ctx > cap;
   const int base = ctx - qlen;
   const int kend = ctx_bad ? 0 : base + t1;
   const int nblk = (kend + TC_KEYS - 1) / TC_KEYS;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::STAGES; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+    for (int i = 0; i < KS; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);
+    }
+    for (int i = 0; i < VS; ++i) {
+      mbar_init(&vfull[i], 1);
+      mbar_init(&vempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&pfull[i], TC_SOFT);
+      mbar_init(&pfull[i], C::SOFT);
       mbar_init(&pvdone[i], 1);
     }
     mbar_init(qbar, 1);
@@ -167,70 +233,58 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
   const uint32_t tmem = *tslot;
   const uint32_t tO = tmem + 128;
   const uint32_t sQ = smem_addr(sm + C::Q_OFF);
-  const uint32_t sP = smem_addr(sm + C::P_OFF);
 
-  if (warp == 9) {
-    // ------------------------------------------------ K/V loads (lane 0 issues)
-    // lane i holds the physical block of 16-token unit (wbase + i)
-    const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
-    const int units = (kend + CHUNK - 1) / CHUNK;
-    auto win_load = [&](int wbase) -> int {
-      const int u = wbase + lane;
-      return u < units ? __ldg(bt + (u * CHUNK) / p.block_size) : 0;
-    };
-    int wbase = 0;
-    int win = win_load(0);
-    if (lane == 0 && nblk > 0) {
-      mbar_arrive_expect_tx(qbar, C::DBOX * C::QATOM);
-      for (int db = 0; db < C::DBOX; ++db)
-        tma_load_3d(sm + C::Q_OFF + db * C::QATOM, &p.tmap_q, db * BOX_DIMS, kvh * G, q0 + t0, qbar);
-    }
-    int loaded = 0;
-    for (int j = 0; j < nblk; ++j) {
-      const int slot = j % C::STAGES;
-      if (j >= C::STAGES &&
-          !__all_sync(FULL_MASK, tc_wait(&empty[slot], ((j / C::STAGES) - 1) & 1))) {
-        if (lane == 0) flags[1] = 1;
-        break;
+  if (warp == C::LOAD_WARP) {
+    // ------------------------------------------------ loads: lane 0 streams K (and Q), lane 1 V
+    if (lane < 2 && nblk > 0) {
+      const bool is_v = lane == 1;
+      const int ns = is_v ? VS : KS;
+      uint64_t* fullb = is_v ? vfull : kfull;
+      uint64_t* emptyb = is_v ? vempty : kempty;
+      const CUtensorMap* map = is_v ? &p.tmap_v : &p.tmap_k;
+      uint8_t* ring = sm + (is_v ? C::V_OFF : C::K_OFF);
+      const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
+      if (!is_v) {
+        mbar_arrive_expect_tx(qbar, C::DBOX * C::QATOM);
+        for (int db = 0; db < C::DBOX; ++db)
+          tma_load_3d(sm + C::Q_OFF + db * C::QATOM, &p.tmap_q, db * BOX_DIMS, kvh * G, q0 + t0, qbar);
       }
-      if (4 * j >= wbase + 32) {  // the next 32 units (8 stages)
-        wbase += 32;
-        win = win_load(wbase);
-      }
-      const int nsub = min(TC_KEYS / CHUNK, units - 4 * j);
-      uint8_t* kd = sm + C::KV_OFF + slot * C::STAGE_BYTES;
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], nsub * 2 * C::DBOX * BOX_BYTES);
-      for (int sub = 0; sub < nsub; ++sub) {
-        int phys = __shfl_sync(FULL_MASK, win, 4 * j + sub - wbase);
-        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
-          if (lane == 0) flags[0] = 1;  // never read outside the pool; the tile's outputs become NaN
-          phys = 0;
+      int loaded = 0;
+      for (int j = 0; j < nblk; ++j) {
+        const int slot = j % ns;
+        if (j >= ns && !tc_wait(&emptyb[slot], ((j / ns) - 1) & 1)) {
+          flags[1] = 1;
+          break;
         }
-        const int key0 = j * TC_KEYS + sub * CHUNK;
-        const int y = phys * p.block_size + key0 % p.block_size;
-        if (lane == 0) {
-#pragma unroll
-          for (int db = 0; db < C::DBOX; ++db) {
-            tma_load_3d(kd + db * C::KATOM + sub * BOX_BYTES, &p.tmap_k, db * BOX_DIMS, kvh, y, &full[slot]);
-            tma_load_3d(kd + C::KBYTES + db * C::KATOM + sub * BOX_BYTES, &p.tmap_v, db * BOX_DIMS, kvh, y,
-                        &full[slot]);
+        const int nsub = min(TC_KEYS / CHUNK, (kend - j * TC_KEYS + CHUNK - 1) / CHUNK);
+        uint8_t* dst = ring + slot * C::KBYTES;
+        mbar_arrive_expect_tx(&fullb[slot], nsub * C::DBOX * BOX_BYTES);
+        for (int sub = 0; sub < nsub; ++sub) {
+          const int key0 = j * TC_KEYS + sub * CHUNK;
+          int phys = __ldg(bt + key0 / p.block_size);
+          if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
+            flags[0] = 1;  // never read outside the pool; the tile's outputs become NaN
+            phys = 0;
           }
+          const int y = phys * p.block_size + key0 % p.block_size;
+#pragma unroll
+          for (int db = 0; db < C::DBOX; ++db)
+            tma_load_3d(dst + db * C::KATOM + sub * BOX_BYTES, map, db * BOX_DIMS, kvh, y, &fullb[slot]);
         }
+        loaded = j + 1;
       }
-      loaded = j + 1;
+      // the copies of the last stages land before the shared memory is released
+      for (int j = max(0, loaded - ns); j < loaded; ++j) (void)tc_wait(&fullb[j % ns], (j / ns) & 1);
     }
-    // the copies of the last stages land before the shared memory is released
-    for (int j = max(0, loaded - C::STAGES); j < loaded; ++j)
-      (void)tc_wait(&full[j % C::STAGES], (j / C::STAGES) & 1);
-  } else if (warp == 8) {
+  } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------ MMA issue (lane 0)
     if (lane == 0 && nblk > 0) {
       bool ok = tc_wait(qbar, 0);
       auto issue_qk = [&](int j) -> bool {
-        const int slot = j % C::STAGES;
-        if (!tc_wait(&full[slot], (j / C::STAGES) & 1)) return false;
+        const int slot = j % KS;
+        if (!tc_wait(&kfull[slot], (j / KS) & 1)) return false;
         tc_fence_after_sync();
-        const uint32_t kb = smem_addr(sm + C::KV_OFF + slot * C::STAGE_BYTES);
+        const uint32_t kb = smem_addr(sm + C::K_OFF + slot * C::KBYTES);
 #pragma unroll
         for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
           const uint32_t off = (ks & 3) << 5;  // 16 dims = 32 bytes along the swizzled row
@@ -238,19 +292,21 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
                    umma_desc_sw128(kb + (ks >> 2) * C::KATOM + off, 16, 1024), C::ID_S, ks > 0);
         }
         umma_commit(&sfull[j & 1]);
+        umma_commit(&kempty[slot]);  // the K stage is free once this Q K^T is done
         return true;
       };
       if (ok) ok = issue_qk(0);
       if (ok && nblk > 1) ok = issue_qk(1);
       for (int j = 0; ok && j < nblk; ++j) {
         const int b = j & 1;
-        if (!tc_wait(&pfull[b], (j >> 1) & 1)) {
+        const int vslot = j % VS;
+        if (!tc_wait(&pfull[b], (j >> 1) & 1) || !tc_wait(&vfull[vslot], (j / VS) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t vb = smem_addr(sm + C::KV_OFF + (j % C::STAGES) * C::STAGE_BYTES + C::KBYTES);
-        const uint32_t pb = sP + b * C::PBUF;
+        const uint32_t vb = smem_addr(sm + C::V_OFF + vslot * C::KBYTES);
+        const uint32_t pb = smem_addr(sm + C::P_OFF + (j % C::PBUFS) * C::PBUF);
 #pragma unroll
         for (int kk = 0; kk < TC_KEYS / 16; ++kk) {
           const uint64_t bdesc = umma_desc_sw128(vb + kk * 2048, C::KATOM, 1024);
@@ -259,7 +315,7 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
             umma_f16(tO, umma_desc_sw128(pb + C::PBYTES + (kk << 5), 16, 1024), bdesc, C::ID_PV, true);
         }
         umma_commit(&pvdone[b]);
-        umma_commit(&empty[j % C::STAGES]);
+        umma_commit(&vempty[vslot]);
         if (j + 2 < nblk && !issue_qk(j + 2)) ok = false;
       }
       if (!ok) flags[1] = 1;
@@ -267,12 +323,12 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
       if (!tc_wait(drain, 0)) flags[1] = 1;
     }
   } else {
-    // ------------------------------------------------ softmax: two threads per query row
-    // warp w (0-7) reads TMEM lanes 32 (w % 4) .. + 31: row r; half h = w / 4 takes keys
+    // ------------------------------------------------ softmax: SPLIT threads per query row
+    // warp w reads TMEM lanes 32 (w % 4) .. + 31: row r; half h = w / 4 (SPLIT 2) takes keys
     // [32 h, 32 h + 32) of every block and O columns [h DO / 2, (h + 1) DO / 2)
-    constexpr int HK = TC_KEYS / 2;
-    constexpr int HO = DO / 2;
-    const int h = warp >> 2;
+    constexpr int HK = TC_KEYS / C::SPLIT;  // keys of a block this thread scores
+    constexpr int HO = DO / C::SPLIT;       // O columns this thread owns
+    const int h = C::SPLIT == 2 ? warp >> 2 : 0;
     const int r = 32 * (warp & 3) + lane;
     const int t = t0 + r / G;
     const bool rv = t < t1;
@@ -280,12 +336,12 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     float* xch = reinterpret_cast<float*>(sm + C::XCH_OFF);  // [block % 2][half][row]
     const float sl2 = p.scale_log2;
-    float m_used = -INFINITY, l = 0.f;  // log2 units; l over this half's keys
+    float m_used = -INFINITY, l = 0.f;  // log2 units; l over this thread's keys
     // Every softmax thread runs every block, so that all of them meet at the
     // named barrier each time; after a wait gives up (ok false, warp-uniform)
     // a warp skips its remaining waits and its results become NaN.
     bool ok = true;
-    auto softmax_sync = []() { asm volatile("bar.sync 1, %0;" ::"n"(TC_SOFT) : "memory"); };
+    auto softmax_sync = []() { asm volatile("bar.sync 1, %0;" ::"n"(C::SOFT) : "memory"); };
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       if (ok) ok = __all_sync(FULL_MASK, tc_wait(bar, parity));
     };
@@ -297,7 +353,7 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
 #pragma unroll
       for (int c = 0; c < HK / 16; ++c) tmem_ld16(tmem + 64 * b + HK * h + lane_off + 16 * c, v[c]);
       tmem_wait_ld();
-      float x[HK];  // raw scores of keys k0 + HK h + c; masked ones become -inf
+      float x[HK];  // raw scores of keys k0 + c; masked ones become -inf
 #pragma unroll
       for (int c = 0; c < HK; ++c) x[c] = __uint_as_float(v[c >> 4][c & 15]);
       const int k0 = j * TC_KEYS + HK * h;
@@ -312,18 +368,24 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
 #pragma unroll
       for (int c = 4; c < HK; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
       float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-      xch[(b * 2 + h) * TC_ROWS + r] = mx;
-      softmax_sync();  // both halves of every row have published their maxima
-      mx = fmaxf(mx, xch[(b * 2 + (h ^ 1)) * TC_ROWS + r]);
+      if constexpr (C::SPLIT == 2) {
+        xch[(b * 2 + h) * TC_ROWS + r] = mx;
+        softmax_sync();  // both halves of every row have published their maxima
+        mx = fmaxf(mx, xch[(b * 2 + (h ^ 1)) * TC_ROWS + r]);
+      }
       const float m_new = fmaxf(m_used, mx * sl2);
-      if (j >= 2) wait(&pvdone[b], ((j - 2) >> 1) & 1);  // P buffer b is free once P V of block j - 2 is done
+      // the P buffer of block j is free once the P V of block j - PBUFS is done
+      if (j >= C::PBUFS) {
+        const int jj = j - C::PBUFS;
+        wait(&pvdone[jj & 1], (jj >> 1) & 1);
+      }
       if (j == 0) {
         m_used = m_new;
       } else {
-        const bool need = m_new > m_used + TC_RESCALE_LOG2;  // the same in both halves of a row
+        const bool need = m_new > m_used + TC_RESCALE_LOG2;  // the same for every thread of a row
         if (__any_sync(FULL_MASK, need)) {
-          // O must hold the P V of block j - 1 before this warp rescales its half rows
-          wait(&pvdone[b ^ 1], ((j - 1) >> 1) & 1);
+          // O must hold the P V of block j - 1 before this warp rescales its rows
+          wait(&pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1);
           tc_fence_after_sync();
           const float f = need ? ex2(m_used - m_new) : 1.f;
 #pragma unroll 1
@@ -341,9 +403,8 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
         }
       }
       const float nb = m_used == -INFINITY ? 0.f : -m_used;  // a row that has seen no key yet
-      // this half of the P row (32 keys, 64 bytes) into buffer b, 128-byte-swizzled K-major;
-      // the sums add the float32 weights
-      uint8_t* prow = sm + C::P_OFF + b * C::PBUF + r * 128;
+      // this thread's keys of the P row (128-byte-swizzled K-major); the sums add the float32 weights
+      uint8_t* prow = sm + C::P_OFF + (j % C::PBUFS) * C::PBUF + r * 128;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int u = 0; u < HK / 8; ++u) {
@@ -359,19 +420,19 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
             wr[i] = pack2<T>(p0 - f2.x, p1 - f2.y);
           }
         }
-        const int pu = ((4 * h + u) ^ (r & 7)) << 4;
+        const int pu = (((HK / 8) * h + u) ^ (r & 7)) << 4;
         *reinterpret_cast<uint4*>(prow + pu) = make_uint4(w[0], w[1], w[2], w[3]);
         if constexpr (BF16) *reinterpret_cast<uint4*>(prow + C::PBYTES + pu) = make_uint4(wr[0], wr[1], wr[2], wr[3]);
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // keys at or past kend in the last stage hold stale data: zero those V rows
+      // keys at or past kend in the last block hold stale data: zero those V rows
       if (j == nblk - 1 && kend < (j + 1) * TC_KEYS) {
-        const int slot = j % C::STAGES;
-        wait(&full[slot], (j / C::STAGES) & 1);
-        uint8_t* vd = sm + C::KV_OFF + slot * C::STAGE_BYTES + C::KBYTES;
+        const int vslot = j % VS;
+        wait(&vfull[vslot], (j / VS) & 1);
+        uint8_t* vd = sm + C::V_OFF + vslot * C::KBYTES;
         const int key_lo = kend - j * TC_KEYS;
         const int units = (TC_KEYS - key_lo) * 8;  // 16-byte units per atom
-        for (int i = threadIdx.x; i < units * C::DBOX; i += TC_SOFT) {
+        for (int i = threadIdx.x; i < units * C::DBOX; i += C::SOFT) {
           const int db = i / units;
           const int rem = i - db * units;
           *reinterpret_cast<uint4*>(vd + db * C::KATOM + (key_lo + rem / 8) * 128 + (rem % 8) * 16) =
@@ -397,11 +458,13 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
         for (int i = 0; i < 16; ++i) o[c + i] = __uint_as_float(w[i]);
       }
     }
-    xch[h * TC_ROWS + r] = l;  // the row sum is the two halves' sums
+    if constexpr (C::SPLIT == 2) xch[(4 + h) * TC_ROWS + r] = l;  // the row sum is the two halves' sums
+    if (!ok) flags[1] = 1;
     tc_fence_before_sync();
     __syncthreads();  // the other warps' flags and the partial sums are visible past this point
     if (rv) {
-      const float lt = l + xch[(h ^ 1) * TC_ROWS + r];
+      float lt = l;
+      if constexpr (C::SPLIT == 2) lt += xch[(4 + (h ^ 1)) * TC_ROWS + r];
       const float inv = (!have || ctx_bad || flags[0] || flags[1]) ? NAN : 1.f / lt;
       T* dst = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + t) * H + kvh * G + r % G) * HEAD_DIM + HO * h;
 #pragma unroll

@@ -427,11 +427,12 @@ cudaError_t launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   p.block_size = a.block_size;
   p.num_blocks = a.num_blocks;
   p.tile_tokens = TC_ROWS / group;
-  p.tiles = (a.max_query_len + p.tile_tokens - 1) / p.tile_tokens;
+  const int tiles = (a.max_query_len + p.tile_tokens - 1) / p.tile_tokens;
+  p.pairs = (tiles + TC_TILES - 1) / TC_TILES;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  if (p.tiles == 0) return cudaSuccess;
+  if (p.pairs == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.tiles, a.num_kv_heads, a.num_seqs);
+  cfg.gridDim = dim3(p.pairs, a.num_kv_heads, a.num_seqs);
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;

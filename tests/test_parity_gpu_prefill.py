@@ -133,3 +133,21 @@ def test_full_size_llama3_8b_prompts_sampled():
             ref = c_oracle.decode(b.q[r:r + 1], kc, vc, b.block_tables[s:s + 1], np.array([i + 1], np.int32),
                                   b.scale)
             assert float(np.abs(out[r] - ref[0]).max()) <= 2e-3, (s, i)
+
+
+def test_prefill_is_repeatable_bit_for_bit():
+    # the kernel's arithmetic order is fixed, so repeated launches agree to the bit; a
+    # race between the pipeline's stages (a buffer reused too early) would show here
+    b = batch(36, [700, 1500, 130], [700, 900, 130], 32, 8, 128)
+    kc, vc = T(b.k_cache), T(b.v_cache)
+    api.pa_reshape_and_cache(T(b.key), T(b.value), kc, vc, T(b.slot_mapping))
+    q, bt, cl, qsl = T(b.q), T(b.block_tables), T(b.context_lens), T(b.query_start_loc)
+    outs = []
+    for _ in range(8):
+        out = torch.empty_like(q)
+        api.pa_prefill(out, q, kc, vc, bt, cl, qsl, 900, b.scale)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    check(outs[0], oracle(b))

@@ -421,8 +421,7 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
   if (!aligned(query_start_loc, 4)) return fail(PA_ERR_INVALID_ARG, "query_start_loc must be 4-byte aligned");
   pa::PrefillArgs a{dtype,      out,       q,           k_cache,      v_cache,      block_tables,
                     context_lens, query_start_loc, max_blocks_per_seq, num_seqs, num_rows,
-                    max_query_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                    false};
+                    max_query_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale};
   return cuda_status(pa::launch_prefill(a, static_cast<cudaStream_t>(stream)), "prefill launch");
 }
 

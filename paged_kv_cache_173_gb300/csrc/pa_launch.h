@@ -95,7 +95,6 @@ struct PrefillArgs {
   int block_size;
   int num_blocks;
   float scale;
-  bool use_mma_sync;  // the m16n8k16 kernel instead of the tcgen05 one
 };
 
 // Record a formatted message as the calling thread's last error; returns status.

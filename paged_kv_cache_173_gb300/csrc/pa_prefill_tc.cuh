@@ -35,10 +35,9 @@
 // (then O and l of that row are rescaled in place), so P stays within
 // [0, 256] and the rescale is rare.
 //
-// The method is the one of paged_prefill_kernel (pa_prefill.cuh): each new
-// token attends to the positions up to its own ("in-depth reading", section
-// 5.1, item 5; "vAttention", paged prefill; online softmax of "vLLM
-// PagedAttention source walk-through", section 3.4).
+// The method: each new token attends to the positions up to its own
+// ("in-depth reading", section 5.1, item 5; "vAttention", paged prefill;
+// online softmax of "vLLM PagedAttention source walk-through", section 3.4).
 #pragma once
 
 #include "pa_decode.cuh"
@@ -175,7 +174,9 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
   const int kend = ctx_bad ? 0 : base + tile_end(ntiles - 1);  // the K/V stream's last key + 1
   const int nblk = tile_blocks(ntiles - 1);
 
-  if (threadIdx.x == 0) {
+  // The K load lane sets up the barriers and starts the Q copy at once, so that the
+  // copy overlaps the TMEM allocation and the barrier below.
+  if (warp == C::KLOAD_WARP && lane == 0) {
     for (int i = 0; i < KS; ++i) {
       mbar_init(&kfull[i], 1);
       mbar_init(&kempty[i], 1);
@@ -195,6 +196,13 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
+    if (nblk > 0) {
+      mbar_arrive_expect_tx(qbar, ntiles * C::QBYTES);
+      for (int u = 0; u < ntiles; ++u)
+        for (int db = 0; db < C::DBOX; ++db)
+          tma_load_3d(sm + C::Q_OFF + u * C::QBYTES + db * C::QATOM, &p.tmap_q, db * BOX_DIMS, kvh * G,
+                      q0 + ta + u * tt, qbar);
+    }
   }
   if (warp == 0) tmem_alloc(tslot, C::TMEM_COLS);
   tc_fence_before_sync();
@@ -213,13 +221,6 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
     int loaded = 0;
     if (lane == 0 && nblk > 0) {
       const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
-      if (!is_v) {
-        mbar_arrive_expect_tx(qbar, ntiles * C::QBYTES);
-        for (int u = 0; u < ntiles; ++u)
-          for (int db = 0; db < C::DBOX; ++db)
-            tma_load_3d(sm + C::Q_OFF + u * C::QBYTES + db * C::QATOM, &p.tmap_q, db * BOX_DIMS, kvh * G,
-                        q0 + ta + u * tt, qbar);
-      }
       // table entry of each box of block j, read a block ahead (the index is clamped to the
       // stream's last key, so that the loads need no select that would wait for them)
       int ph[NSUB];

@@ -42,8 +42,11 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention KV-read GB/s (% of GB300 HBM peak) and decode tokens/s"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_173_gb300", "csrc", "pa_decode.cuh")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.md")
+CSRC = os.path.join(ROOT, "paged_kv_cache_173_gb300", "csrc")
+# ncu DRAM traffic records: file, and the kernel sources whose hash they were taken on
+DECODE_TRAFFIC = (os.path.join(ROOT, "profiles", "decode_traffic.md"), ("pa_decode.cuh", "pa_ptx.cuh"))
+PREFILL_TRAFFIC = (os.path.join(ROOT, "profiles", "prefill_traffic.md"),
+                   ("pa_prefill.cuh", "pa_prefill_tc.cuh", "pa_decode.cuh", "pa_ptx.cuh"))
 
 
 # ----------------------------------------------------------------- workload
@@ -121,24 +124,26 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_source_sha() -> str:
+def source_sha(sources) -> str:
+    """sha256 of the kernel sources, in order, first 16 hex digits."""
     h = hashlib.sha256()
-    for p in (DECODE_SRC, os.path.join(os.path.dirname(DECODE_SRC), "pa_ptx.cuh")):
-        with open(p, "rb") as f:
+    for name in sources:
+        with open(os.path.join(CSRC, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def load_traffic(workload: str, kernel: str):
-    """ncu DRAM bytes (read + write) per decode launch, if they were taken on
-    the current kernel source for this workload and kernel."""
+def load_traffic(workload: str, kernel: str, record=DECODE_TRAFFIC):
+    """ncu DRAM bytes (read + write) per launch, if they were taken on the
+    current kernel sources for this workload and kernel."""
+    path, sources = record
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(path) as f:
             text = f.read()
         rec = json.loads(text.split("```json", 1)[1].split("```", 1)[0])
     except Exception:
         return None
-    if rec.get("source_sha") != decode_source_sha():
+    if rec.get("source_sha") != source_sha(sources):
         return None
     return rec.get("per_workload", {}).get(f"{workload}/{kernel}")
 
@@ -664,7 +669,9 @@ def run_prefill(args):
                    "steps_per_graph": G, "kernel_timing": mode},
         "kernel_ms": {n_: round(float(v), 4) for (n_, _), v in zip(kernels, per)},
         "roofline": {"kernel": "paged_prefill", "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": load_traffic(args.workload + ("-bf16" if b.dtype == "bf16" else ""), "paged_prefill",
+                                             PREFILL_TRAFFIC),
                      "peak_kind": f"{peak_kind} (fp16 MMAs take the bf16 figure: the same nominal rate)"},
         "gpu_launches": 2 * K,
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",

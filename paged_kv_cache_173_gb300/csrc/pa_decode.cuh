@@ -1186,15 +1186,17 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
 #endif
 
 // CTA shape per head size: 4 warps x 2 stages (8 KB stages up to d = 128,
-// three CTAs per SM); d = 256 has 16 KB stages and uses 2 warps x 2 stages
-// to keep three CTAs per SM.  E4M3 stages are 8 KB for every head size (two
-// chunks up to d = 128), so E4M3 keeps 4 warps x 2 stages throughout; the
-// sweep over 2-8 warps and 2-4 stages found nothing faster.
+// three CTAs per SM).  d = 256 has 16 KB stages and uses 2 warps x 1 stage,
+// six CTAs per SM: more CTAs in flight beat deeper per-warp pipelining there
+// (59.9 -> 55.0 us on the head-dim-256 workload; 2x2, 3x2, 4x2, 2x3, 4x1,
+// 8x1 and 1-warp shapes were slower).  E4M3 stages are 8 KB for every head
+// size (two chunks up to d = 128), so E4M3 keeps 4 warps x 2 stages
+// throughout; sweeps over 2-8 warps and 1-4 stages found nothing faster.
 template <int HEAD_DIM, int ELEM = 2>
 struct DecodeShape {
   static constexpr int WARPS = ELEM == 1 ? PA_DECODE_FP8_WARPS : (HEAD_DIM > 128 ? 2 : PA_DECODE_WARPS);
   static constexpr int STAGES = ELEM == 1 ? (HEAD_DIM > 128 ? 2 : PA_DECODE_FP8_STAGES)
-                                          : (HEAD_DIM > 128 ? 2 : PA_DECODE_STAGES);
+                                          : (HEAD_DIM > 128 ? 1 : PA_DECODE_STAGES);
 };
 
 template <typename T, typename KV, int HEAD_DIM>

@@ -1192,11 +1192,16 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
 // 8x1 and 1-warp shapes were slower).  E4M3 stages are 8 KB for every head
 // size (two chunks up to d = 128), so E4M3 keeps 4 warps x 2 stages
 // throughout; sweeps over 2-8 warps and 1-4 stages found nothing faster.
-template <int HEAD_DIM, int ELEM = 2>
+// PARTS: the split-K launch.  Its CTAs each cover one partition (at most
+// partition_size tokens), and at d = 128 one stage per warp (six CTAs per
+// SM) is faster there: llama3-8b 53.2 -> 52.6 us, long-context 227.0 ->
+// 217.9 us, 70B unchanged.  The single launch keeps two stages (with one it
+// lost 10-30%).
+template <int HEAD_DIM, int ELEM = 2, bool PARTS = false>
 struct DecodeShape {
   static constexpr int WARPS = ELEM == 1 ? PA_DECODE_FP8_WARPS : (HEAD_DIM > 128 ? 2 : PA_DECODE_WARPS);
   static constexpr int STAGES = ELEM == 1 ? (HEAD_DIM > 128 ? 2 : PA_DECODE_FP8_STAGES)
-                                          : (HEAD_DIM > 128 ? 1 : PA_DECODE_STAGES);
+                                          : (HEAD_DIM > 128 || (PARTS && HEAD_DIM == 128) ? 1 : PA_DECODE_STAGES);
 };
 
 template <typename T, typename KV, int HEAD_DIM>
@@ -1243,12 +1248,12 @@ int members_per_cta(const DecodeArgs& a) {
   return std::max(1, std::min(a.seqs_per_group, 8 * NT / G));
 }
 
-template <typename T, typename KV, int HEAD_DIM, int NT, int MODE>
+template <typename T, typename KV, int HEAD_DIM, int NT, int MODE, bool PARTS = false>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   constexpr bool CLUSTER = MODE == MODE_CLUSTER;
   constexpr int ELEM = kElemBytes<KV>;
-  constexpr int WARPS = DecodeShape<HEAD_DIM, ELEM>::WARPS;
-  constexpr int STAGES = DecodeShape<HEAD_DIM, ELEM>::STAGES;
+  constexpr int WARPS = DecodeShape<HEAD_DIM, ELEM, PARTS>::WARPS;
+  constexpr int STAGES = DecodeShape<HEAD_DIM, ELEM, PARTS>::STAGES;
   using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES, ELEM>;
   auto kern = paged_decode_kernel<T, KV, HEAD_DIM, NT, WARPS, STAGES, MODE>;
   static std::atomic<uint64_t> smem_set{0};
@@ -1327,8 +1332,9 @@ cudaError_t decode_slots(int* slots) {
 template <typename T, typename KV, int HEAD_DIM, int NT>
 cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
   if (a.cluster_size >= 0) {
-    return a.cluster_size > 0 ? launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER>(a, stream)
-                              : launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID>(a, stream);
+    if (a.cluster_size > 0) return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER>(a, stream);
+    return a.ws != nullptr ? launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, true>(a, stream)
+                           : launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID>(a, stream);
   }
   int slots = 0;
   cudaError_t e = decode_slots<T, KV, HEAD_DIM, NT>(&slots);

@@ -301,13 +301,20 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
         tc_fence_after_sync();
         return true;
       };
+      // The shared-memory descriptors are built once and moved by byte offsets per MMA: the
+      // issue of one thread is the MMAs' limit, and rebuilding a descriptor is a dependent
+      // chain of integer operations per instruction.
+      const uint64_t dq = umma_desc_sw128(sQ, 16, 1024);                                 // Q, K-major
+      const uint64_t dk = umma_desc_sw128(smem_addr(sm + C::K_OFF), 16, 1024);           // K, K-major
+      const uint64_t dv = umma_desc_sw128(smem_addr(sm + C::V_OFF), C::KATOM, 1024);     // V, MN-major
       auto qk = [&](int u, int j) {
-        const uint32_t kb = smem_addr(sm + C::K_OFF + (j % KS) * C::KBYTES);
+        const uint64_t qu = umma_desc_add(dq, u * C::QBYTES);
+        const uint64_t kj = umma_desc_add(dk, (j % KS) * C::KBYTES);
 #pragma unroll
         for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
-          const uint32_t off = (ks & 3) << 5;  // 16 dims = 32 bytes along the swizzled row
-          umma_f16(tmem + 256 * u, umma_desc_sw128(sQ + u * C::QBYTES + (ks >> 2) * C::QATOM + off, 16, 1024),
-                   umma_desc_sw128(kb + (ks >> 2) * C::KATOM + off, 16, 1024), C::ID_S, ks > 0);
+          const uint32_t off = (ks >> 2) * C::QATOM + ((ks & 3) << 5);  // 16 dims = 32 bytes along a row
+          const uint32_t koff = (ks >> 2) * C::KATOM + ((ks & 3) << 5);
+          umma_f16(tmem + 256 * u, umma_desc_add(qu, off), umma_desc_add(kj, koff), C::ID_S, ks > 0);
         }
         umma_commit(&sfull[u]);
       };
@@ -333,13 +340,13 @@ paged_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
             have_v = true;
           }
           tc_fence_after_sync();
-          const uint32_t vb = smem_addr(sm + C::V_OFF + vslot * C::KBYTES);
+          const uint64_t vj = umma_desc_add(dv, vslot * C::KBYTES);
           const uint32_t tP = tmem + 256 * u;
           const uint32_t tO = tP + 128;
 #pragma unroll
           for (int kk = 0; kk < TC_KEYS / 16; ++kk) {  // 16 keys = 8 columns of P
             const uint32_t pcol = 64 * (kk >> 2) + 8 * (kk & 3);
-            const uint64_t bdesc = umma_desc_sw128(vb + kk * 2048, C::KATOM, 1024);
+            const uint64_t bdesc = umma_desc_add(vj, kk * 2048);
             umma_f16_ts(tO, tP + pcol, bdesc, C::ID_PV, j > 0 || kk > 0);
             if constexpr (BF16) umma_f16_ts(tO, tP + pcol + 32, bdesc, C::ID_PV, true);
           }

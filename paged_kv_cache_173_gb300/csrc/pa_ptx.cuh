@@ -292,6 +292,12 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The descriptor `d` moved by `bytes` (a multiple of 16): the start-address
+// field holds address / 16 in its low 14 bits, so an offset adds to the
+// descriptor as long as the moved address stays below 256 KB, which every
+// shared-memory address does.  One add instead of rebuilding the descriptor.
+__device__ __forceinline__ uint64_t umma_desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // Instruction descriptor of a kind::f16 MMA with float32 accumulators:
 // A and B both fp16 (bf16 = false) or both bf16, M x N, B K-major (b_mn =
 // false) or MN-major; A is K-major.

@@ -1,7 +1,10 @@
-// pa_ptx.cuh -- thin inline-PTX wrappers used by the decode kernels (sm_103a).
+// pa_ptx.cuh -- thin inline-PTX wrappers used by the kernels (sm_103a).
 //
-// Asynchronous bulk copies (the TMA engine's non-tensor mode) with mbarrier
-// completion, ldmatrix / movmatrix fragment moves and the m16n8k16 f16 MMA.
+// mbarrier waits (every one bounded in time), TMA tensor copies with mbarrier
+// completion, ldmatrix / movmatrix fragment moves and the m16n8k16 MMA of the
+// decode kernels, and the tcgen05 / tensor-memory wrappers of the prefill
+// kernel (MMA descriptors, MMA issue and commit, TMEM allocation, loads and
+// stores).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -52,20 +55,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Non-blocking probe of the phase with the given parity (test_wait never
-// suspends the thread): true once that phase has completed.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -99,53 +88,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
-// Wait for the phase with the given parity with as little wake-up latency
-// as possible: test_wait never suspends the thread; the clock is read every
-// 256 probes.  Gives up (returns false) after `limit_ns` nanoseconds.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  const uint32_t a = smem_addr(bar);
-  uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if ((i & 255u) == 0) {
-      const uint64_t t = global_timer_ns();
-      if (i == 0) t0 = t;
-      else if (t - t0 > limit_ns) return false;
-    }
-  }
-}
-
-// try_wait without a suspend-time hint: the hardware picks how long a
-// probe may block.  Gives up after `limit_ns` nanoseconds.
-__device__ __forceinline__ bool mbar_wait_try(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  }
-}
-
 // ------------------------------------------------------------- bulk copies --
-// Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
-// 16-byte aligned); completion is counted in bytes on `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
-                                              uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
 // 3-D tiled tensor copy global -> shared through a tensor map (a
 // __grid_constant__ kernel parameter); completion counted on `bar`.
 // Coordinates are in elements, innermost first.

@@ -90,11 +90,18 @@ def test_prefill_matches_oracle(name):
     check(run(b), oracle(b))
 
 
-@pytest.mark.parametrize("name", ["whole-prompts-mha", "chunks-gqa4"])
+@pytest.mark.parametrize("name", ["whole-prompts-mha", "chunks-gqa4", "mixed-gqa8-d64-b32"])
 def test_prefill_bf16_matches_oracle(name):
     ctx, ql, H, Hk, d, B = CASES[name]
     b = batch(32, ctx, ql, H, Hk, d, B, dtype="bf16")
     check(run(b), oracle(b), "bf16")
+
+
+def test_prompts_spanning_several_tile_pairs_with_a_ragged_last_pair():
+    # MHA at d = 64: a tile is 128 tokens, a CTA's pair 256; 700 and 1100 tokens leave a last
+    # pair with one partial tile, and 300 leaves a pair whose second tile does not exist
+    b = batch(37, [700, 1100, 300], [700, 1100, 300], 4, 4, 64)
+    check(run(b), oracle(b))
 
 
 def test_first_row_of_a_prompt_returns_its_value():

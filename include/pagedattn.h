@@ -291,9 +291,12 @@ int pa_decode_prefix_splitk(void* out, const void* q, const void* k_cache, const
  * residual.
  *
  * Device-value outcomes: a context length below qlen or above
- * max_blocks_per_seq * block_size, or a block id read from the table outside
- * [0, num_blocks), gives NaN in the affected rows.  A sequence with qlen <= 0
- * writes nothing.  Nothing is read out of bounds.
+ * max_blocks_per_seq * block_size gives NaN in every row of that sequence.  A
+ * block id read from the table outside [0, num_blocks) gives NaN in every row
+ * of the CTA that reads it: two consecutive tiles of 128 rows (128 / G tokens
+ * times the G query heads of a KV head each), so rows of that pair that stop
+ * before the bad block are NaN too.  A sequence with qlen <= 0 writes
+ * nothing.  Nothing is read out of bounds.
  */
 int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,

@@ -425,6 +425,25 @@ int pa_decode_splitk_fp8(void* out, const void* q, const void* k_cache, const vo
                          int max_num_partitions, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/*
+ * pa_selftest_wait -- checks, on the device, the bounded wait that every
+ * pipeline of this library uses on its mbarriers (TMA copies landing, MMAs
+ * completing, softmax threads handing over P): a wait that runs past its
+ * limit gives up and reports instead of spinning, so a stage that never
+ * completes cannot hang the GPU; the library's kernels then write NaN rows.
+ *
+ * One warp waits on a phase that nothing completes, with a limit of
+ * limit_us microseconds, then on a phase completed by one arrival.
+ *
+ *   result    device int32 [3], 4-byte aligned: [0] = 1 if the first wait
+ *             gave up, [1] = 1 if the second wait returned, [2] = the
+ *             microseconds the first wait took (>= limit_us when it gave up)
+ *   limit_us  1 .. 10,000,000
+ *
+ * Asynchronous on `stream`; the device context stays usable afterwards.
+ */
+int pa_selftest_wait(int32_t* result, unsigned limit_us, void* stream);
+
 /* Fixed text naming a status code. */
 const char* pa_status_string(int status);
 

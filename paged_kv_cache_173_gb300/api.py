@@ -282,6 +282,22 @@ def pa_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cach
     _lib.check("pa_prefill", st)
 
 
+def pa_selftest_wait(device=None, limit_us: int = 20000,
+                     stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """Run the library's bounded-wait self-test on `device` (default: the current CUDA
+    device) and return {"gave_up", "completed", "waited_us"} once it has finished."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if dev.type != "cuda":
+        raise ValueError("the self-test runs on a CUDA device")
+    res = torch.full((3,), -1, dtype=torch.int32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = _lib.lib().pa_selftest_wait(int(res.data_ptr()), int(limit_us), int(s.cuda_stream))
+    _lib.check("pa_selftest_wait", st)
+    s.synchronize()
+    r = res.cpu().tolist()
+    return {"gave_up": r[0] == 1, "completed": r[1] == 1, "waited_us": r[2]}
+
+
 def pa_status_string(status: int) -> str:
     return _lib.status_name(status)
 

@@ -255,6 +255,16 @@ const char* pa_status_string(int status) {
 
 const char* pa_last_error(void) { return g_last_error; }
 
+int pa_selftest_wait(int32_t* result, unsigned limit_us, void* stream) {
+  if (!result) return fail(PA_ERR_INVALID_ARG, "result is NULL");
+  if (!aligned(result, 4)) return fail(PA_ERR_INVALID_ARG, "result must be 4-byte aligned");
+  if (limit_us == 0 || limit_us > 10000000u)
+    return fail(PA_ERR_INVALID_ARG, "limit_us %u must be in 1 .. 10,000,000", limit_us);
+  return cuda_status(pa::launch_wait_selftest(result, static_cast<uint64_t>(limit_us) * 1000u,
+                                              static_cast<cudaStream_t>(stream)),
+                     "wait self-test launch");
+}
+
 size_t pa_splitk_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_num_partitions) {
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_num_partitions <= 0) return 0;
   const size_t rows = pa::ws_rows(num_seqs, num_heads, max_num_partitions);

@@ -12,6 +12,10 @@
 //                             compression inside the block)
 //  copy_blocks_kernel         whole-block copies, the copy step of
 //                             copy-on-write
+//  wait_selftest_kernel       one warp through the bounded mbarrier wait that
+//                             every pipeline of the library uses: a wait on a
+//                             phase nothing completes must give up after its
+//                             limit, and a completed phase must be seen
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -212,6 +216,38 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) 
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, reshape_and_cache_kernel, p);
   if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+namespace {
+
+// result[0] = 1 if the wait on a phase that nothing completes gave up, result[1]
+// = 1 if the wait on a phase completed by one arrival returned, result[2] = the
+// microseconds the first wait took.
+__global__ void wait_selftest_kernel(int32_t* result, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar[2];
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);  // nothing arrives here
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&bar[1])) : "memory");
+  }
+  __syncwarp();
+  const uint64_t t0 = global_timer_ns();
+  const bool never = mbar_wait_bounded(&bar[0], 0, limit_ns);
+  const uint64_t t1 = global_timer_ns();
+  const bool done = mbar_wait_bounded(&bar[1], 0, limit_ns);
+  if (threadIdx.x == 0) {
+    result[0] = never ? 0 : 1;
+    result[1] = done ? 1 : 0;
+    result[2] = static_cast<int32_t>((t1 - t0) / 1000u);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(int32_t* result, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(result, limit_ns);
   return cudaGetLastError();
 }
 

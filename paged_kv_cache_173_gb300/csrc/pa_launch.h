@@ -102,6 +102,7 @@ int set_last_error(int status, const char* fmt, ...);
 
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
+cudaError_t launch_wait_selftest(int32_t* result, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceArgs& a, cudaStream_t stream);
 

@@ -192,3 +192,8 @@ def _prefill(L, **kw):
 ])
 def test_prefill_checks_arguments(L, kw, status):
     assert _prefill(L, **kw) == status
+
+
+@pytest.mark.parametrize("args", [(None, 1000), (A, 0), (A, 10_000_001), (A + 2, 1000)])
+def test_wait_selftest_checks_arguments(L, args):
+    assert L.pa_selftest_wait(args[0], args[1], None) == _lib.PA_ERR_INVALID_ARG

@@ -42,27 +42,31 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention KV-read GB/s (% of GB300 HBM peak) and decode tokens/s"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # the vendor's nominal HBM3e bandwidth of one GB300, for context
+# full-size configurations timed after the headline, each as its own entry of "configs"
+DEFAULT_CONFIGS = "llama2-70b-b16,llama2-70b-b32,long-context"
 CSRC = os.path.join(ROOT, "paged_kv_cache_173_gb300", "csrc")
-# ncu DRAM traffic records: file, and the kernel sources whose hash they were taken on
-DECODE_TRAFFIC = (os.path.join(ROOT, "profiles", "decode_traffic.md"), ("pa_decode.cuh", "pa_ptx.cuh"))
-PREFILL_TRAFFIC = (os.path.join(ROOT, "profiles", "prefill_traffic.md"),
-                   ("pa_prefill.cuh", "pa_prefill_tc.cuh", "pa_decode.cuh", "pa_ptx.cuh"))
+# ncu DRAM traffic records (JSON): each names the kernel sources whose hash it was taken on
+DECODE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_traffic.json")
+PREFILL_TRAFFIC = os.path.join(ROOT, "profiles", "prefill_traffic.json")
 
 
 # ----------------------------------------------------------------- workload
-def make_workload(name: str, seed: int, partition_size: int, dtype: str = "fp16", kv_dtype: str = ""):
+def make_workload(name: str, seed: int, partition_size: int, dtype: str = "fp16", kv_dtype: str = "",
+                  draw_pools: bool = True):
     from paged_kv_cache_173_gb300 import workloads
     kw = dict(seed=seed, poison=False, partition_size=partition_size, dtype=dtype, kv_dtype=kv_dtype)
+    big = {} if draw_pools else {"draw_pools": False}  # only the presets with large pools take it
     if name == "llama3-8b":
         b = workloads.llama3_8b(**kw)
         desc = ("llama3-8b decode layer: S=64, H=32, Hk=8, d=128, B=16, ctx~U[128,2048], "
                 "1.25x pool, shuffled ids, 1 new token/seq")
     elif name in ("llama2-70b-b16", "llama2-70b-b32"):
         bs = int(name[-2:])
-        b = workloads.llama2_70b(block_size=bs, **kw)
+        b = workloads.llama2_70b(block_size=bs, **kw, **big)
         desc = f"llama2-70b GQA decode: S=32, H=64, Hk=8, d=128, B={bs}, ctx=8192, 1.25x pool, shuffled"
     elif name == "long-context":
-        b = workloads.long_context(**kw)
+        b = workloads.long_context(**kw, **big)
         desc = "long-context decode: S=4, ctx {32K,64K,96K,128K}, H=32, Hk=8, d=128, B=16"
     elif name == "shared-prefix":
         b = workloads.shared_prefix(**kw)
@@ -133,17 +137,16 @@ def source_sha(sources) -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(workload: str, kernel: str, record=DECODE_TRAFFIC):
-    """ncu DRAM bytes (read + write) per launch, if they were taken on the
-    current kernel sources for this workload and kernel."""
-    path, sources = record
+def load_traffic(workload: str, kernel: str, record: str = DECODE_TRAFFIC):
+    """ncu DRAM bytes (read + write) per launch from a JSON record, if they
+    were taken on the current kernel sources for this workload and kernel;
+    None otherwise."""
     try:
-        with open(path) as f:
-            text = f.read()
-        rec = json.loads(text.split("```json", 1)[1].split("```", 1)[0])
-    except Exception:
-        return None
-    if rec.get("source_sha") != source_sha(sources):
+        with open(record) as f:
+            rec = json.load(f)
+        if rec.get("source_sha") != source_sha(rec["sources"]):
+            return None
+    except (OSError, ValueError, KeyError, TypeError):
         return None
     return rec.get("per_workload", {}).get(f"{workload}/{kernel}")
 
@@ -239,13 +242,21 @@ def _make_event(torch, external: bool):
 
 
 def time_path(torch, dev, stream, kernels, nrep: int, K: int, W: int, clocks=None, dist=None):
-    """Time exactly K steps of one path; a step calls each of `kernels` (name,
-    fn(r)) in order on replica r % nrep.  Steps run as CUDA-graph replays; the
-    last G steps carry an event between kernels.  Those events are recorded
-    inside the graph when torch supports external events, otherwise the last
-    G steps run eagerly (the host enqueues them while the GPU still replays the
-    graphs).  Returns total ms, per-kernel mean ms, wall times and the timing mode."""
-    G = min(K, 8 * nrep)
+    """Time exactly K steps of one path; a step calls each of `kernels`
+    (name, fn(r)) in order on replica r % nrep.
+
+    The timed region holds the path's own launches and nothing else: CUDA-graph
+    replays of plain steps (a graph of G steps replayed K // G times, then a
+    graph of the K % G remaining steps), bracketed by two events.  The
+    per-kernel split comes from a separate pass after the timed region: G
+    more steps with an event between kernels, recorded inside a graph when
+    torch supports external events, else enqueued eagerly.  Event nodes keep
+    the launches of that pass from overlapping, so its durations are upper
+    bounds.  Returns (ms of the K timed steps, per-kernel mean ms of the
+    separate pass, wall-clock bounds of the timed region, how the split was
+    taken, G)."""
+    G = min(K, 8 * nrep)  # a multiple of nrep whenever K >= 8 * nrep
+    n_full, tail = divmod(K, G)
 
     def step(r, ev=None):
         for j, (_, fn) in enumerate(kernels):
@@ -267,34 +278,16 @@ def time_path(torch, dev, stream, kernels, nrep: int, K: int, W: int, clocks=Non
                 step(i, evs[i] if evs is not None else None)
         return g
 
-    n_plain = (K - G) // G
-    tail = K - G - n_plain * G
-    g_plain = capture(G) if n_plain else None
+    g_full = capture(G) if n_full else None
     g_tail = capture(tail) if tail else None
-    mode = "graph-events"
-    evs = None
-    g_ev = None
-    try:
-        evs = [[_make_event(torch, True) for _ in range(len(kernels) + 1)] for _ in range(G)]
-        g_ev = capture(G, evs)
-        with torch.cuda.stream(stream):
-            g_ev.replay()
-        torch.cuda.synchronize(dev)
-        evs[0][0].elapsed_time(evs[0][1])
-    except Exception:
-        mode = "eager-events"
-        g_ev = None
-        evs = [[_make_event(torch, False) for _ in range(len(kernels) + 1)] for _ in range(G)]
-    with torch.cuda.stream(stream):  # untimed pass over every graph
-        if g_plain:
-            g_plain.replay()
-        if g_tail:
+    with torch.cuda.stream(stream):  # untimed rehearsal of every graph
+        if g_full is not None:
+            g_full.replay()
+        if g_tail is not None:
             g_tail.replay()
-        if g_ev is None:
-            for i in range(G):
-                step(i, evs[i])
     torch.cuda.synchronize(dev)
 
+    # ---- the timed region: K plain steps
     if clocks:
         clocks.start()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -305,15 +298,10 @@ def time_path(torch, dev, stream, kernels, nrep: int, K: int, W: int, clocks=Non
     wall0 = time.time()
     with torch.cuda.stream(stream):
         e0.record()
-        for _ in range(n_plain):
-            g_plain.replay()
-        if g_tail:
+        for _ in range(n_full):
+            g_full.replay()
+        if g_tail is not None:
             g_tail.replay()
-        if g_ev is not None:
-            g_ev.replay()
-        else:
-            for i in range(G):
-                step(i, evs[i])
         e1.record()
     torch.cuda.synchronize(dev)
     if dist is not None:
@@ -322,17 +310,82 @@ def time_path(torch, dev, stream, kernels, nrep: int, K: int, W: int, clocks=Non
     if clocks:
         clocks.stop()
     ms = e0.elapsed_time(e1)
+
+    # ---- the per-kernel split: a separate pass of G steps with events
+    mode = "separate pass after the timed region, events inside a graph"
+    try:
+        evs = [[_make_event(torch, True) for _ in range(len(kernels) + 1)] for _ in range(G)]
+        g_ev = capture(G, evs)
+        with torch.cuda.stream(stream):
+            g_ev.replay()  # first replay uploads the graph
+            g_ev.replay()
+        torch.cuda.synchronize(dev)
+        evs[0][0].elapsed_time(evs[0][1])
+    except Exception:
+        mode = "separate pass after the timed region, eager events"
+        evs = [[_make_event(torch, False) for _ in range(len(kernels) + 1)] for _ in range(G)]
+        with torch.cuda.stream(stream):
+            for i in range(G):
+                step(i, evs[i])
+        torch.cuda.synchronize(dev)
     per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(len(kernels))] for i in range(G)])
     return ms, per.mean(axis=0), (wall0, wall1), mode, G
 
 
-def run_gpu(args, rank: int, world: int):
+def device_pools(torch, b, dev, seed: int):
+    """K and V pools of the batch's shape filled on the device: standard
+    normal float32 draws (torch's generator, seeded) rounded to the pool's
+    element type; E4M3 pools hold the codes of N(0,1) / k_scale as the host
+    recipe does."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed))
+    pools = []
+    for _ in range(2):
+        x = torch.randn(b.k_cache.shape, generator=g, device=dev, dtype=torch.float32)
+        if b.kv_dtype == "fp8":
+            pools.append((x / b.k_scale).to(torch.float8_e4m3fn).view(torch.uint8))
+        else:
+            pools.append(x.to(torch.bfloat16 if b.dtype == "bf16" else torch.float16))
+        del x
+    return pools
+
+
+def other_bytes(b, path: str) -> dict:
+    """Bytes a step moves besides the KV reads, by kind: the queries read and
+    the outputs written, the block-table entries and context lengths read, the
+    new tokens' K/V read and written into the pools (with their slots), and,
+    for the split-K and shared-prefix paths, the float32 partial rows written
+    by the decode and read by the reduce."""
+    S, H, d, B = b.num_seqs, b.num_heads, b.head_dim, b.block_size
+    qe = 2
+    kve = 1 if b.kv_dtype == "fp8" else 2
+    ctx = b.context_lens.astype(np.int64)
+    T = b.num_tokens
+    r = {
+        "q": S * H * d * qe,
+        "out": S * H * d * qe,
+        "block_tables": int(np.sum((ctx + B - 1) // B)) * 4,
+        "context_lens": S * 4,
+        "new_tokens": T * b.num_kv_heads * d * (2 * qe + 2 * kve) + T * 8,
+        "splitk_partials": 0,
+    }
+    if path in ("splitk", "prefix"):
+        nparts = (ctx + b.partition_size - 1) // b.partition_size
+        rows = int(np.sum(np.where(nparts > 1, nparts, 0))) * H
+        r["splitk_partials"] = 2 * rows * (d + 2) * 4
+    return r
+
+
+def measure_workload(args, name: str, dev, world: int, dist_g, host_pools: bool = True):
+    """Time every decode path of one workload (each K steps, as time_path
+    does) and return the batch, the device buffers and the per-path results.
+    host_pools=False draws the pools on the device (device_pools)."""
     import torch
     from paged_kv_cache_173_gb300 import api, workloads
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    b, desc = make_workload(args.workload, args.seed + rank, args.partition_size, args.dtype, args.kv_dtype)
+    rank = int(os.environ.get("RANK", "0"))
+    b, desc = make_workload(name, args.seed + rank, args.partition_size, args.dtype, args.kv_dtype,
+                            draw_pools=host_pools)
     kv_bytes = workloads.algorithmic_kv_bytes(b)
     write_kv, decode_kv, splitk_kv = kv_ops(api, b)
     ps = b.partition_size
@@ -342,10 +395,12 @@ def run_gpu(args, rank: int, world: int):
     pool_bytes = 2 * b.k_cache.nbytes
     l2_bytes = 129 * 2 ** 20
     R = max(2, min(8, math.ceil(4 * l2_bytes / max(1, kv_bytes)) + 1))
-    reps = []
-    k0, v0, q0 = t(b.k_cache), t(b.v_cache), t(b.q)
-    for r in range(R):
-        reps.append((k0.clone(), v0.clone(), q0.clone()) if r else (k0, v0, q0))
+    if host_pools:
+        k0, v0 = t(b.k_cache), t(b.v_cache)
+    else:
+        k0, v0 = device_pools(torch, b, dev, args.seed + 7919 * (rank + 1))
+    q0 = t(b.q)
+    reps = [(k0.clone(), v0.clone(), q0.clone()) if r else (k0, v0, q0) for r in range(R)]
     key, value, sm = t(b.key), t(b.value), t(b.slot_mapping)
     bt, cl = t(b.block_tables), t(b.context_lens)
     out = torch.empty_like(q0)
@@ -386,25 +441,60 @@ def run_gpu(args, rank: int, world: int):
         raise SystemExit(f"--path {args.path} needs a workload with shared-prefix groups")
     want = list(paths) if args.path == "auto" else [args.path]
     stream = torch.cuda.Stream(dev)
-    K, W = args.steps, args.warmup
-    import torch.distributed as dist
-    dist_g = dist if (world > 1 and dist.is_initialized()) else None
     results = {}
-    for name in want:
+    for pname in want:
         clocks = ClockSampler(dev.index)
-        ms, per, walls, mode, G = time_path(torch, dev, stream, paths[name], R, K, W, clocks, dist_g)
+        ms, per, walls, mode, G = time_path(torch, dev, stream, paths[pname], R, args.steps, args.warmup, clocks,
+                                            dist_g)
         if dist_g is not None:
             ms = max_over_ranks(ms, dev)
-        results[name] = dict(ms=ms, per=per, clocks=clocks.summary(*walls), mode=mode, G=G)
-    best = min(results, key=lambda n: results[n]["ms"])
-    r0 = results[best]
-    kern = paths[best]
+        results[pname] = dict(ms=ms, per=per, clocks=clocks.summary(*walls), mode=mode, G=G)
+    best = min(results, key=lambda n: results[n]["ms"])  # chosen on the plain timed steps
+    return dict(b=b, desc=desc, kv_bytes=kv_bytes, paths=paths, results=results, best=best, R=R,
+                pool_bytes=pool_bytes, reps=reps, ws=ws, P=P, stream=stream)
+
+
+def summarize(m, world: int, K: int, peak: float) -> dict:
+    """The per-path figures of one measured workload: step time, whole-job
+    GB/s, fractions of the copy bandwidth for the step and for the decode
+    launch (its algorithmic bytes over its separate-pass event time)."""
+    from paged_kv_cache_173_gb300 import workloads
+    b, kv_bytes = m["b"], m["kv_bytes"]
+    out = {}
+    for pname, v in m["results"].items():
+        roof = workloads.unique_kv_bytes(b) if pname == "prefix" else kv_bytes
+        t_dec = float(v["per"][1])
+        val = whole_job_gbs(kv_bytes, K, world, v["ms"])
+        out[pname] = {
+            "ms_per_step": round(v["ms"] / K, 5),
+            "value": round(val, 1),
+            "step_frac": round(val / world / peak, 4),
+            "kernel_ms": {kn: round(float(x), 5) for (kn, _), x in zip(m["paths"][pname], v["per"])},
+            "kernel_frac": round(roof / (t_dec * 1e-3) / 1e9 / peak, 4),
+        }
+    return out
+
+
+def run_gpu(args, rank: int, world: int):
+    import torch
+    from paged_kv_cache_173_gb300 import workloads
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    import torch.distributed as dist
+    dist_g = dist if (world > 1 and dist.is_initialized()) else None
+    K, W = args.steps, args.warmup
+    peak, peak_kind = load_peak()
+
+    m = measure_workload(args, args.workload, dev, world, dist_g, host_pools=True)
+    b, kv_bytes, best = m["b"], m["kv_bytes"], m["best"]
+    r0 = m["results"][best]
+    kern = m["paths"][best]
     decode_name = kern[1][0]
     t_decode = float(r0["per"][1])
 
-    e2e = run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, best)
+    e2e = run_e2e(args, b, dev, m["reps"], m["ws"], m["P"], kv_bytes, m["stream"], best)
 
-    peak, peak_kind = load_peak()
     ms = r0["ms"]
     value = whole_job_gbs(kv_bytes, K, world, ms)
     step_ms = ms / K
@@ -413,6 +503,7 @@ def run_gpu(args, rank: int, world: int):
     roof_bytes = workloads.unique_kv_bytes(b) if best == "prefix" else kv_bytes
     achieved = roof_bytes / (t_decode * 1e-3) / 1e9
     traffic = load_traffic(workload_key(args), decode_name)
+    ob = other_bytes(b, best)
     res = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -427,22 +518,29 @@ def run_gpu(args, rank: int, world: int):
         "dtype": "bf16" if b.dtype == "bf16" else "f16",
         "data": "synthetic",
         "config": {
-            "workload": desc,
+            "workload": m["desc"],
             "kv_cache": "e4m3, one float scale per pool" if b.kv_dtype == "fp8" else b.dtype,
             "kv_bytes_per_step": kv_bytes,
             "path": best,
+            "path_chosen_on": "the plain timed steps of each path",
             "step": " -> ".join(n for n, _ in kern),
-            "partition_size": ps if best in ("splitk", "prefix") else None,
+            "partition_size": b.partition_size if best in ("splitk", "prefix") else None,
             "roofline_bytes": ("unique KV bytes (each shared block once)" if best == "prefix"
                                else "algorithmic KV bytes"),
-            "l2": f"{R} rotating pool replicas ({R * pool_bytes / 1e9:.2f} GB) > 129 MB L2; steps back to back",
+            "l2": (f"{m['R']} rotating pool replicas ({m['R'] * m['pool_bytes'] / 1e9:.2f} GB) > 129 MB L2; "
+                   "steps back to back"),
+            "timed_region": f"{K} plain steps as CUDA-graph replays, no events inside",
             "steps_per_graph": r0["G"],
             "kernel_timing": r0["mode"],
         },
         "hbm_frac_of_step": round(value / world / peak, 4),
         "hbm_peak_gbs": peak,
         "hbm_peak_kind": peak_kind,
+        "hbm_frac_of_nominal": round(value / world / NOMINAL_HBM_GBS, 4),
+        "nominal_hbm_gbs": NOMINAL_HBM_GBS,
         "tokens_per_s": round(b.num_seqs * world / (step_ms * 1e-3), 1),
+        "other_bytes_per_step": ob,
+        "other_bytes_frac_of_kv": round(sum(ob.values()) / kv_bytes, 5),
         "kernel_ms": {n: round(float(v), 5) for (n, _), v in zip(kern, r0["per"])},
         "roofline": {
             "kernel": decode_name,
@@ -457,13 +555,33 @@ def run_gpu(args, rank: int, world: int):
         "gpu_launches": (len(kern) + (1 if best == "prefix" else 0)) * K,
         "e2e": e2e,
         "clocks": r0["clocks"],
-        "paths": {n: {"ms_per_step": round(v["ms"] / K, 5),
-                      "value": round(whole_job_gbs(kv_bytes, K, world, v["ms"]), 1),
-                      "kernel_ms": {kn: round(float(x), 5) for (kn, _), x in zip(paths[n], v["per"])}}
-                  for n, v in results.items()},
+        "paths": summarize(m, world, K, peak),
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(b, kv_bytes, budget_s=args.cpu_seconds)
+    del m
+    torch.cuda.empty_cache()
+
+    # the other full-size configurations, each timed the same way
+    names = [] if args.configs == "none" else [c for c in args.configs.split(",") if c and c != args.workload]
+    if names:
+        res["configs"] = {}
+        launches = 0
+        for name in names:
+            mc = measure_workload(args, name, dev, world, dist_g, host_pools=False)
+            per_path = summarize(mc, world, K, peak)
+            bp = mc["best"]
+            entry = {"workload": mc["desc"], "kv_bytes_per_step": mc["kv_bytes"], "path": bp,
+                     "partition_size": mc["b"].partition_size if bp in ("splitk", "prefix") else None,
+                     "values": "pools drawn on the device (torch generator, N(0,1))",
+                     "clocks": mc["results"][bp]["clocks"], **per_path[bp],
+                     "tokens_per_s": round(mc["b"].num_seqs * world / (mc["results"][bp]["ms"] / K * 1e-3), 1),
+                     "paths": per_path}
+            launches += len(mc["paths"][bp]) * K
+            res["configs"][name] = entry
+            del mc
+            torch.cuda.empty_cache()
+        res["configs_gpu_launches"] = launches
     return res
 
 
@@ -845,6 +963,10 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--reference-seconds", type=float, default=90.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--configs", default=None,
+                   help="comma-separated workloads timed after the headline, each in the line's "
+                        f"\"configs\" object (default with the llama3-8b decode step: {DEFAULT_CONFIGS}; "
+                        "'none' for none)")
     return p.parse_args(argv)
 
 
@@ -856,6 +978,9 @@ def main(argv=None):
         raise SystemExit("--kv-dtype fp8 takes --dtype fp16")
     if args.warmup < 3:
         args.warmup = 3
+    if args.configs is None:
+        plain = args.workload == "llama3-8b" and args.dtype == "fp16" and not args.kv_dtype and args.path == "auto"
+        args.configs = DEFAULT_CONFIGS if plain else "none"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

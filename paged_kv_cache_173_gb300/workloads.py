@@ -138,8 +138,14 @@ def build_batch(
     q_scale: float = 1.0,
     dtype: str = "fp16",
     kv_dtype: str = "",
+    draw_pools: bool = True,
 ) -> PagedBatch:
     """Build one batch.
+
+    ``draw_pools=False`` leaves the K and V pools undrawn (allocated, not
+    filled, and not taken from ``rng``, so the new tokens' draws move up):
+    for timing runs that fill the pools on the device themselves.  It needs
+    ``poison=False``.
 
     ``share_groups``: lists of sequence indices whose first
     ``shared_prefix_len`` tokens (a whole number of blocks) live in the same
@@ -203,7 +209,12 @@ def build_batch(
     q = _normal_f16(rng, (S, H, d), dtype=dtype)
     if q_scale != 1.0:
         q = (q.astype(np.float32) * np.float32(q_scale)).astype(np.float16)
-    if kv_dtype == "fp8":
+    if not draw_pools:
+        assert not poison, "undrawn pools cannot be poisoned"
+        k_cache = np.empty((N, B, Hk, d), dtype=np.uint8 if kv_dtype == "fp8" else
+                           (np.float16 if dtype == "fp16" else np.uint16))
+        v_cache = np.empty_like(k_cache)
+    elif kv_dtype == "fp8":
         assert dtype == "fp16", "FP8 caches take float16 queries and new tokens"
         k_cache = f32_to_e4m3_codes(_normal_f16(rng, (N, B, Hk, d)).astype(np.float32) / np.float32(FP8_SCALE))
         v_cache = f32_to_e4m3_codes(_normal_f16(rng, (N, B, Hk, d)).astype(np.float32) / np.float32(FP8_SCALE))
@@ -380,22 +391,25 @@ def llama3_8b(seed: int = 0, num_seqs: int = 64, poison: bool = True,
 
 
 def llama2_70b(seed: int = 0, block_size: int = 16, num_seqs: int = 32, ctx: int = 8192,
-               poison: bool = True, partition_size: int = 512, dtype: str = "fp16", kv_dtype: str = "") -> PagedBatch:
+               poison: bool = True, partition_size: int = 512, dtype: str = "fp16", kv_dtype: str = "",
+               draw_pools: bool = True) -> PagedBatch:
     """Llama-2-70B-shaped GQA decode: 64 q heads, 8 KV heads (GQA 8), d = 128;
     every context ``ctx`` tokens; one new token per sequence at position
     ctx - 1; 1.25x pool, shuffled ids."""
     return build_batch(name=f"llama2-70b-b{block_size}", seed=seed, context_lens=[ctx] * num_seqs,
                        num_heads=64, num_kv_heads=8, head_dim=128, block_size=block_size,
-                       poison=poison, partition_size=partition_size, dtype=dtype, kv_dtype=kv_dtype)
+                       poison=poison, partition_size=partition_size, dtype=dtype, kv_dtype=kv_dtype,
+                       draw_pools=draw_pools)
 
 
 def long_context(seed: int = 0, ctxs: Sequence[int] = (32768, 65536, 98304, 131072),
-                 poison: bool = True, partition_size: int = 512, dtype: str = "fp16", kv_dtype: str = "") -> PagedBatch:
+                 poison: bool = True, partition_size: int = 512, dtype: str = "fp16", kv_dtype: str = "",
+                 draw_pools: bool = True) -> PagedBatch:
     """Long-context split-K decode: 32 q heads, 8 KV heads, d = 128, B = 16;
     4 sequences of 32K..128K tokens; 512-token partitions."""
     return build_batch(name="long-context", seed=seed, context_lens=list(ctxs), num_heads=32,
                        num_kv_heads=8, head_dim=128, block_size=16, poison=poison,
-                       partition_size=partition_size, dtype=dtype, kv_dtype=kv_dtype)
+                       partition_size=partition_size, dtype=dtype, kv_dtype=kv_dtype, draw_pools=draw_pools)
 
 
 def shared_prefix(seed: int = 0, num_prompts: int = 16, samples: int = 8, prompt_len: int = 1024,

@@ -155,13 +155,9 @@ def test_head_dim_256_matches_oracle(dtype, shape):
     check(d.splitk(1024), ref, dtype)
 
 
-def test_bf16_full_size_llama3_8b_sampled():
+def test_bf16_full_size_llama3_8b_every_sequence():
     b = workloads.llama3_8b(dtype="bf16")
     d = Dev(b)
-    seqs = [0, 21, 63]
-    ref = oracle_out(b, seqs)
-    out = d.decode()
-    sk = d.splitk(512)
-    for i, s in enumerate(seqs):
-        check(out[s:s + 1], ref[i:i + 1], "bf16")
-        check(sk[s:s + 1], ref[i:i + 1], "bf16")
+    ref = oracle_out(b)
+    check(d.decode(), ref, "bf16")
+    check(d.splitk(512), ref, "bf16")

@@ -218,13 +218,14 @@ def test_fp8_copy_blocks_is_bit_exact():
     assert np.array_equal(d.v_cache.cpu().numpy(), ref_v)
 
 
-def test_fp8_full_size_llama3_8b_sampled():
-    b = workloads.llama3_8b(kv_dtype="fp8")
+@pytest.mark.parametrize("name", ["llama3-8b", "llama2-70b-b16", "long-context"])
+def test_fp8_full_size_every_sequence(name):
+    make = {"llama3-8b": lambda: workloads.llama3_8b(kv_dtype="fp8"),
+            "llama2-70b-b16": lambda: workloads.llama2_70b(block_size=16, kv_dtype="fp8"),
+            "long-context": lambda: workloads.long_context(kv_dtype="fp8")}[name]
+    b = make()
     d = Dev(b)
-    seqs = [0, 21, 63]
-    ref = oracle_out(b, seqs)
-    out = d.decode()
-    sk = d.splitk(512)
-    for i, s in enumerate(seqs):
-        check(out[s:s + 1], ref[i:i + 1])
-        check(sk[s:s + 1], ref[i:i + 1])
+    ref = oracle_out(b)
+    check(d.decode(), ref)
+    check(d.splitk(512), ref)
+    check(d.splitk(1024), ref)

@@ -181,14 +181,11 @@ def test_bad_context_length_gives_nan_for_that_sequence_only():
     assert float(np.abs(out[others] - ref[others]).max()) <= 2e-3
 
 
-def test_prefix_full_size_shared_prefix_sampled():
-    b = workloads.shared_prefix()
+@pytest.mark.parametrize("kv_dtype", ["", "fp8"])
+def test_prefix_full_size_shared_prefix_every_sequence(kv_dtype):
+    b = workloads.shared_prefix(kv_dtype=kv_dtype)
     assert b.seqs_per_group == 8 and (b.prefix_lens == 1024).all()
-    seqs = [0, 7, 8, 77, 127]
-    ref = oracle_out(b, seqs)
-    out = Dev(b).prefix(512)
-    for i, s in enumerate(seqs):
-        check(out[s:s + 1], ref[i:i + 1])
+    check(Dev(b).prefix(512), oracle_out(b))
 
 
 def test_seqs_per_group_one_is_per_sequence_decode():

@@ -17,7 +17,10 @@
  *  - Pointers are DEVICE pointers owned by the caller.  The library allocates
  *    nothing and keeps no state between calls except a per-thread text of
  *    the last error (pa_last_error), a per-device record of which kernel
- *    attributes it has already set, and the fixed device array that
+ *    attributes it has already set, a per-thread cache of the TMA
+ *    descriptors it encoded for recently seen pools (a descriptor depends
+ *    only on the pool's address and shape, so a cached one is always the one
+ *    a fresh encoding gives), and the fixed device array that
  *    pa_decode_splitk_static uses as its workspace.
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL means the legacy default stream).  The caller synchronises.
@@ -259,6 +262,74 @@ int pa_decode_prefix_splitk(void* out, const void* q, const void* k_cache, const
                             void* stream);
 
 /*
+ * pa_append_and_decode -- one decode step in one launch: each sequence's
+ * new token is written into the cache and attention is computed over the
+ * whole context, new token included.
+ *
+ * A decode step first appends the new token's K/V to the sequence's last
+ * block and then attends over every valid slot ("Efficient Memory
+ * Management for LLM Serving with PagedAttention -- in-depth reading",
+ * section 3.4, steps 1 and 3; "vLLM PagedAttention source walk-through",
+ * section 3.2, append_token: block table[pos / block_size], offset
+ * pos % block_size).  This call does both for one new token per sequence at
+ * position pos = context_lens[s] - 1, so the result, pools included, is the
+ * one of
+ *
+ *   pa_reshape_and_cache (or pa_reshape_and_cache_fp8) with
+ *       slot_mapping[s] = block_tables[s][pos / block_size] * block_size
+ *                         + pos % block_size,
+ *   then pa_decode (or pa_decode_fp8).
+ *
+ * The decode's CTA that reads position pos writes the row into the pools
+ * and uses it directly, so no separate cache-write launch precedes the
+ * decode.
+ *
+ *   key, value     [num_seqs][num_kv_heads][head_dim] of dtype, the new
+ *                  token of each sequence (read only)
+ *   k_cache,
+ *   v_cache        the pools; the new tokens' slots are written
+ *   dtype, kv_dtype, k_scale, v_scale
+ *                  as pa_decode_prefix_splitk: 16-bit pools of the query
+ *                  type, or E4M3 pools with PA_FP16 queries and new tokens;
+ *                  an E4M3 pool stores the code nearest to the float32
+ *                  quotient key / k_scale (value / v_scale), as
+ *                  pa_reshape_and_cache_fp8 does
+ *
+ * Precondition: the slot written for sequence s is read by no other
+ * sequence of the call (copy-on-write has given a shared block its own copy
+ * before a sequence appends to it: "Unveiling the NVIDIA driver stack",
+ * section 4; pa_copy_blocks).  Otherwise that other sequence may see the old
+ * or the new row.
+ *
+ * Other arguments as pa_decode.  Device-value outcomes as pa_decode; a
+ * sequence with context_lens[s] <= 0, a context length past the table's
+ * capacity, or an out-of-pool block id at position pos writes nothing into
+ * the pools.
+ */
+int pa_append_and_decode(void* out, const void* q, const void* key, const void* value, void* k_cache,
+                         void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, float scale, int dtype, int kv_dtype,
+                         float k_scale, float v_scale, void* stream);
+
+/*
+ * pa_append_and_decode_splitk -- pa_append_and_decode with the split-K
+ * decode: the new tokens' cache write, then the partitions of
+ * pa_decode_splitk, in one launch.  The partition covering position
+ * context_lens[s] - 1 writes the row.  Follow with pa_splitk_reduce (same
+ * partition_size, max_num_partitions, workspace) on the same stream.
+ *
+ * Arguments as pa_append_and_decode plus the split-K arguments of
+ * pa_decode_splitk; outcomes and precondition as pa_append_and_decode.
+ */
+int pa_append_and_decode_splitk(void* out, const void* q, const void* key, const void* value, void* k_cache,
+                                void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                int head_dim, int block_size, int num_blocks, float scale, int dtype,
+                                int kv_dtype, float k_scale, float v_scale, int partition_size,
+                                int max_num_partitions, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pa_prefill -- paged attention for prompt tokens: whole prompts, or chunks
  * of them appended to a cached context (chunked prefill).
  *
@@ -345,7 +416,12 @@ int pa_splitk_reduce(void* out, const void* workspace, size_t workspace_bytes,
  *    message; nothing is launched.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and remembers it;
- *    make that first call before any stream capture.
+ *    make that first call before any stream capture.  The address is
+ *    remembered for the life of the process: after cudaDeviceReset (or
+ *    anything else that destroys the device's primary context) it no longer
+ *    names the array, so do not call this entry point on that device again.
+ *  - Arguments are checked as for pa_decode_splitk first; a valid batch that
+ *    is too large for the array is then rejected as below.
  *  - Every call on a device shares the one array and leaves its partials
  *    there.  Nothing in it needs to start at zero: each call writes every
  *    row it later reads.  Calls whose kernels overlap on the GPU (different

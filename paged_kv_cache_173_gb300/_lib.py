@@ -42,6 +42,10 @@ SIGNATURES = {
                                   _I, _P, _SZ, _P]),
     "pa_decode_prefix_splitk": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _F, _F,
                                      _I, _P, _I, _I, _P, _SZ, _P]),
+    "pa_append_and_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _F, _F,
+                                  _P]),
+    "pa_append_and_decode_splitk": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _F,
+                                         _F, _I, _I, _P, _SZ, _P]),
     "pa_prefill": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "pa_selftest_wait": (_I, [_P, ctypes.c_uint, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),

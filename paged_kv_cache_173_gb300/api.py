@@ -259,6 +259,49 @@ def pa_decode_prefix_splitk(out: torch.Tensor, q: torch.Tensor, k_cache: torch.T
     _lib.check("pa_decode_prefix_splitk", st)
 
 
+def _append_common(out, q, key, value, k_cache, v_cache, block_tables, context_lens):
+    codes = k_cache.dtype in _CODE_DTYPES
+    dev, S, H, d, N, B, Hk, M, ptrs, pcl = _decode_common(out, q, k_cache, v_cache, block_tables, context_lens,
+                                                          codes=codes)
+    if key.shape != (S, Hk, d) or value.shape != (S, Hk, d):
+        raise ValueError("key/value must be [S, Hk, d]: one new token per sequence")
+    pkey, pval = _need(key, "key", q.dtype, dev), _need(value, "value", q.dtype, dev)
+    dt = _dtype_code(q)
+    return dev, S, H, d, N, B, Hk, M, ptrs, pcl, pkey, pval, dt, (PA_FP8_E4M3 if codes else dt)
+
+
+def pa_append_and_decode(out: torch.Tensor, q: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                         k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                         context_lens: torch.Tensor, scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
+                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """One decode step in one launch: key/value [S, Hk, d] (one new token per sequence) go
+    into the pools at position context_lens[s] - 1, then out = pa_decode over the whole
+    context.  E4M3 pools (uint8 / float8_e4m3fn) take k_scale and v_scale."""
+    dev, S, H, d, N, B, Hk, M, (po, pq, pk, pv, pbt), pcl, pkey, pval, dt, kv = _append_common(
+        out, q, key, value, k_cache, v_cache, block_tables, context_lens)
+    st = _lib.lib().pa_append_and_decode(po, pq, pkey, pval, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N, float(scale),
+                                         dt, kv, float(k_scale), float(v_scale), _stream_ptr(q, stream))
+    _lib.check("pa_append_and_decode", st)
+
+
+def pa_append_and_decode_splitk(out: torch.Tensor, q: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                                k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                context_lens: torch.Tensor, scale: float, partition_size: int,
+                                workspace: torch.Tensor, max_num_partitions: Optional[int] = None,
+                                k_scale: float = 1.0, v_scale: float = 1.0,
+                                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """pa_append_and_decode with the split-K partitions; follow with pa_splitk_reduce."""
+    dev, S, H, d, N, B, Hk, M, (po, pq, pk, pv, pbt), pcl, pkey, pval, dt, kv = _append_common(
+        out, q, key, value, k_cache, v_cache, block_tables, context_lens)
+    P = max_num_partitions or max_num_partitions_for(M, B, partition_size)
+    ws = _need(workspace, "workspace", workspace.dtype, dev)
+    st = _lib.lib().pa_append_and_decode_splitk(
+        po, pq, pkey, pval, pk, pv, pbt, M, pcl, S, H, Hk, d, B, N, float(scale), dt, kv, float(k_scale),
+        float(v_scale), int(partition_size), int(P), ws, workspace.numel() * workspace.element_size(),
+        _stream_ptr(q, stream))
+    _lib.check("pa_append_and_decode_splitk", st)
+
+
 def pa_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                block_tables: torch.Tensor, context_lens: torch.Tensor, query_start_loc: torch.Tensor,
                max_query_len: int, scale: float, stream: Optional[torch.cuda.Stream] = None) -> None:

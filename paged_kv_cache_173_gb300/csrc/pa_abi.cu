@@ -203,6 +203,60 @@ int splitk_impl(void* out, const void* q, const void* k_cache, const void* v_cac
   return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)), "split-K decode launch");
 }
 
+// The new-token arguments and cache types of the append entry points.
+int check_append(const void* key, const void* value, int num_seqs, int dtype, int kv_dtype, float k_scale,
+                 float v_scale) {
+  if (kv_dtype == PA_FP8_E4M3) {
+    const int st = check_fp8_decode(dtype, k_scale, v_scale);
+    if (st != PA_OK) return st;
+  } else if (kv_dtype != dtype) {
+    return fail(PA_ERR_UNSUPPORTED, "kv_dtype %d must equal dtype %d or be PA_FP8_E4M3", kv_dtype, dtype);
+  }
+  if (num_seqs == 0) return PA_OK;
+  if (!key || !value) return fail(PA_ERR_INVALID_ARG, "key and value must not be NULL");
+  if (!aligned(key, 16) || !aligned(value, 16))
+    return fail(PA_ERR_INVALID_ARG, "key and value must be 16-byte aligned");
+  return PA_OK;
+}
+
+// pa_append_and_decode / pa_append_and_decode_splitk: the decode arguments
+// with the new tokens' rows; workspace == NULL selects the single pass.
+int append_impl(void* out, const void* q, const void* key, const void* value, void* k_cache, void* v_cache,
+                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                int dtype, int kv_dtype, float k_scale, float v_scale, bool splitk, int partition_size,
+                int max_num_partitions, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_append(key, value, num_seqs, dtype, kv_dtype, k_scale, v_scale);
+  if (st != PA_OK) return st;
+  st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                    num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype);
+  if (st != PA_OK) return st;
+  if (splitk) {
+    st = check_splitk(max_blocks_per_seq, block_size, partition_size, max_num_partitions, workspace,
+                      workspace_bytes, num_seqs, num_heads, head_dim);
+    if (st != PA_OK) return st;
+  }
+  if (num_seqs == 0) return ok();
+  const bool fp8 = kv_dtype == PA_FP8_E4M3;
+  pa::DecodeArgs a = decode_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                 num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                 dtype, kv_dtype, fp8 ? k_scale : 1.f, fp8 ? v_scale : 1.f);
+  a.new_key = key;
+  a.new_value = value;
+  if (splitk) {
+    a.ws = static_cast<float*>(workspace);
+    a.partition_size = partition_size;
+    a.max_num_partitions = max_num_partitions;
+    a.cluster_size = 0;
+  } else {
+    a.cluster_size = -1;
+    a.partition_size = max_blocks_per_seq * block_size;
+    a.max_num_partitions = 1;
+  }
+  return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)),
+                     splitk ? "append + split-K decode launch" : "append + decode launch");
+}
+
 // The checks shared by both cache writes.
 int check_reshape(const void* key, const void* value, const void* k_cache, const void* v_cache,
                   const int64_t* slot_mapping, int num_tokens, int num_blocks, int block_size,
@@ -230,6 +284,19 @@ int check_reshape(const void* key, const void* value, const void* k_cache, const
 }  // namespace
 
 namespace pa {
+
+int check_splitk_decode_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                             int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                             int num_blocks, float scale, int dtype, int partition_size) {
+  const int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                              num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype);
+  if (st != PA_OK) return st;
+  if (partition_size <= 0 || partition_size % block_size != 0)
+    return fail(PA_ERR_INVALID_ARG, "partition_size %d must be a positive multiple of block_size %d",
+                partition_size, block_size);
+  return PA_OK;
+}
 
 int set_last_error(int status, const char* fmt, ...) {
   va_list ap;
@@ -408,6 +475,28 @@ int pa_decode_prefix_splitk(void* out, const void* q, const void* k_cache, const
   a.seqs_per_group = seqs_per_group;
   return cuda_status(pa::launch_decode_prefix(a, static_cast<cudaStream_t>(stream)),
                      "shared-prefix decode launch");
+}
+
+int pa_append_and_decode(void* out, const void* q, const void* key, const void* value, void* k_cache,
+                         void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, float scale, int dtype, int kv_dtype,
+                         float k_scale, float v_scale, void* stream) {
+  return append_impl(out, q, key, value, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                     num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, kv_dtype,
+                     k_scale, v_scale, false, 0, 1, nullptr, 0, stream);
+}
+
+int pa_append_and_decode_splitk(void* out, const void* q, const void* key, const void* value, void* k_cache,
+                                void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                int head_dim, int block_size, int num_blocks, float scale, int dtype,
+                                int kv_dtype, float k_scale, float v_scale, int partition_size,
+                                int max_num_partitions, void* workspace, size_t workspace_bytes, void* stream) {
+  return append_impl(out, q, key, value, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                     num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, kv_dtype,
+                     k_scale, v_scale, true, partition_size, max_num_partitions, workspace, workspace_bytes,
+                     stream);
 }
 
 int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -82,6 +82,16 @@ struct DecodeParams {
   int members_per_cta;  // shared pass: sequences of a group per CTA
   int subgroups;        // shared pass: CTAs per group along grid z
   int num_seqs;
+  // Append (the cache write fused into the decode): sequence s's new token,
+  // rows new_k / new_v [S][Hk][d] of T, goes into the pools k_pool / v_pool
+  // at the slot of position ctx - 1; E4M3 pools store the code nearest to
+  // x / k_scale (x / v_scale).
+  const void* new_k;
+  const void* new_v;
+  void* k_pool;
+  void* v_pool;
+  float k_scale;
+  float v_scale;
 };
 
 enum DecodeMode { MODE_GRID = 0, MODE_CLUSTER = 1, MODE_SHARED = 2 };
@@ -525,6 +535,89 @@ __device__ __forceinline__ void attend_pair_e4m3(WarpAcc<HEAD_DIM, NT>& acc,
   }
 }
 
+// ------------------------------------------------------- the fused append
+// A sequence's new K and V rows for one KV head, as the 16-byte units (8
+// elements of T) that the lanes of one warp hold: unit x < U of the K row,
+// then the V row; lane i holds units i, i + 32, ...
+template <int HEAD_DIM>
+struct AppendRow {
+  static constexpr int U = HEAD_DIM / 8;        // units per row
+  static constexpr int NV = (2 * U + 31) / 32;  // units per lane
+  uint4 v[NV];
+};
+
+template <int HEAD_DIM>
+__device__ __forceinline__ void append_load(AppendRow<HEAD_DIM>& a, const DecodeParams& p, int s, int kvh,
+                                            int lane) {
+  constexpr int U = AppendRow<HEAD_DIM>::U;
+  const size_t row = (static_cast<size_t>(s) * p.num_kv_heads + kvh) * U;
+  const uint4* k = static_cast<const uint4*>(p.new_k) + row;
+  const uint4* v = static_cast<const uint4*>(p.new_v) + row;
+#pragma unroll
+  for (int j = 0; j < AppendRow<HEAD_DIM>::NV; ++j) {
+    const int x = lane + 32 * j;
+    if (x < 2 * U) a.v[j] = __ldg((x < U ? k : v) + (x % U));
+  }
+}
+
+// Write the rows into the pools at pool row `prow` (block * B + offset) and
+// into the landed shared-memory chunk at `cbase` (K boxes, V boxes at
+// + half_bytes), token row r, where TMA put what the pool held before the
+// write.  16-bit pools take the bits; E4M3 pools take, per element, the code
+// nearest to the float32 quotient x / scale (the conversion the E4M3 cache
+// write uses), so both hold what a separate cache write would leave.
+template <typename KV, int HEAD_DIM, int ROW_BYTES, int BOX_B, int HALF_BYTES>
+__device__ __forceinline__ void append_store(const AppendRow<HEAD_DIM>& a, const DecodeParams& p, int64_t prow,
+                                             int kvh, uint32_t cbase, uint32_t r, int lane) {
+  constexpr int U = AppendRow<HEAD_DIM>::U;
+  constexpr int UPB = ROW_BYTES / 16;  // 16-byte units per box row
+#pragma unroll
+  for (int j = 0; j < AppendRow<HEAD_DIM>::NV; ++j) {
+    const int x = lane + 32 * j;
+    if (x >= 2 * U) continue;
+    const int which = x >= U ? 1 : 0;  // 0: K, 1: V
+    const int u = x % U;
+    const int64_t grow = prow * p.num_kv_heads + kvh;  // the (slot, head) row of the pool
+    if constexpr (!kIsFp8<KV>) {
+      uint4* g = static_cast<uint4*>(which ? p.v_pool : p.k_pool) + grow * U + u;
+      *g = a.v[j];
+      const uint32_t sa = cbase + which * HALF_BYTES + (u / UPB) * BOX_B + swizzled<ROW_BYTES>(r, u % UPB);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sa), "r"(a.v[j].x), "r"(a.v[j].y),
+                   "r"(a.v[j].z), "r"(a.v[j].w)
+                   : "memory");
+    } else {
+      const float sc = which ? p.v_scale : p.k_scale;
+      const uint32_t w[4] = {a.v[j].x, a.v[j].y, a.v[j].z, a.v[j].w};
+      uint32_t o[2] = {0u, 0u};
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float2 f = unpack_half2(w[jj]);
+        const uint32_t c0 = float_to_e4m3_sat(__fdiv_rn(f.x, sc));
+        const uint32_t c1 = float_to_e4m3_sat(__fdiv_rn(f.y, sc));
+        o[jj >> 1] |= (c0 | (c1 << 8)) << ((jj & 1) * 16);
+      }
+      uint2* g = static_cast<uint2*>(which ? p.v_pool : p.k_pool) + grow * U + u;  // 8 codes per unit
+      *g = make_uint2(o[0], o[1]);
+      const int cu = u >> 1;  // the 16-code unit of the row holding these 8 codes
+      const uint32_t sa =
+          cbase + which * HALF_BYTES + (cu / UPB) * BOX_B + swizzled<ROW_BYTES>(r, cu % UPB) + (u & 1) * 8;
+      asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(sa), "r"(o[0]), "r"(o[1]) : "memory");
+    }
+  }
+}
+
+// The fused cache write of one warp's new-token chunk: load the rows, store
+// them into the pools and over row r of the landed chunk at `cbase`.  Kept
+// out of line: it runs once per (sequence, KV head), and inlined into the
+// chunk loop it would raise the register count of the whole kernel.
+template <typename KV, int HEAD_DIM, int ROW_BYTES, int BOX_B, int HALF_BYTES>
+__device__ __noinline__ void append_chunk_row(const DecodeParams& p, int s, int kvh, int64_t prow, uint32_t cbase,
+                                              uint32_t r, int lane) {
+  AppendRow<HEAD_DIM> nv;
+  append_load<HEAD_DIM>(nv, p, s, kvh, lane);
+  append_store<KV, HEAD_DIM, ROW_BYTES, BOX_B, HALF_BYTES>(nv, p, prow, kvh, cbase, r, lane);
+}
+
 // Sum the per-lane partial running sums over the 8 row groups of the warp.
 template <int HEAD_DIM, int NT>
 __device__ __forceinline__ void reduce_warp_sums(WarpAcc<HEAD_DIM, NT>& acc) {
@@ -578,11 +671,17 @@ __device__ __forceinline__ void store_warp_state(const WarpAcc<HEAD_DIM, NT>& ac
 //   table row once and scores every member's queries against it, writing
 //   each member's partition row (or `out` for a one-partition sequence).
 // KV: the cache element type, T or E4M3.
-template <typename T, typename KV, int HEAD_DIM, int NT, int WARPS, int STAGES, int MODE>
-__global__ void __launch_bounds__(WARPS * 32)
-paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+// APPEND: the cache write of each sequence's new token is fused in.  The
+//   warp that holds the chunk of position ctx - 1 (one per sequence and KV
+//   head, in the CTA covering the sequence's last chunk) writes the new K/V
+//   row into the pools at that position's slot and over the same row of its
+//   landed stage, then attends as usual: the result is the one of a separate
+//   cache write followed by the decode.  No other CTA reads that slot.
+template <typename T, typename KV, int HEAD_DIM, int NT, int WARPS, int STAGES, int MODE, bool APPEND>
+__device__ __forceinline__ void decode_cta(const DecodeParams& p) {
   constexpr bool CLUSTER = MODE == MODE_CLUSTER;
   constexpr bool SHARED = MODE == MODE_SHARED;
+  static_assert(!(APPEND && SHARED), "the shared pass does not write the cache");
   constexpr bool FP8 = kIsFp8<KV>;
   static_assert(!FP8 || std::is_same<T, __half>::value, "E4M3 caches take float16 queries");
   using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES, kElemBytes<KV>>;
@@ -708,6 +807,17 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int c1 = CLUSTER ? cmax : min(c0 + p.partition_chunks, nchunks);
   const int nk = first < c1 ? (c1 - first + WARPS - 1) / WARPS : 0;  // <= nk_cap
 
+  // Append: the warp-local index of the chunk holding position ctx - 1 (the
+  // sequence's last chunk) if this warp holds it, else -1; its physical block
+  // is taken when the chunk is issued (-1 if outside the pool: nothing is
+  // written and the result is NaN, as after a skipped cache write).
+  int app_k = -1;
+  int app_phys = -1;
+  if constexpr (APPEND) {
+    const int c_last = nchunks - 1;  // nchunks > 0 here
+    if (c_last >= first && c_last < c1 && (c_last - first) % WARPS == 0) app_k = (c_last - first) / WARPS;
+  }
+
   // Shared pass: members whose table entries over this partition differ from
   // the first sequence's get NaN (one bit per member of the CTA).
   int* mismatch = reinterpret_cast<int*>(smem + Cfg::BAR_BYTES - sizeof(int));
@@ -749,7 +859,11 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
         win_nxt = win_load(k + 32);
       }
       int phys = __shfl_sync(FULL_MASK, win_cur, k & 31);
-      if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
+      const bool in_pool = static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
+      if constexpr (APPEND) {
+        if (k == app_k) app_phys = in_pool ? phys : -1;
+      }
+      if (!in_pool) {
         bad = true;  // never read outside the pool; the result becomes NaN
         phys = 0;
       }
@@ -790,6 +904,17 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     const int ch = first + k0 * WARPS;
     const int valid = min(CHUNK, ctx - ch * CHUNK);
     const uint32_t stage = smem_addr(wring + slot * Cfg::STAGE_BYTES);
+    if constexpr (APPEND) {
+      // the stage holding the new token's chunk (the warp's last)
+      if (app_k >= 0 && it == app_k / CPS && app_phys >= 0) {
+        const int pos = ctx - 1;
+        const int64_t prow = static_cast<int64_t>(app_phys) * p.block_size + (pos & (p.block_size - 1));
+        append_chunk_row<KV, HEAD_DIM, Cfg::ROW_BYTES, Cfg::BOX_B, Cfg::HALF_BYTES>(
+            p, s, kvh, prow, stage + (app_k % CPS) * Cfg::CHUNK_BYTES, static_cast<uint32_t>(pos & (CHUNK - 1)),
+            lane);
+        __syncwarp();  // the new row is in shared memory before any lane reads the chunk
+      }
+    }
     if constexpr (FP8) {
       if (CPS == 2 && k0 + 1 < nk) {  // two chunks: the first is full (the second lies further in)
         const int valid2 = min(CHUNK, ctx - (ch + WARPS) * CHUNK);
@@ -911,6 +1036,32 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     cluster.sync();  // no CTA leaves while the others still read its shared memory
   }
   allow_dependent_launch();
+}
+
+template <typename T, typename KV, int HEAD_DIM, int NT, int WARPS, int STAGES, int MODE>
+__global__ void __launch_bounds__(WARPS * 32) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+  decode_cta<T, KV, HEAD_DIM, NT, WARPS, STAGES, MODE, false>(p);
+}
+
+// Resident CTAs per SM that an append kernel is compiled to keep: the count
+// its plain twin reaches (set by the twin's registers, or by shared memory
+// where that binds first), so that the fused write costs no occupancy.
+// Unbounded, the append path would raise the register count past it.
+constexpr int append_min_ctas(int elem, int head_dim, int nt, int warps, int stages) {
+  if (elem == 1) {  // E4M3: 4 warps x 2 stages of 8 KB (4 KB at d = 64)
+    if (head_dim == 64) return nt == 1 ? 6 : 4;
+    return 3;
+  }
+  if (head_dim == 64) return nt == 1 ? 6 : 4;
+  if (head_dim == 128) return (nt == 1 && warps == 4 && stages == 1) ? 5 : 3;
+  return 6;  // d = 256: 2 warps x 1 stage of 16 KB
+}
+
+// The decode with the new tokens' cache write fused in (APPEND above).
+template <typename T, typename KV, int HEAD_DIM, int NT, int WARPS, int STAGES, int MODE>
+__global__ void __launch_bounds__(WARPS * 32, append_min_ctas(kElemBytes<KV>, HEAD_DIM, NT, WARPS, STAGES))
+    paged_append_decode_kernel(const __grid_constant__ DecodeParams p) {
+  decode_cta<T, KV, HEAD_DIM, NT, WARPS, STAGES, MODE, true>(p);
 }
 
 // ================================================================ reduce
@@ -1140,7 +1291,7 @@ constexpr CUtensorMapDataType tma_dtype() {
 // of 16 rows x 1 head x one box row (128 bytes; 64 for 64 one-byte dims),
 // swizzled over the box row's width.
 template <typename KV, int HEAD_DIM>
-cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int num_kv_heads, int64_t rows) {
+cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, int num_kv_heads, int64_t rows) {
   using Cfg = DecodeCfg<HEAD_DIM, 1, 1, 1, kElemBytes<KV>>;
   EncodeTiledFn enc = nullptr;
   cudaError_t e = encode_fn(&enc);
@@ -1157,6 +1308,43 @@ cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int num_kv_heads, 
                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// encode_pool_map through a per-thread cache of recent encodings.  A map is a
+// pure function of (pool address, heads, rows) for a given element type and
+// head size (each instantiation has its own cache), so a hit is always the
+// map that encoding would produce, even for a pool freed and reallocated at
+// the same address.  Decode loops that rotate a few pools skip the encode.
+template <typename KV, int HEAD_DIM>
+cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int num_kv_heads, int64_t rows) {
+  constexpr int kEntries = 16;
+  struct Entry {
+    CUtensorMap map;
+    const void* pool;
+    int64_t rows;
+    int heads;
+  };
+  thread_local Entry cache[kEntries];  // zero-initialised: pool == nullptr marks an empty entry
+  thread_local int next = 0;
+  if (pool != nullptr) {
+    for (int i = 0; i < kEntries; ++i) {
+      const Entry& e = cache[i];
+      if (e.pool == pool && e.rows == rows && e.heads == num_kv_heads) {
+        *map = e.map;
+        return cudaSuccess;
+      }
+    }
+  }
+  const cudaError_t err = encode_pool_map<KV, HEAD_DIM>(map, pool, num_kv_heads, rows);
+  if (err == cudaSuccess && pool != nullptr) {
+    Entry& e = cache[next];
+    e.map = *map;
+    e.pool = pool;
+    e.rows = rows;
+    e.heads = num_kv_heads;
+    next = (next + 1) % kEntries;
+  }
+  return err;
 }
 
 template <typename Kernel>
@@ -1237,6 +1425,12 @@ cudaError_t fill_decode_params(const DecodeArgs& a, DecodeParams* pp) {
   p.members_per_cta = 1;
   p.subgroups = 1;
   p.num_seqs = a.num_seqs;
+  p.new_k = a.new_key;
+  p.new_v = a.new_value;
+  p.k_pool = const_cast<void*>(a.k_cache);  // written only by the append path
+  p.v_pool = const_cast<void*>(a.v_cache);
+  p.k_scale = fp8 ? a.k_scale : 1.f;
+  p.v_scale = fp8 ? a.v_scale : 1.f;
   return cudaSuccess;
 }
 
@@ -1248,14 +1442,20 @@ int members_per_cta(const DecodeArgs& a) {
   return std::max(1, std::min(a.seqs_per_group, 8 * NT / G));
 }
 
-template <typename T, typename KV, int HEAD_DIM, int NT, int MODE, bool PARTS = false>
+template <typename T, typename KV, int HEAD_DIM, int NT, int MODE, bool PARTS = false, bool APPEND = false>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   constexpr bool CLUSTER = MODE == MODE_CLUSTER;
   constexpr int ELEM = kElemBytes<KV>;
   constexpr int WARPS = DecodeShape<HEAD_DIM, ELEM, PARTS>::WARPS;
   constexpr int STAGES = DecodeShape<HEAD_DIM, ELEM, PARTS>::STAGES;
   using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES, ELEM>;
-  auto kern = paged_decode_kernel<T, KV, HEAD_DIM, NT, WARPS, STAGES, MODE>;
+  auto kern = [] {
+    if constexpr (APPEND) {
+      return paged_append_decode_kernel<T, KV, HEAD_DIM, NT, WARPS, STAGES, MODE>;
+    } else {
+      return paged_decode_kernel<T, KV, HEAD_DIM, NT, WARPS, STAGES, MODE>;
+    }
+  }();
   static std::atomic<uint64_t> smem_set{0};
   cudaError_t e = ensure_smem(kern, Cfg::SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return e;
@@ -1329,12 +1529,12 @@ cudaError_t decode_slots(int* slots) {
 // Single-launch decode: one CTA per (sequence, KV head) when those fill the
 // resident slots; otherwise a cluster of up to 8 CTAs per pair, each with at
 // least 512 tokens of capacity.  Split-K (a workspace given): the plain grid.
-template <typename T, typename KV, int HEAD_DIM, int NT>
+template <typename T, typename KV, int HEAD_DIM, int NT, bool APPEND = false>
 cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
   if (a.cluster_size >= 0) {
-    if (a.cluster_size > 0) return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER>(a, stream);
-    return a.ws != nullptr ? launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, true>(a, stream)
-                           : launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID>(a, stream);
+    if (a.cluster_size > 0) return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER, false, APPEND>(a, stream);
+    return a.ws != nullptr ? launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, true, APPEND>(a, stream)
+                           : launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, false, APPEND>(a, stream);
   }
   int slots = 0;
   cudaError_t e = decode_slots<T, KV, HEAD_DIM, NT>(&slots);
@@ -1347,9 +1547,9 @@ cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
   b.cluster_size = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(8, k)));
   if (b.cluster_size == 1) {
     b.cluster_size = 0;
-    return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID>(b, stream);
+    return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, false, APPEND>(b, stream);
   }
-  return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER>(b, stream);
+  return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER, false, APPEND>(b, stream);
 }
 
 template <typename T, int HEAD_DIM>
@@ -1390,18 +1590,28 @@ cudaError_t launch_reduce_t(const ReduceArgs& a, cudaStream_t stream) {
 
 // Entry points used by the per-dtype translation units (KV = T for 16-bit
 // caches, E4M3 for one-byte caches).
-template <typename T, typename KV = T>
-cudaError_t launch_decode_typed(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.num_seqs == 0) return cudaSuccess;
+template <typename T, typename KV, bool APPEND>
+cudaError_t launch_decode_typed_as(const DecodeArgs& a, cudaStream_t stream) {
   const bool two = a.num_heads / a.num_kv_heads > 8;
   switch (a.head_dim) {
     case 64:
-      return two ? launch_decode_auto<T, KV, 64, 2>(a, stream) : launch_decode_auto<T, KV, 64, 1>(a, stream);
+      return two ? launch_decode_auto<T, KV, 64, 2, APPEND>(a, stream)
+                 : launch_decode_auto<T, KV, 64, 1, APPEND>(a, stream);
     case 128:
-      return two ? launch_decode_auto<T, KV, 128, 2>(a, stream) : launch_decode_auto<T, KV, 128, 1>(a, stream);
-    case 256: return two ? cudaErrorInvalidValue : launch_decode_auto<T, KV, 256, 1>(a, stream);
+      return two ? launch_decode_auto<T, KV, 128, 2, APPEND>(a, stream)
+                 : launch_decode_auto<T, KV, 128, 1, APPEND>(a, stream);
+    case 256: return two ? cudaErrorInvalidValue : launch_decode_auto<T, KV, 256, 1, APPEND>(a, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// The append variant (the new tokens' cache write fused in) when the
+// arguments carry new K/V rows.
+template <typename T, typename KV = T>
+cudaError_t launch_decode_typed(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  return a.new_key != nullptr ? launch_decode_typed_as<T, KV, true>(a, stream)
+                              : launch_decode_typed_as<T, KV, false>(a, stream);
 }
 
 // Shared-prefix split-K: the shared pass (query tiles of NTS x 8 rows: the

@@ -60,6 +60,10 @@ struct DecodeArgs {
                            // 0: plain grid; < 0: chosen from occupancy
   const int32_t* prefix_lens;  // shared-prefix split-K: [ceil(num_seqs / seqs_per_group)], else null
   int seqs_per_group;
+  // Append: one new token per sequence, [S][Hk][d] of `dtype`, written into
+  // the pools at the slot of position ctx - 1 by the decode itself (null: none).
+  const void* new_key;
+  const void* new_value;
 };
 
 struct ReduceArgs {
@@ -99,6 +103,14 @@ struct PrefillArgs {
 
 // Record a formatted message as the calling thread's last error; returns status.
 int set_last_error(int status, const char* fmt, ...);
+
+// The host checks of a split-K decode call except those of its workspace
+// (shapes, types, pointers, partition_size a positive multiple of
+// block_size); PA_OK or the status and last-error text of the first failure.
+int check_splitk_decode_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                             int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                             int num_blocks, float scale, int dtype, int partition_size);
 
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);

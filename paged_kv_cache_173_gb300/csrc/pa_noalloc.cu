@@ -56,12 +56,15 @@ extern "C" int pa_decode_splitk_static(void* out, const void* q, const void* k_c
                                        int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                        int block_size, int num_blocks, float scale, int dtype,
                                        int partition_size, void* stream) {
-  int max_num_partitions = 1;
-  if (partition_size > 0 && block_size > 0 && max_blocks_per_seq > 0) {
-    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
-    const int64_t parts = (cap + partition_size - 1) / partition_size;
-    max_num_partitions = parts > INT32_MAX ? INT32_MAX : static_cast<int>(parts);
-  }
+  // the arguments first, so that an invalid call is reported as such and not
+  // as a batch too large for the scratch
+  const int chk = pa::check_splitk_decode_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                               context_lens, num_seqs, num_heads, num_kv_heads, head_dim,
+                                               block_size, num_blocks, scale, dtype, partition_size);
+  if (chk != PA_OK) return chk;
+  const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+  const int64_t parts = (cap + partition_size - 1) / partition_size;
+  const int max_num_partitions = parts > INT32_MAX ? INT32_MAX : static_cast<int>(parts);
   const size_t need = pa_splitk_workspace_bytes(num_seqs, num_heads, head_dim, max_num_partitions);
   if (need > PA_STATIC_SCRATCH_BYTES)
     return pa::set_last_error(PA_ERR_UNSUPPORTED,

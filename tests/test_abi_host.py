@@ -197,3 +197,40 @@ def test_prefill_checks_arguments(L, kw, status):
 @pytest.mark.parametrize("args", [(None, 1000), (A, 0), (A, 10_000_001), (A + 2, 1000)])
 def test_wait_selftest_checks_arguments(L, args):
     assert L.pa_selftest_wait(args[0], args[1], None) == _lib.PA_ERR_INVALID_ARG
+
+
+def _append(L, splitk=False, **kw):
+    args = dict(out=A, q=A, key=A, value=A, k=A, v=A, S=2, H=8, Hk=2, d=128, dtype=0, kv=0, ks=1.0, vs=1.0,
+                ps=64, P=2, ws=A, wsb=10 ** 9)
+    args.update(kw)
+    head = (args["out"], args["q"], args["key"], args["value"], args["k"], args["v"], A, 8, A, args["S"],
+            args["H"], args["Hk"], args["d"], 16, 32, 0.1, args["dtype"], args["kv"], args["ks"], args["vs"])
+    if splitk:
+        return L.pa_append_and_decode_splitk(*head, args["ps"], args["P"], args["ws"], args["wsb"], None)
+    return L.pa_append_and_decode(*head, None)
+
+
+@pytest.mark.parametrize("splitk", [False, True])
+@pytest.mark.parametrize("kw,status", [
+    (dict(key=None), _lib.PA_ERR_INVALID_ARG),
+    (dict(value=A + 8), _lib.PA_ERR_INVALID_ARG),
+    (dict(kv=1), _lib.PA_ERR_UNSUPPORTED),                 # 16-bit pools of another type than q
+    (dict(dtype=1, kv=2), _lib.PA_ERR_UNSUPPORTED),        # E4M3 pools take fp16 queries
+    (dict(kv=2, ks=0.0), _lib.PA_ERR_INVALID_ARG),
+    (dict(kv=2, vs=float("nan")), _lib.PA_ERR_INVALID_ARG),
+    (dict(d=96), _lib.PA_ERR_UNSUPPORTED),
+    (dict(k=None), _lib.PA_ERR_INVALID_ARG),
+])
+def test_append_rejects_bad_arguments(L, splitk, kw, status):
+    assert _append(L, splitk, **kw) == status
+    assert _lib.last_error() != ""
+
+
+@pytest.mark.parametrize("kw", [dict(ps=40), dict(P=1), dict(ws=None), dict(wsb=100)])
+def test_append_splitk_rejects_bad_workspace(L, kw):
+    assert _append(L, True, **kw) == _lib.PA_ERR_INVALID_ARG
+
+
+def test_append_empty_batch_is_a_no_op(L):
+    assert _append(L, S=0, key=None, value=None, q=None, out=None) == _lib.PA_OK
+    assert _append(L, True, S=0, key=None, value=None, ws=None) == _lib.PA_OK

@@ -110,6 +110,20 @@ def kv_ops(api, b):
                                                                            ps, ws, P))
 
 
+def append_ops(api, b):
+    """The fused cache write + decode calls (single pass, split-K) for the batch's cache type."""
+    ks, vs = b.k_scale, b.v_scale
+    return (lambda out, q, key, value, kc, vc, bt, cl: api.pa_append_and_decode(
+                out, q, key, value, kc, vc, bt, cl, b.scale, k_scale=ks, v_scale=vs),
+            lambda out, q, key, value, kc, vc, bt, cl, ps, ws, P: api.pa_append_and_decode_splitk(
+                out, q, key, value, kc, vc, bt, cl, b.scale, ps, ws, P, k_scale=ks, v_scale=vs))
+
+
+def decode_index(kernels) -> int:
+    """Position of the decode launch in a path's kernel list."""
+    return next(i for i, (n, _) in enumerate(kernels) if "decode" in n)
+
+
 def to_device(a: np.ndarray, dtype: str, dev):
     """A workload array on the device; bfloat16 bit patterns become bf16 tensors."""
     import torch
@@ -366,10 +380,11 @@ def other_bytes(b, path: str) -> dict:
         "out": S * H * d * qe,
         "block_tables": int(np.sum((ctx + B - 1) // B)) * 4,
         "context_lens": S * 4,
-        "new_tokens": T * b.num_kv_heads * d * (2 * qe + 2 * kve) + T * 8,
+        # read from the inputs and written into the pools; separate writes also read the slot ids
+        "new_tokens": T * b.num_kv_heads * d * (2 * qe + 2 * kve) + (0 if path.startswith("append") else T * 8),
         "splitk_partials": 0,
     }
-    if path in ("splitk", "prefix"):
+    if path in ("splitk", "prefix", "append_splitk"):
         nparts = (ctx + b.partition_size - 1) // b.partition_size
         rows = int(np.sum(np.where(nparts > 1, nparts, 0))) * H
         r["splitk_partials"] = 2 * rows * (d + 2) * 4
@@ -422,10 +437,23 @@ def measure_workload(args, name: str, dev, world: int, dist_g, host_pools: bool 
     def reduce(r):
         api.pa_splitk_reduce(out, ws, cl, M, B, ps, P)
 
+    append_kv, append_splitk_kv = append_ops(api, b)
+
+    def append(r):
+        kc, vc, q = reps[r % R]
+        append_kv(out, q, key, value, kc, vc, bt, cl)
+
+    def append_splitk(r):
+        kc, vc, q = reps[r % R]
+        append_splitk_kv(out, q, key, value, kc, vc, bt, cl, ps, ws, P)
+
     paths = {
         "decode": [("reshape_and_cache", reshape), ("paged_decode", decode)],
         "splitk": [("reshape_and_cache", reshape), ("paged_decode_splitk", decode_splitk),
                    ("splitk_reduce", reduce)],
+        # the cache write fused into the decode launch
+        "append": [("append_and_decode", append)],
+        "append_splitk": [("append_and_decode_splitk", append_splitk), ("splitk_reduce", reduce)],
     }
     if b.prefix_lens is not None:  # sequences share prompt blocks in consecutive groups
         plens = t(b.prefix_lens)
@@ -463,7 +491,9 @@ def summarize(m, world: int, K: int, peak: float) -> dict:
     out = {}
     for pname, v in m["results"].items():
         roof = workloads.unique_kv_bytes(b) if pname == "prefix" else kv_bytes
-        t_dec = float(v["per"][1])
+        t_dec = float(v["per"][decode_index(m["paths"][pname])])
+        if len(m["paths"][pname]) == 1:  # one launch per step: the timed region's average
+            t_dec = v["ms"] / K
         val = whole_job_gbs(kv_bytes, K, world, v["ms"])
         out[pname] = {
             "ms_per_step": round(v["ms"] / K, 5),
@@ -490,8 +520,9 @@ def run_gpu(args, rank: int, world: int):
     b, kv_bytes, best = m["b"], m["kv_bytes"], m["best"]
     r0 = m["results"][best]
     kern = m["paths"][best]
-    decode_name = kern[1][0]
-    t_decode = float(r0["per"][1])
+    di = decode_index(kern)
+    decode_name = kern[di][0]
+    t_decode = float(r0["per"][di])
 
     e2e = run_e2e(args, b, dev, m["reps"], m["ws"], m["P"], kv_bytes, m["stream"], best)
 
@@ -501,7 +532,12 @@ def run_gpu(args, rank: int, world: int):
     # the shared-prefix path reads each shared block once: its algorithmic
     # bytes are the unique bytes
     roof_bytes = workloads.unique_kv_bytes(b) if best == "prefix" else kv_bytes
-    achieved = roof_bytes / (t_decode * 1e-3) / 1e9
+    # The decode launch's average duration: on a one-kernel step the timed
+    # region holds K launches of it and nothing else, so it is the region's
+    # time over K; otherwise its time in the separate event pass.
+    one_kernel = len(kern) == 1
+    t_roof = step_ms if one_kernel else t_decode
+    achieved = roof_bytes / (t_roof * 1e-3) / 1e9
     traffic = load_traffic(workload_key(args), decode_name)
     ob = other_bytes(b, best)
     res = {
@@ -524,7 +560,7 @@ def run_gpu(args, rank: int, world: int):
             "path": best,
             "path_chosen_on": "the plain timed steps of each path",
             "step": " -> ".join(n for n, _ in kern),
-            "partition_size": b.partition_size if best in ("splitk", "prefix") else None,
+            "partition_size": b.partition_size if best in ("splitk", "prefix", "append_splitk") else None,
             "roofline_bytes": ("unique KV bytes (each shared block once)" if best == "prefix"
                                else "algorithmic KV bytes"),
             "l2": (f"{m['R']} rotating pool replicas ({m['R'] * m['pool_bytes'] / 1e9:.2f} GB) > 129 MB L2; "
@@ -551,6 +587,10 @@ def run_gpu(args, rank: int, world: int):
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
             "peak_kind": f"{peak_kind} (copy GB/s)",
+            "duration_ms": round(t_roof, 5),
+            "duration_from": ("the timed region: K launches, one per step, nothing else" if one_kernel
+                              else "the separate event pass (launches kept from overlapping)"),
+            "isolated_frac": round(roof_bytes / (t_decode * 1e-3) / 1e9 / peak, 4),
         },
         "gpu_launches": (len(kern) + (1 if best == "prefix" else 0)) * K,
         "e2e": e2e,
@@ -572,7 +612,7 @@ def run_gpu(args, rank: int, world: int):
             per_path = summarize(mc, world, K, peak)
             bp = mc["best"]
             entry = {"workload": mc["desc"], "kv_bytes_per_step": mc["kv_bytes"], "path": bp,
-                     "partition_size": mc["b"].partition_size if bp in ("splitk", "prefix") else None,
+                     "partition_size": mc["b"].partition_size if bp in ("splitk", "prefix", "append_splitk") else None,
                      "values": "pools drawn on the device (torch generator, N(0,1))",
                      "clocks": mc["results"][bp]["clocks"], **per_path[bp],
                      "tokens_per_s": round(mc["b"].num_seqs * world / (mc["results"][bp]["ms"] / K * 1e-3), 1),
@@ -612,55 +652,141 @@ class StagedInputs:
 
 
 def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, path):
-    """Same step through the public API with pinned host inputs and output."""
+    """The same step through the public API with pinned host inputs and output,
+    pipelined the way a serving loop runs it: step i + 1's inputs go to the
+    device on one copy stream while step i computes, and step i's output comes
+    back on another.  Inputs and outputs are double-buffered; a step's
+    kernels wait for its inputs, and a buffer is refilled only after the step
+    that used it is done (and, for the output, read back).  Every step copies
+    all of its inputs in (one pinned buffer, one copy) and its output out.
+    The timed region runs from before the first input copy to after the last
+    output copy."""
     import torch
     from paged_kv_cache_173_gb300 import api
 
-    host = {k: to_device(getattr(b, k), b.dtype, "cpu")
-            for k in ("q", "key", "value", "slot_mapping", "block_tables", "context_lens")}
+    names = ["q", "key", "value", "block_tables", "context_lens"]
+    if not path.startswith("append"):
+        names.append("slot_mapping")
+    host = {k: to_device(getattr(b, k), b.dtype, "cpu") for k in names}
     if path == "prefix":
         host["prefix_lens"] = torch.from_numpy(b.prefix_lens)
-    staged = StagedInputs(host, dev)
-    devb = staged.dev
-    out = torch.empty_like(devb["q"])
-    out_h = torch.empty_like(host["q"]).pin_memory()
-    h2d = staged.nbytes
-    d2h = out_h.numel() * out_h.element_size()
+    staged = [StagedInputs(host, dev) for _ in range(2)]
+    outs = [torch.empty_like(staged[0].dev["q"]) for _ in range(2)]
+    outs_h = [torch.empty_like(host["q"]).pin_memory() for _ in range(2)]
+    h2d = staged[0].nbytes
+    d2h = outs_h[0].numel() * outs_h[0].element_size()
     M, B, ps, R = b.max_blocks_per_seq, b.block_size, b.partition_size, len(reps)
     write_kv, decode_kv, splitk_kv = kv_ops(api, b)
+    append_kv, append_splitk_kv = append_ops(api, b)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    inputs_ready = [ev(), ev()]
+    computed = [ev(), ev()]
+    read_back = [ev(), ev()]
 
-    def step(i):
+    def kernels(i, devb, out):
         kc, vc, _ = reps[i % R]
-        staged.send()  # every input of the step, one copy
+        q, bt, cl = devb["q"], devb["block_tables"], devb["context_lens"]
+        if path == "append":
+            append_kv(out, q, devb["key"], devb["value"], kc, vc, bt, cl)
+            return
+        if path == "append_splitk":
+            append_splitk_kv(out, q, devb["key"], devb["value"], kc, vc, bt, cl, ps, ws, P)
+            api.pa_splitk_reduce(out, ws, cl, M, B, ps, P)
+            return
         write_kv(devb["key"], devb["value"], kc, vc, devb["slot_mapping"])
         if path == "decode":
-            decode_kv(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"])
+            decode_kv(out, q, kc, vc, bt, cl)
         elif path == "prefix":
-            api.pa_decode_prefix_splitk(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"], b.scale,
-                                        b.seqs_per_group, devb["prefix_lens"], ps, ws, P, k_scale=b.k_scale,
-                                        v_scale=b.v_scale)
-            api.pa_splitk_reduce(out, ws, devb["context_lens"], M, B, ps, P)
+            api.pa_decode_prefix_splitk(out, q, kc, vc, bt, cl, b.scale, b.seqs_per_group, devb["prefix_lens"], ps,
+                                        ws, P, k_scale=b.k_scale, v_scale=b.v_scale)
+            api.pa_splitk_reduce(out, ws, cl, M, B, ps, P)
         else:
-            splitk_kv(out, devb["q"], kc, vc, devb["block_tables"], devb["context_lens"], ps, ws, P)
-            api.pa_splitk_reduce(out, ws, devb["context_lens"], M, B, ps, P)
-        out_h.copy_(out, non_blocking=True)
+            splitk_kv(out, q, kc, vc, bt, cl, ps, ws, P)
+            api.pa_splitk_reduce(out, ws, cl, M, B, ps, P)
+
+    def send(i, first=None):
+        j = i % 2
+        with torch.cuda.stream(up):
+            if first is not None:
+                up.wait_event(first)
+            if i >= 2:
+                up.wait_event(computed[j])  # step i - 2 is done with these inputs
+            staged[j].send()
+            inputs_ready[j].record(up)
+
+    def run(n, e_start=None):
+        send(0, e_start)
+        for i in range(n):
+            j = i % 2
+            if i + 1 < n:
+                send(i + 1)
+            stream.wait_event(inputs_ready[j])
+            if i >= 2:
+                stream.wait_event(read_back[j])  # step i - 2's output has been read back
+            with torch.cuda.stream(stream):
+                kernels(i, staged[j].dev, outs[j])
+                computed[j].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[j])
+                outs_h[j].copy_(outs[j], non_blocking=True)
+                read_back[j].record(down)
+        stream.wait_event(read_back[(n - 1) % 2])
+        if n >= 2:
+            stream.wait_event(read_back[(n - 2) % 2])
 
     n = max(3, min(args.steps, args.e2e_steps))
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            step(i)
-        torch.cuda.synchronize(dev)
+    run(3)  # warm-up
+    torch.cuda.synchronize(dev)
+
+    def timed(fn):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(n):
-            step(i)
-        e1.record()
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
-    return {"value": round(kv_bytes * n / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
-            "ms_per_step": round(ms / n, 5)}
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            e0.record()
+        t0 = time.perf_counter()
+        steps = fn(e0)
+        host_s = time.perf_counter() - t0
+        with torch.cuda.stream(stream):
+            e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1), steps, host_s
+
+    # eager: the host enqueues every call and copy of every step
+    ms_e, n_e, host_s = timed(lambda e0: (run(n, e0), n)[1])
+    eager = {"value": round(kv_bytes * n_e / (ms_e * 1e-3) / 1e9, 1), "ms_per_step": round(ms_e / n_e, 5),
+             "steps": n_e, "host_enqueue_us_per_step": round(host_s / n_e * 1e6, 2)}
+    res = {"unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+           "pipelining": "inputs of step i+1 copied in while step i computes; outputs copied out behind it",
+           "eager": eager}
+    # graph: the same calls and copies of G pipelined steps captured once and replayed, as a
+    # serving loop replays its decode step (G a multiple of the replica and buffer rotations)
+    G = min(n, 8 * R)
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            start = torch.cuda.Event()
+            start.record(stream)
+            run(G, start)
+        with torch.cuda.stream(stream):
+            g.replay()  # the first replay uploads the graph
+        torch.cuda.synchronize(dev)
+
+        def replays(e0):
+            stream.wait_event(e0)
+            with torch.cuda.stream(stream):
+                for _ in range(max(1, n // G)):
+                    g.replay()
+            return max(1, n // G) * G
+
+        ms_g, n_g, _ = timed(replays)
+        res.update({"value": round(kv_bytes * n_g / (ms_g * 1e-3) / 1e9, 1), "ms_per_step": round(ms_g / n_g, 5),
+                    "steps": n_g, "mode": f"CUDA graph of {G} pipelined steps (copies included), replayed"})
+    except Exception as exc:  # no capture: the eager figures are the e2e
+        res.update({"value": eager["value"], "ms_per_step": eager["ms_per_step"], "steps": n_e,
+                    "mode": f"eager (graph capture failed: {type(exc).__name__})"})
+    return res
 
 
 # ------------------------------------------------------------ copy_blocks
@@ -954,10 +1080,13 @@ def parse_args(argv=None):
                         "reshape + pa_prefill on --workload prefill-llama3-8b, chunked-prefill-llama3-8b "
                         "or prefill-long")
     p.add_argument("--copy-pairs", type=int, default=1024)
-    p.add_argument("--path", choices=["auto", "decode", "splitk", "prefix"], default="auto",
-                   help="decode: reshape + pa_decode; splitk: reshape + pa_decode_splitk + reduce; prefix "
-                        "(shared-prefix workload): reshape + pa_decode_prefix_splitk + reduce; auto: time "
-                        "every path the workload has, report the fastest")
+    p.add_argument("--path", choices=["auto", "decode", "splitk", "append", "append_splitk", "prefix"],
+                   default="auto",
+                   help="decode: reshape + pa_decode; splitk: reshape + pa_decode_splitk + reduce; append: "
+                        "pa_append_and_decode (the cache write fused in); append_splitk: "
+                        "pa_append_and_decode_splitk + reduce; prefix (shared-prefix workload): reshape + "
+                        "pa_decode_prefix_splitk + reduce; auto: time every path the workload has, report the "
+                        "fastest")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=2000)
     p.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -610,6 +610,38 @@ def test_fp8_cache_write_and_decode_equal_library_attention_on_dequantised_value
         np.testing.assert_allclose(got[s], ref, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fp8_cache_write_matches_torch_division_and_conversion_on_every_written_row(dtype):
+    # every written row: the code of the float32 quotient x / scale (IEEE division, as
+    # torch divides a float32 tensor by a float32 scalar), by torch's float8 conversion;
+    # the new tokens are drawn as bfloat16 (or float16) and scaled so that every quotient
+    # stays inside the E4M3 range, where torch's conversion rounds and does not saturate
+    b = workloads.build_batch(name="fp8w", seed=33, context_lens=[1, 17, 40, 64, 300], num_heads=8,
+                              num_kv_heads=4, head_dim=128, block_size=16, kv_dtype="fp8")
+    rng = np.random.default_rng(34)
+    shape = b.key.shape
+    if dtype == "bf16":
+        key = workloads.f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(3.0))
+        value = workloads.f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(3.0))
+        as_f32 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).float()  # noqa: E731
+    else:
+        key = (rng.standard_normal(shape, dtype=np.float32) * np.float32(3.0)).astype(np.float16)
+        value = (rng.standard_normal(shape, dtype=np.float32) * np.float32(3.0)).astype(np.float16)
+        as_f32 = lambda a: torch.from_numpy(a).float()  # noqa: E731
+    ks, vs = float(np.float32(0.0371)), float(np.float32(0.123))
+    kc, vc = c_oracle.reshape_and_cache_fp8(key, value, b.k_cache, b.v_cache, b.slot_mapping, ks, vs, dtype=dtype)
+    for x, sc, pool, old in ((key, ks, kc, b.k_cache), (value, vs, vc, b.v_cache)):
+        q = as_f32(x) / torch.tensor(sc, dtype=torch.float32)
+        assert float(q.abs().max()) < 448.0
+        want = q.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        written = np.zeros(pool.shape[:2], dtype=bool)
+        for t, slot in enumerate(b.slot_mapping):
+            blk, off = divmod(int(slot), b.block_size)
+            assert np.array_equal(pool[blk, off], want[t]), (t, slot)
+            written[blk, off] = True
+        assert np.array_equal(pool[~written], old[~written])  # nothing else changed
+
+
 def test_copy_blocks_of_one_byte_pools_matches_the_numpy_statement():
     rng = np.random.default_rng(17)
     k = rng.integers(0, 256, (6, 16, 2, 64), dtype=np.uint8)

@@ -119,6 +119,10 @@ def append_ops(api, b):
                 out, q, key, value, kc, vc, bt, cl, b.scale, ps, ws, P, k_scale=ks, v_scale=vs))
 
 
+# kernel launches per step of each path (a call may launch more than one)
+LAUNCHES_PER_STEP = {"decode": 2, "splitk": 3, "append": 1, "append_splitk": 2, "prefix": 4}
+
+
 def decode_index(kernels) -> int:
     """Position of the decode launch in a path's kernel list."""
     return next(i for i, (n, _) in enumerate(kernels) if "decode" in n)
@@ -592,7 +596,7 @@ def run_gpu(args, rank: int, world: int):
                               else "the separate event pass (launches kept from overlapping)"),
             "isolated_frac": round(roof_bytes / (t_decode * 1e-3) / 1e9 / peak, 4),
         },
-        "gpu_launches": (len(kern) + (1 if best == "prefix" else 0)) * K,
+        "gpu_launches": LAUNCHES_PER_STEP[best] * K,
         "e2e": e2e,
         "clocks": r0["clocks"],
         "paths": summarize(m, world, K, peak),
@@ -617,7 +621,7 @@ def run_gpu(args, rank: int, world: int):
                      "clocks": mc["results"][bp]["clocks"], **per_path[bp],
                      "tokens_per_s": round(mc["b"].num_seqs * world / (mc["results"][bp]["ms"] / K * 1e-3), 1),
                      "paths": per_path}
-            launches += len(mc["paths"][bp]) * K
+            launches += LAUNCHES_PER_STEP[bp] * K
             res["configs"][name] = entry
             del mc
             torch.cuda.empty_cache()

@@ -1366,13 +1366,6 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
 #define PA_DECODE_STAGES 2
 #endif
 
-// E4M3 single launch: when positive, each CTA of a (sequence, KV head) covers
-// at most this many tokens of the table's capacity (a cluster of up to 8 CTAs
-// per pair); 0 keeps the occupancy-based choice.
-#ifndef PA_FP8_CLUSTER_TOKENS
-#define PA_FP8_CLUSTER_TOKENS 0
-#endif
-
 #ifndef PA_DECODE_FP8_WARPS
 #define PA_DECODE_FP8_WARPS 4
 #endif
@@ -1550,11 +1543,6 @@ cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
   int64_t k = pairs > 0 ? slots / pairs : 1;
   const int64_t cap = static_cast<int64_t>(a.max_blocks_per_seq) * a.block_size;
   k = std::min<int64_t>(k, (cap + 511) / 512);
-#if PA_FP8_CLUSTER_TOKENS > 0
-  // E4M3: a CTA's warps widen and score every chunk themselves, so one long
-  // sequence on one CTA can outlast the rest of the batch; clusters split it.
-  if (kIsFp8<KV>) k = std::max<int64_t>(k, (cap + PA_FP8_CLUSTER_TOKENS - 1) / PA_FP8_CLUSTER_TOKENS);
-#endif
   DecodeArgs b = a;
   b.cluster_size = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(8, k)));
   if (b.cluster_size == 1) {

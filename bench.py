@@ -761,6 +761,16 @@ def run_e2e(args, b, dev, reps, ws, P, kv_bytes, stream, path):
     ms_e, n_e, host_s = timed(lambda e0: (run(n, e0), n)[1])
     eager = {"value": round(kv_bytes * n_e / (ms_e * 1e-3) / 1e9, 1), "ms_per_step": round(ms_e / n_e, 5),
              "steps": n_e, "host_enqueue_us_per_step": round(host_s / n_e * 1e6, 2)}
+    # the host cost of the step's library calls alone (Python binding, ctypes, argument
+    # checks, launch), enqueued back to back with no copy and no event between them
+    calls = min(n, 500)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        t0 = time.perf_counter()
+        for i in range(calls):
+            kernels(i, staged[0].dev, outs[0])
+        eager["host_us_per_step_calls_only"] = round((time.perf_counter() - t0) / calls * 1e6, 2)
+    torch.cuda.synchronize(dev)
     res = {"unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
            "pipelining": "inputs of step i+1 copied in while step i computes; outputs copied out behind it",
            "eager": eager}

@@ -340,3 +340,25 @@ def test_copy_on_write_fork_then_decode():
     assert max_err(out, ref) <= TOL
     # the other samples still read the shared block, unchanged
     assert np.array_equal(kc.cpu().numpy()[shared_last].view(np.uint16), kc_h[shared_last].view(np.uint16))
+
+
+# ------------------------------------------------------------ maximum sizes
+def test_the_largest_batch_every_sequence():
+    # num_seqs at its limit (65535, the grid's z extent): every entry point, every sequence
+    rng = np.random.default_rng(61)
+    b = workloads.build_batch(name="max-batch", seed=61, rng=rng, context_lens=rng.integers(1, 33, size=65535),
+                              num_heads=8, num_kv_heads=1, head_dim=64, block_size=16)
+    assert b.num_seqs == 65535
+    ref = oracle_out(b)
+    d = Dev(b)
+    assert max_err(d.decode(), ref) <= TOL
+    assert max_err(d.splitk(16), ref) <= TOL
+    ref_k, ref_v = c_oracle.reshape_and_cache(b.key, b.value, b.k_cache, b.v_cache, b.slot_mapping)
+    assert np.array_equal(d.k_cache.cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
+    # the fused step on fresh pools: the same write and the same attention
+    kc, vc = T(b.k_cache), T(b.v_cache)
+    out = torch.empty_like(d.q)
+    api.pa_append_and_decode(out, d.q, T(b.key), T(b.value), kc, vc, d.bt, d.cl, b.scale)
+    assert max_err(out, ref) <= TOL
+    assert np.array_equal(kc.cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
+    assert np.array_equal(vc.cpu().numpy().view(np.uint16), ref_v.view(np.uint16))

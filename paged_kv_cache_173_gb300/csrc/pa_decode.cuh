@@ -48,6 +48,7 @@ namespace {
 
 constexpr unsigned FULL_MASK = 0xffffffffu;
 constexpr int CHUNK = 16;                       // tokens per pipeline stage
+constexpr int kLongestFirstMax = 256;           // batches the single launch ranks longest first
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000;  // 2 s: a stage that takes longer is an error
 
 // ================================================================ decode
@@ -94,7 +95,13 @@ struct DecodeParams {
   float v_scale;
 };
 
-enum DecodeMode { MODE_GRID = 0, MODE_CLUSTER = 1, MODE_SHARED = 2 };
+// MODE_LONGEST_FIRST: a single launch (one CTA per (KV head, sequence)) over
+// at most kLongestFirstMax sequences in which CTA z takes the sequence of
+// rank z in decreasing context length (ties by index), so that the CTAs left
+// for a second wave are the shortest.  Otherwise it is MODE_GRID.  (Llama-3-
+// 8B-shaped batch, 64 sequences x 8 KV heads on 456 slots: E4M3 fused step
+// 32.7 -> 29.8 us, fp16 decode 52.9 -> 51.9 us.)
+enum DecodeMode { MODE_GRID = 0, MODE_CLUSTER = 1, MODE_SHARED = 2, MODE_LONGEST_FIRST = 3 };
 
 // Tokens of a sequence that its group's shared pass covers: the group's
 // prefix length lp when it is a positive multiple of the partition size that
@@ -146,6 +153,7 @@ struct DecodeCfg {
   static constexpr int TAIL_BYTES = CTA_OFFSET + CTA_BYTES;
   static constexpr int BAR_BYTES = 1024;  // the ring that follows is 1024-byte aligned
   static_assert(WARPS * STAGES * 8 <= BAR_BYTES, "barrier area");
+  static_assert(RING_BYTES >= (kLongestFirstMax + 1) * 4, "the longest-first ranking fits in the ring");
   // + 1024 so that the ring can be aligned whatever the base alignment is
   static constexpr int SMEM_BYTES = 1024 + BAR_BYTES + (RING_BYTES > TAIL_BYTES ? RING_BYTES : TAIL_BYTES);
 };
@@ -681,6 +689,7 @@ template <typename T, typename KV, int HEAD_DIM, int NT, int WARPS, int STAGES, 
 __device__ __forceinline__ void decode_cta(const DecodeParams& p) {
   constexpr bool CLUSTER = MODE == MODE_CLUSTER;
   constexpr bool SHARED = MODE == MODE_SHARED;
+  constexpr bool LONGEST = MODE == MODE_LONGEST_FIRST;
   static_assert(!(APPEND && SHARED), "the shared pass does not write the cache");
   constexpr bool FP8 = kIsFp8<KV>;
   static_assert(!FP8 || std::is_same<T, __half>::value, "E4M3 caches take float16 queries");
@@ -729,13 +738,35 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p) {
     }
   } else {
     s = static_cast<int>(blockIdx.z);
+    if constexpr (LONGEST) {
+      // rank every context length against the others in shared memory (the
+      // ring is not in use yet); the thread whose sequence has rank z names it
+      int* lens = reinterpret_cast<int*>(ring);
+      int* pick = lens + kLongestFirstMax;
+      const int S = p.num_seqs;
+      for (int t = threadIdx.x; t < S; t += WARPS * 32) lens[t] = __ldg(p.context_lens + t);
+      __syncthreads();
+      for (int t = threadIdx.x; t < S; t += WARPS * 32) {
+        const int ct = lens[t];
+        int rank = 0;
+        for (int j = 0; j < S; ++j) {
+          const int cj = lens[j];
+          rank += (cj > ct) | ((cj == ct) & (j < t));
+        }
+        if (rank == s) *pick = t;
+      }
+      __syncthreads();
+      s = *pick;
+      ctx = lens[s];
+      __syncthreads();  // the ring is free again before any copy lands in it
+    }
     s0 = s;
     if (!CLUSTER && p.prefix_lens != nullptr) {
       const int gi = s / p.seqs_per_group;
       lp = __ldg(p.prefix_lens + gi);
       ctx_lead = __ldg(p.context_lens + gi * p.seqs_per_group);
     }
-    ctx = __ldg(p.context_lens + s);
+    if constexpr (!LONGEST) ctx = __ldg(p.context_lens + s);
   }
   const int cpb_log2 = p.chunks_per_block_log2;
   const int table_chunks = p.max_blocks_per_seq << cpb_log2;
@@ -803,7 +834,7 @@ __device__ __forceinline__ void decode_cta(const DecodeParams& p) {
     allow_dependent_launch();
     return;
   }
-  const bool single = MODE == MODE_GRID && nparts == 1;
+  const bool single = (MODE == MODE_GRID || LONGEST) && nparts == 1;
   const int c1 = CLUSTER ? cmax : min(c0 + p.partition_chunks, nchunks);
   const int nk = first < c1 ? (c1 - first + WARPS - 1) / WARPS : 0;  // <= nk_cap
 
@@ -1547,6 +1578,14 @@ cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
   b.cluster_size = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(8, k)));
   if (b.cluster_size == 1) {
     b.cluster_size = 0;
+    // A second wave of CTAs, but at most one: the longest sequences go in the
+    // first.  Over more waves the block scheduler balances by itself, and the
+    // ranking would scatter sequences that sit side by side in the batch and
+    // share blocks (samples of one prompt), whose reads L2 serves when their
+    // CTAs run together.
+    if (pairs > slots && pairs <= 2 * static_cast<int64_t>(slots) && a.num_seqs <= kLongestFirstMax &&
+        a.prefix_lens == nullptr)
+      return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_LONGEST_FIRST, false, APPEND>(b, stream);
     return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, false, APPEND>(b, stream);
   }
   return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER, false, APPEND>(b, stream);

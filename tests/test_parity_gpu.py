@@ -106,7 +106,17 @@ SMALL = {
     "gqa3-d64-b16": lambda: workloads.build_batch(name="g3", seed=6, context_lens=[17, 250, 31],
                                                   num_heads=9, num_kv_heads=3, head_dim=64,
                                                   block_size=16),
+    # 80 sequences x 8 KV heads: more CTAs than resident slots (456 at three
+    # per SM), at most twice as many, so pa_decode ranks the sequences
+    # longest first (the lengths repeat, so ties occur)
+    "ranked-s80": lambda: _ranked(),
 }
+
+
+def _ranked(seed=11):
+    ctx = np.random.default_rng(seed).choice([1, 2, 16, 17, 33, 100, 257, 300], size=80)
+    return workloads.build_batch(name="ranked", seed=seed, context_lens=ctx.tolist(), num_heads=32,
+                                 num_kv_heads=8, head_dim=128, block_size=16)
 
 
 @pytest.mark.parametrize("name", list(SMALL))
@@ -222,6 +232,25 @@ def test_device_value_outcomes():
         assert np.isnan(o[3]).all()
         for s in (0, 4):
             assert np.max(np.abs(o[s] - ref[s])) <= TOL
+
+
+def test_ranked_decode_device_value_outcomes():
+    # the longest-first launch puts each result in its own sequence's row,
+    # whatever rank its context length has (an impossible length ranks first)
+    b = _ranked(seed=12)
+    d = Dev(b)
+    ref = oracle_out(b)
+    cl = b.context_lens.copy()
+    cl[10] = 0
+    cl[20] = b.max_blocks_per_seq * b.block_size + 1
+    cl[30] = -4
+    bt = b.block_tables.copy()
+    bt[40, 0] = b.num_blocks + 7
+    o = d.decode(cl=T(cl), bt=T(bt)).float().cpu().numpy()
+    assert np.all(o[10] == 0)
+    assert np.isnan(o[20]).all() and np.isnan(o[30]).all() and np.isnan(o[40]).all()
+    keep = np.setdiff1d(np.arange(b.num_seqs), [10, 20, 30, 40])
+    assert np.max(np.abs(o[keep] - ref[keep])) <= TOL
 
 
 def _few_pairs(ctx, seed=7):

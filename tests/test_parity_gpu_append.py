@@ -166,6 +166,11 @@ def small(name, dtype="fp16", kv_dtype=""):
                                                          block_size=256, **kw),
         "d256-gqa4": lambda: workloads.build_batch(name="d256", seed=9, context_lens=[1, 200, 1500, 16, 17],
                                                    num_heads=16, num_kv_heads=4, head_dim=256, block_size=16, **kw),
+        # more (sequence, KV head) pairs than resident CTAs (three per SM at
+        # d = 128), but at most twice as many: the single launch ranks the
+        # sequences longest first; the lengths repeat
+        "ranked": lambda: workloads.build_batch(name="ranked", seed=11, context_lens=RANKED_CTX, num_heads=32,
+                                                num_kv_heads=8, head_dim=128, block_size=16, **kw),
         # few (sequence, KV head) pairs, large capacity: the single launch runs clusters
         "cluster": lambda: workloads.build_batch(name="few", seed=7, context_lens=[1, 5, 17, 100, 1000, 4096],
                                                  num_heads=4, num_kv_heads=1, head_dim=128, block_size=16,
@@ -174,7 +179,9 @@ def small(name, dtype="fp16", kv_dtype=""):
     return cases[name]()
 
 
-NAMES = ["tiny", "llama3-8b-s8", "llama2-70b-b32", "long-context-s", "gqa16-d128-b256", "d256-gqa4", "cluster"]
+RANKED_CTX = np.random.default_rng(11).choice([1, 2, 16, 17, 33, 100, 257, 300], size=80).tolist()
+NAMES = ["tiny", "llama3-8b-s8", "llama2-70b-b32", "long-context-s", "gqa16-d128-b256", "d256-gqa4", "ranked",
+         "cluster"]
 TYPES = [("fp16", ""), ("bf16", ""), ("fp16", "fp8")]
 
 

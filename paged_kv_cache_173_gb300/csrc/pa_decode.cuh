@@ -1403,6 +1403,18 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
 #ifndef PA_DECODE_FP8_STAGES
 #define PA_DECODE_FP8_STAGES 2
 #endif
+// the per-sequence (suffix) pass of the shared-prefix decode, up to d = 128
+#ifndef PA_SUFFIX_WARPS
+#define PA_SUFFIX_WARPS 2
+#endif
+#ifndef PA_SUFFIX_STAGES
+#define PA_SUFFIX_STAGES 2
+#endif
+
+// Launch kinds, each with its CTA shape: the single launch, the split-K
+// launch, and the two passes of the shared-prefix decode (the per-sequence
+// suffixes, the shared prefix).
+enum LaunchKind { KIND_SINGLE = 0, KIND_SPLITK = 1, KIND_SUFFIX = 2, KIND_SHARED = 3 };
 
 // CTA shape per head size: 4 warps x 2 stages (8 KB stages up to d = 128,
 // three CTAs per SM).  d = 256 has 16 KB stages and uses 2 warps x 1 stage,
@@ -1411,16 +1423,27 @@ cudaError_t ensure_smem(Kernel k, int bytes, std::atomic<uint64_t>& done_mask) {
 // 8x1 and 1-warp shapes were slower).  E4M3 stages are 8 KB for every head
 // size (two chunks up to d = 128), so E4M3 keeps 4 warps x 2 stages
 // throughout; sweeps over 2-8 warps and 1-4 stages found nothing faster.
-// PARTS: the split-K launch.  Its CTAs each cover one partition (at most
-// partition_size tokens), and at d = 128 one stage per warp (six CTAs per
-// SM) is faster there: llama3-8b 53.2 -> 52.6 us, long-context 227.0 ->
+// KIND_SPLITK: the split-K launch.  Its CTAs each cover one partition (at
+// most partition_size tokens), and at d = 128 one stage per warp (six CTAs
+// per SM) is faster there: llama3-8b 53.2 -> 52.6 us, long-context 227.0 ->
 // 217.9 us, 70B unchanged.  The single launch keeps two stages (with one it
-// lost 10-30%).
-template <int HEAD_DIM, int ELEM = 2, bool PARTS = false>
+// lost 10-30%).  KIND_SUFFIX: the per-sequence pass of the shared-prefix
+// decode, whose CTAs cover suffixes of a partition or less: 2 warps x 2
+// stages (six CTAs per SM) for both element types (shared-prefix batch:
+// E4M3 144.0 -> 124.6 us, fp16 179.7 -> 178.5 us; 2x1, 2x3, 3x2, 1x4 and
+// the split-K shapes were slower).  KIND_SHARED, the shared pass, keeps the
+// single launch's shape (4x1, 2x2 and 8x1 were slower).
+template <int HEAD_DIM, int ELEM = 2, int KIND = KIND_SINGLE>
 struct DecodeShape {
-  static constexpr int WARPS = ELEM == 1 ? PA_DECODE_FP8_WARPS : (HEAD_DIM > 128 ? 2 : PA_DECODE_WARPS);
-  static constexpr int STAGES = ELEM == 1 ? (HEAD_DIM > 128 ? 2 : PA_DECODE_FP8_STAGES)
-                                          : (HEAD_DIM > 128 || (PARTS && HEAD_DIM == 128) ? 1 : PA_DECODE_STAGES);
+  static constexpr bool FP8 = ELEM == 1;
+  static constexpr bool PARTS = KIND == KIND_SPLITK || KIND == KIND_SUFFIX;
+  static constexpr bool SUFFIX = KIND == KIND_SUFFIX && HEAD_DIM <= 128;
+  static constexpr int WARPS = SUFFIX ? PA_SUFFIX_WARPS
+                               : FP8  ? PA_DECODE_FP8_WARPS
+                                      : (HEAD_DIM > 128 ? 2 : PA_DECODE_WARPS);
+  static constexpr int STAGES = SUFFIX ? PA_SUFFIX_STAGES
+                                : FP8  ? (HEAD_DIM > 128 ? 2 : PA_DECODE_FP8_STAGES)
+                                       : (HEAD_DIM > 128 || (PARTS && HEAD_DIM == 128) ? 1 : PA_DECODE_STAGES);
 };
 
 template <typename T, typename KV, int HEAD_DIM>
@@ -1473,12 +1496,12 @@ int members_per_cta(const DecodeArgs& a) {
   return std::max(1, std::min(a.seqs_per_group, 8 * NT / G));
 }
 
-template <typename T, typename KV, int HEAD_DIM, int NT, int MODE, bool PARTS = false, bool APPEND = false>
+template <typename T, typename KV, int HEAD_DIM, int NT, int MODE, int KIND = KIND_SINGLE, bool APPEND = false>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   constexpr bool CLUSTER = MODE == MODE_CLUSTER;
   constexpr int ELEM = kElemBytes<KV>;
-  constexpr int WARPS = DecodeShape<HEAD_DIM, ELEM, PARTS>::WARPS;
-  constexpr int STAGES = DecodeShape<HEAD_DIM, ELEM, PARTS>::STAGES;
+  constexpr int WARPS = DecodeShape<HEAD_DIM, ELEM, KIND>::WARPS;
+  constexpr int STAGES = DecodeShape<HEAD_DIM, ELEM, KIND>::STAGES;
   using Cfg = DecodeCfg<HEAD_DIM, NT, WARPS, STAGES, ELEM>;
   auto kern = [] {
     if constexpr (APPEND) {
@@ -1563,9 +1586,9 @@ cudaError_t decode_slots(int* slots) {
 template <typename T, typename KV, int HEAD_DIM, int NT, bool APPEND = false>
 cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
   if (a.cluster_size >= 0) {
-    if (a.cluster_size > 0) return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER, false, APPEND>(a, stream);
-    return a.ws != nullptr ? launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, true, APPEND>(a, stream)
-                           : launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, false, APPEND>(a, stream);
+    if (a.cluster_size > 0) return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER, KIND_SINGLE, APPEND>(a, stream);
+    return a.ws != nullptr ? launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, KIND_SPLITK, APPEND>(a, stream)
+                           : launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, KIND_SINGLE, APPEND>(a, stream);
   }
   int slots = 0;
   cudaError_t e = decode_slots<T, KV, HEAD_DIM, NT>(&slots);
@@ -1585,10 +1608,10 @@ cudaError_t launch_decode_auto(const DecodeArgs& a, cudaStream_t stream) {
     // CTAs run together.
     if (pairs > slots && pairs <= 2 * static_cast<int64_t>(slots) && a.num_seqs <= kLongestFirstMax &&
         a.prefix_lens == nullptr)
-      return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_LONGEST_FIRST, false, APPEND>(b, stream);
-    return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, false, APPEND>(b, stream);
+      return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_LONGEST_FIRST, KIND_SINGLE, APPEND>(b, stream);
+    return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, KIND_SINGLE, APPEND>(b, stream);
   }
-  return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER, false, APPEND>(b, stream);
+  return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_CLUSTER, KIND_SINGLE, APPEND>(b, stream);
 }
 
 template <typename T, int HEAD_DIM>
@@ -1662,9 +1685,9 @@ cudaError_t launch_decode_typed(const DecodeArgs& a, cudaStream_t stream) {
 // 187.8 -> 179.7 us per step).
 template <typename T, typename KV, int HEAD_DIM, int NTS, int NT>
 cudaError_t launch_prefix_t(const DecodeArgs& a, cudaStream_t stream) {
-  cudaError_t e = launch_decode_t<T, KV, HEAD_DIM, NTS, MODE_SHARED>(a, stream);
+  cudaError_t e = launch_decode_t<T, KV, HEAD_DIM, NTS, MODE_SHARED, KIND_SHARED>(a, stream);
   if (e != cudaSuccess) return e;
-  return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, true>(a, stream);
+  return launch_decode_t<T, KV, HEAD_DIM, NT, MODE_GRID, KIND_SUFFIX>(a, stream);
 }
 
 template <typename T, typename KV = T>

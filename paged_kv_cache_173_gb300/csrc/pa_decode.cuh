@@ -1642,9 +1642,13 @@ cudaError_t launch_reduce_t(const ReduceArgs& a, cudaStream_t stream) {
   } else if (a.max_num_partitions <= 32) {  // one warp per (sequence, head)
     cfg.gridDim = dim3((a.num_heads + 7) / 8, a.num_seqs);
     e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<T, HEAD_DIM, 1>, p);
-  } else {  // four warps per (sequence, head)
+  } else if (a.max_num_partitions <= 64) {  // four warps per (sequence, head)
     cfg.gridDim = dim3((a.num_heads + 1) / 2, a.num_seqs);
     e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<T, HEAD_DIM, 4>, p);
+  } else {  // eight warps per (sequence, head): fewer serial round trips per warp
+            // (long context, 256 partitions: step 216.5 -> 209.4 us)
+    cfg.gridDim = dim3(a.num_heads, a.num_seqs);
+    e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<T, HEAD_DIM, 8>, p);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

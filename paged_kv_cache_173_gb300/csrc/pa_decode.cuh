@@ -1200,14 +1200,19 @@ __global__ void __launch_bounds__(256) splitk_reduce_small_kernel(const __grid_c
 
 // Warps per (sequence, head): WPH warps split the partitions (q = sub, sub +
 // WPH, ...); each lane owns HEAD_DIM / 32 consecutive output dims and reads
-// them as one vector per partition.  A CTA has 8 warps = 8 / WPH heads.
+// them as one vector per partition.  A CTA has 8 warps = 8 / WPH heads, or
+// 16 warps for one head when WPH = 16.
+template <int WPH>
+constexpr int reduce_warps() { return WPH > 8 ? WPH : 8; }
+
 template <typename T, int HEAD_DIM, int WPH>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(reduce_warps<WPH>() * 32) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
   constexpr int VEC = HEAD_DIM / 32;
-  constexpr int HPC = 8 / WPH;
+  constexpr int NW = reduce_warps<WPH>();
+  constexpr int HPC = NW / WPH;
   using VecT = FVec<VEC>;
-  __shared__ float sm_m[8], sm_l[8];
-  __shared__ VecT sm_o[8][32];
+  __shared__ float sm_m[NW], sm_l[NW];
+  __shared__ VecT sm_o[NW][32];
   grid_dependency_wait();  // the partitions come from the decode kernel just before
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1645,10 +1650,15 @@ cudaError_t launch_reduce_t(const ReduceArgs& a, cudaStream_t stream) {
   } else if (a.max_num_partitions <= 64) {  // four warps per (sequence, head)
     cfg.gridDim = dim3((a.num_heads + 1) / 2, a.num_seqs);
     e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<T, HEAD_DIM, 4>, p);
-  } else {  // eight warps per (sequence, head): fewer serial round trips per warp
-            // (long context, 256 partitions: step 216.5 -> 209.4 us)
+  } else if (a.max_num_partitions <= 128) {  // eight warps per (sequence, head): fewer serial
+                                             // round trips per warp
     cfg.gridDim = dim3(a.num_heads, a.num_seqs);
     e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<T, HEAD_DIM, 8>, p);
+  } else {  // sixteen warps per (sequence, head), one head per CTA (long context, 256
+            // partitions: step 216.5 us with four warps, 209.5 with eight, 207.5 with sixteen)
+    cfg.gridDim = dim3(a.num_heads, a.num_seqs);
+    cfg.blockDim = dim3(16 * 32);
+    e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<T, HEAD_DIM, 16>, p);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
